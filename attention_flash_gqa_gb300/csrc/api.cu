@@ -1,0 +1,277 @@
+// C ABI of the attention library (declared in include/attn.h): argument checks,
+// workspace layout, TMA tensor maps and kernel launches. No allocation, no host
+// synchronisation except in attn_get_device_status().
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace {
+
+// [0]: fault flags; [1]: id of the first pipeline wait that gave up (0 = none).
+__device__ unsigned g_attn_status[2] = {0u, 0u};
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct DeviceInfo {
+    bool init = false;
+    bool ok = false;
+    int sms = 0;
+    unsigned* status = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+
+// Per-device facts, queried once: sm_103, SM count, address of the status word.
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.init) {
+        d.init = true;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        void* p = nullptr;
+        const bool sym = cudaGetSymbolAddress(&p, g_attn_status) == cudaSuccess;
+        d.status = static_cast<unsigned*>(p);
+        d.ok = major == 10 && minor == 3 && sym && d.sms > 0;
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                    cudaSuccess &&
+                q == cudaDriverEntryPointSuccess)
+                g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        if (!g_encode) d.ok = false;
+    }
+    return d.ok ? &d : nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D map over a [batch, rows, heads, dim] bf16 tensor, box = 64 dims x 1 head x 128 rows.
+bool make_map(CUtensorMap* m, const void* base, int D, int H, int rows, int batch) {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)rows * H * D * 2};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_common(int Hq, int Hkv, float scale, int causal, int window) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    if (window < 0) return ATTN_ERR_INVALID_ARG;
+    if (causal != 1) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+int check_prefill_shape(long long rows, int Hq, int Hkv, int D, int S) {
+    if (D != 256 && D != 512) return ATTN_ERR_UNSUPPORTED;
+    if (S > 65535LL * 128) return ATTN_ERR_UNSUPPORTED;
+    if (rows > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;  // TMA row coordinates are int32
+    (void)Hq, (void)Hkv;
+    return ATTN_OK;
+}
+
+size_t bwd_ws(long long rows, int Hq, int D) {
+    return align256((size_t)rows * Hq * D * 4) + align256((size_t)rows * Hq * 4);
+}
+
+size_t decode_ws(int B, int Hq, int D) {
+    return align256((size_t)B * 4) + align256((size_t)(B + attn::decode_max_grid()) * Hq * attn::decode_row_floats() * 4);
+}
+
+int fwd_common(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
+               const int32_t* cu, int nseq, int S, long long rows, int batch_dim, int Hq, int Hkv, int D, float scale,
+               int window, void* stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    attn::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const int map_rows = (int)(cu ? rows : S);
+    if (!make_map(&L.tq, q, D, Hq, map_rows, batch_dim) || !make_map(&L.tk, k, D, Hkv, map_rows, batch_dim) ||
+        !make_map(&L.tv, v, D, Hkv, map_rows, batch_dim))
+        return ATTN_ERR_LAUNCH;
+    L.o = o, L.lse = lse, L.cu_seqlens = cu, L.status = dev->status;
+    L.nseq = nseq, L.Hq = Hq, L.Hkv = Hkv, L.S = S, L.D = D, L.total_rows = (int)rows, L.window = window;
+    L.scale = scale;
+    return attn::launch_fwd(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_version(void) { return 100; }
+
+const char* attn_status_string(int s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+        case ATTN_ERR_LAUNCH: return "ATTN_ERR_LAUNCH";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+        case ATTN_ERR_DEVICE_BOUNDS: return "ATTN_ERR_DEVICE_BOUNDS";
+        case ATTN_ERR_NO_DEVICE: return "ATTN_ERR_NO_DEVICE";
+        default: return "ATTN_ERR_UNKNOWN";
+    }
+}
+
+size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D, int num_seqs, int max_pages_per_seq) {
+    (void)Hkv, (void)num_seqs, (void)max_pages_per_seq;
+    if (B < 0 || Hq < 0 || S < 0 || D < 0) return 0;
+    switch (op) {
+        case ATTN_OP_FWD:
+        case ATTN_OP_FWD_VARLEN: return 0;
+        case ATTN_OP_BWD:
+        case ATTN_OP_BWD_VARLEN: return bwd_ws((long long)B * S, Hq, D);
+        case ATTN_OP_DECODE_PAGED: return decode_ws(B, Hq, D);
+        default: return 0;
+    }
+}
+
+int attn_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float scale, int causal, int window, void* workspace, size_t workspace_bytes,
+             void* stream) {
+    (void)workspace, (void)workspace_bytes;
+    if (!q || !k || !v || !o || !lse || B < 0 || S < 0) return ATTN_ERR_INVALID_ARG;
+    int st = check_common(Hq, Hkv, scale, causal, window);
+    if (st) return st;
+    const long long rows = (long long)B * S;
+    if ((st = check_prefill_shape(rows, Hq, Hkv, D, S))) return st;
+    if (B > 65535 / (D / 256)) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+    if (rows == 0) return ATTN_OK;
+    return fwd_common(q, k, v, o, lse, nullptr, B, S, rows, B, Hq, Hkv, D, scale, window, stream);
+}
+
+int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
+                    const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
+                    float scale, int causal, int window, void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace, (void)workspace_bytes;
+    if (!q || !k || !v || !o || !lse || !cu_seqlens || num_seqs < 0 || total_tokens < 0 || max_seqlen < 0)
+        return ATTN_ERR_INVALID_ARG;
+    int st = check_common(Hq, Hkv, scale, causal, window);
+    if (st) return st;
+    if ((st = check_prefill_shape(total_tokens, Hq, Hkv, D, max_seqlen))) return st;
+    if (num_seqs > 65535 / (D / 256)) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
+    if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
+    return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, 1, Hq, Hkv, D, scale, window,
+                      stream);
+}
+
+int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const attn_bf16* o, const float* lse,
+             const attn_bf16* dO, attn_bf16* dQ, attn_bf16* dK, attn_bf16* dV, int B, int Hq, int Hkv, int S, int D,
+             float scale, int causal, int window, const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
+             void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k || !v || !o || !lse || !dO || !dQ || !dK || !dV || B < 0 || S < 0) return ATTN_ERR_INVALID_ARG;
+    int st = check_common(Hq, Hkv, scale, causal, window);
+    if (st) return st;
+    const bool varlen = cu_seqlens != nullptr;
+    if (varlen && (B != 1 || num_seqs < 0 || max_seqlen < 0)) return ATTN_ERR_INVALID_ARG;
+    const long long rows = (long long)B * S;
+    const int grid_len = varlen ? max_seqlen : S;
+    if ((st = check_prefill_shape(rows, Hq, Hkv, D, grid_len))) return st;
+    if ((varlen ? num_seqs : B) > 65535) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
+        !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
+        return ATTN_ERR_MISALIGNED;
+    const size_t need = bwd_ws(rows, Hq, D);
+    if (rows > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
+    if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u)) return ATTN_ERR_MISALIGNED;
+    if (rows == 0 || (varlen && (num_seqs == 0 || max_seqlen == 0))) return ATTN_OK;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    attn::BwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const int map_rows = varlen ? (int)rows : S, batch = varlen ? 1 : B;
+    if (!make_map(&L.tq, q, D, Hq, map_rows, batch) || !make_map(&L.tk, k, D, Hkv, map_rows, batch) ||
+        !make_map(&L.tv, v, D, Hkv, map_rows, batch) || !make_map(&L.tdo, dO, D, Hq, map_rows, batch))
+        return ATTN_ERR_LAUNCH;
+    L.q = q, L.k = k, L.v = v, L.o = o, L.dO = dO, L.lse = lse, L.dQ = dQ, L.dK = dK, L.dV = dV;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    L.dq_acc = reinterpret_cast<float*>(ws);
+    L.delta = reinterpret_cast<float*>(ws + align256((size_t)rows * Hq * D * 4));
+    L.cu_seqlens = cu_seqlens, L.status = dev->status;
+    L.nseq = varlen ? num_seqs : B;
+    L.Hq = Hq, L.Hkv = Hkv, L.S = grid_len, L.D = D, L.total_rows = (int)rows, L.window = window, L.scale = scale;
+    return attn::launch_bwd(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
+                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || max_pages_per_seq < 0 || num_pages < 0 || page_size <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (D != 128 || page_size != 16 || Hkv > 8 || (G != 1 && G != 2 && G != 4 && G != 8) || B > 4096)
+        return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    if (B == 0) return ATTN_OK;
+    if (!workspace || workspace_bytes < decode_ws(B, Hq, D)) return ATTN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    attn::DecodeLaunch L;
+    L.q = q, L.k_cache = k_cache, L.v_cache = v_cache, L.block_table = block_table, L.seq_lens = seq_lens;
+    L.o = o, L.lse = lse, L.status = dev->status;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    L.counters = reinterpret_cast<int32_t*>(ws);
+    L.part = reinterpret_cast<float*>(ws + align256((size_t)B * 4));
+    L.B = B, L.Hq = Hq, L.Hkv = Hkv, L.max_pages = max_pages_per_seq, L.num_pages = num_pages, L.scale = scale;
+    long long units = (long long)B * (max_pages_per_seq > 0 ? max_pages_per_seq : 1);
+    int grid = dev->sms < attn::decode_max_grid() ? dev->sms : attn::decode_max_grid();
+    if (units < grid) grid = (int)units;
+    L.grid = grid < 1 ? 1 : grid;
+    return attn::launch_decode_paged(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int attn_get_device_status(void* stream) {
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+    unsigned words[2] = {0u, 0u}, zero[2] = {0u, 0u};
+    if (cudaMemcpyFromSymbol(words, g_attn_status, sizeof(words)) != cudaSuccess) return ATTN_ERR_LAUNCH;
+    if ((words[0] || words[1]) && cudaMemcpyToSymbol(g_attn_status, zero, sizeof(zero)) != cudaSuccess)
+        return ATTN_ERR_LAUNCH;
+    const unsigned flags = words[0];
+    if (flags && std::getenv("ATTN_DEBUG"))
+        std::fprintf(stderr, "attn: device status flags=0x%x first timed-out wait site=0x%x\n", flags, words[1]);
+    if (flags & attn::DEVSTAT_TIMEOUT) return ATTN_ERR_DEVICE_TIMEOUT;
+    if (flags & attn::DEVSTAT_BOUNDS) return ATTN_ERR_DEVICE_BOUNDS;
+    return ATTN_OK;
+}
+
+}  // extern "C"

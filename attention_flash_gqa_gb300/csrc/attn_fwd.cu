@@ -1,0 +1,380 @@
+// Causal / sliding-window attention forward on tcgen05 tensor cores (D = 256 or 512).
+//
+// Sources: "Gemma4 FFPA attention backend support ..." (operator table: fused
+// attention instead of the MATH path that materialises S x S; "Integration": head_dim
+// 512 causal attention, dense and varlen paths), and the sliding-window head_dim 256
+// layers of "Root cause analysis: Gemma4 sliding-window BF16 cuDNN SDPA NaN on H100".
+//
+// One CTA computes a 128-query tile of one head against all keys it may see, for one
+// 256-wide half of the output columns (D = 512 runs two CTAs per tile, each recomputing
+// the full-width scores; D = 256 runs one). Tensor memory (512 columns x 128 lanes):
+//   cols [0, 256)   O accumulator, fp32, row i = lane i
+//   cols [256, 384) S buffer 0, [384, 512) S buffer 1 (double-buffered scores)
+// Shared memory: the Q tile (resident), a ring of 32 KB slots (one slot = 128 rows x
+// 128 columns of K or V as two 128-byte-swizzled 64-column sub-tiles, filled by TMA),
+// and the bf16 P tile written by the softmax warps.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one thread): Q once, then K/V slots in MMA order
+//   warp 1      TMEM owner; one thread issues every UMMA and commit
+//   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Masking, fp32 online
+//               softmax in the log2 domain with lazy rescaling (the running max moves
+//               only when a tile's max exceeds it by more than 2^8), P -> smem, O
+//               rescale in TMEM, and the epilogue (O / l -> bf16, lse).
+// KV tiles outside the causal / window range are never loaded (tile-granular skipping);
+// only tiles that straddle the diagonal, the window edge or the sequence end are masked.
+#include <cuda_runtime.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBQ = 128, kBKV = 128, kDV = 256;
+constexpr int kThreads = 192;
+constexpr uint32_t kSlotBytes = 32768;
+constexpr uint32_t kSubBytes = 16384;  // 128 rows x 64 bf16
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int DQK>
+struct FwdCfg {
+    static constexpr int kQChunks = DQK / 128;  // 32 KB slots per K tile
+    static constexpr int kVChunks = kDV / 128;  // 32 KB slots per V half-tile
+    static constexpr int kStages = DQK == 256 ? 4 : 2;
+    static constexpr uint32_t kQBytes = DQK * 256;  // 128 rows x DQK bf16
+    static constexpr uint32_t kOffSlots = kQBytes;
+    static constexpr uint32_t kOffP = kOffSlots + kStages * kSlotBytes;
+    static constexpr uint32_t kOffBar = kOffP + kSlotBytes;
+    static constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
+};
+
+struct FwdArgs {
+    uint16_t* o;
+    float* lse;
+    const int32_t* cu_seqlens;
+    unsigned* status;
+    int Hq, Hkv, S, D, window, n_qtiles, nsplit, T;
+    float scale_log2;
+};
+
+template <int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+               const __grid_constant__ CUtensorMap tv, FwdArgs a) {
+    using C = FwdCfg<DQK>;
+    // ---- which tile ------------------------------------------------------------------
+    const int h = blockIdx.x;
+    const int seq = blockIdx.y / a.nsplit, split = blockIdx.y % a.nsplit;
+    const int q_tile = a.n_qtiles - 1 - (int)blockIdx.z;  // longest tiles first
+    int seq_start = 0, L = a.S, bcoord = seq;
+    if (a.cu_seqlens) {
+        seq_start = a.cu_seqlens[seq];
+        L = a.cu_seqlens[seq + 1] - seq_start;
+        bcoord = 0;
+    }
+    const int q0 = q_tile * kBQ;
+    if (q0 >= L) return;  // uniform: before any barrier or TMEM use
+    const int g = h / (a.Hq / a.Hkv);
+    const int dv0 = split * kDV;
+    const int kv_hi = min(L, q0 + kBQ);
+    const int kv_lo = a.window > 0 ? max(0, q0 - a.window + 1) : 0;
+    const int t_begin = kv_lo / kBKV, t_end = (kv_hi + kBKV - 1) / kBKV;
+    const int n = t_end - t_begin;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase, sSlots = sbase + C::kOffSlots, sP = sbase + C::kOffP;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;                     // [kStages]
+    uint64_t* empty = bars + C::kStages;       // [kStages]
+    uint64_t* q_full = bars + 2 * C::kStages;  // 1
+    uint64_t* s_full = q_full + 1;             // [2]
+    uint64_t* p_full = s_full + 2;             // 1
+    uint64_t* pv_done = p_full + 1;            // 1
+    uint64_t* mma_idle = pv_done + 1;          // 1
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(q_full), 1);
+        mbar_init(smem_u32(&s_full[0]), 1);
+        mbar_init(smem_u32(&s_full[1]), 1);
+        mbar_init(smem_u32(p_full), 128);
+        mbar_init(smem_u32(pv_done), 1);
+        mbar_init(smem_u32(mma_idle), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tO = tbase, tS0 = tbase + 256;
+
+    if (warp == 0) {
+        // ------------------------------- TMA producer ----------------------------------
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            const int row_q = seq_start + q0;
+            mbar_expect_tx(smem_u32(q_full), C::kQBytes);
+            for (int c = 0; c < DQK / 64; ++c)
+                tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, row_q, bcoord);
+            int slot = 0, round = 0;
+            bool ok = true;
+            auto load_chunk = [&](const CUtensorMap* map, int col0, int row0) -> bool {
+                if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x11)) return false;
+                const uint32_t fb = smem_u32(&full[slot]);
+                mbar_expect_tx(fb, kSlotBytes);
+                const uint32_t dst = sSlots + slot * kSlotBytes;
+                tma_load_4d(dst, map, fb, col0, g, row0, bcoord);
+                tma_load_4d(dst + kSubBytes, map, fb, col0 + 64, g, row0, bcoord);
+                if (++slot == C::kStages) slot = 0, ++round;
+                return true;
+            };
+            auto load_k = [&](int t) -> bool {
+                for (int c = 0; c < C::kQChunks; ++c)
+                    if (!load_chunk(&tk, c * 128, seq_start + (t_begin + t) * kBKV)) return false;
+                return true;
+            };
+            auto load_v = [&](int t) -> bool {
+                for (int c = 0; c < C::kVChunks; ++c)
+                    if (!load_chunk(&tv, dv0 + c * 128, seq_start + (t_begin + t) * kBKV)) return false;
+                return true;
+            };
+            ok = load_k(0);
+            if (ok && n > 1) ok = load_k(1);
+            for (int j = 0; ok && j < n; ++j) {
+                ok = load_v(j);
+                if (ok && j + 2 < n) ok = load_k(j + 2);
+            }
+            // Drain: wait (bounded) for the last copy issued into every slot.
+            const int issued = round * C::kStages + slot;
+            for (int s = 0; s < C::kStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x18);
+            }
+            mbar_drain(smem_u32(q_full), 0, a.status, 0x19);
+        }
+    } else if (warp == 1) {
+        // ------------------------------- UMMA issuer -----------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // Q K^T: both K-major
+            constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);   // P V: V is N-major
+            int slot = 0, round = 0;
+            bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.status, 0x12);
+            tc_fence_after();
+            auto next_slot = [&]() -> bool {
+                if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x13)) return false;
+                tc_fence_after();
+                return true;
+            };
+            auto release_slot = [&]() {
+                umma_commit(smem_u32(&empty[slot]));
+                if (++slot == C::kStages) slot = 0, ++round;
+            };
+            auto issue_s = [&](int buf) -> bool {
+                const uint32_t dst = tS0 + buf * 128;
+                for (int c = 0; c < C::kQChunks; ++c) {
+                    if (!next_slot()) return false;
+                    const uint32_t kslot = sSlots + slot * kSlotBytes;
+                    for (int sub = 0; sub < 2; ++sub)
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sdesc_sw128(sQ + (2 * c + sub) * kSubBytes + kk * 32, 16, 1024);
+                            const uint64_t bd = sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
+                            umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
+                        }
+                    release_slot();
+                }
+                umma_commit(smem_u32(&s_full[buf]));
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                for (int c = 0; c < C::kVChunks; ++c) {
+                    if (!next_slot()) return false;
+                    const uint32_t vslot = sSlots + slot * kSlotBytes;
+                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
+                        const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
+                        umma_bf16_ss(tO + c * 128, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    release_slot();
+                }
+                umma_commit(smem_u32(pv_done));
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            if (ok && n > 1) ok = issue_s(1);
+            for (int j = 0; ok && j < n; ++j) {
+                ok = mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.status, 0x14);
+                if (!ok) break;
+                tc_fence_after();
+                ok = issue_pv(j);
+                if (ok && j + 2 < n) ok = issue_s(j & 1);
+            }
+            // every issued UMMA has finished before TMEM may be released
+            umma_commit(smem_u32(mma_idle));
+            mbar_drain(smem_u32(mma_idle), 0, a.status, 0x1a);
+        }
+    } else {
+        // --------------------------------- softmax --------------------------------------
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // query row within the tile == TMEM lane
+        const int qi = q0 + r;           // query index within the sequence
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            const int buf = j & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[buf]), (j >> 1) & 1, abort_flag, a.status, 0x15));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tS0 + buf * 128 + c * 32 + lane_base, raw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[e]);
+            }
+            const int key0 = (t_begin + j) * kBKV;
+            const bool edge = (key0 + kBKV - 1 > q0) || (a.window > 0 && q0 + kBQ - 1 - key0 >= a.window) ||
+                              (key0 + kBKV > L);
+            if (edge) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = key0 + c;
+                    const bool allowed = key <= qi && key < L && (a.window <= 0 || qi - key < a.window);
+                    if (!allowed) s[c] = -INFINITY;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            const float m_tile = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
+            float alpha = 1.f;
+            const bool moved = m_tile > m_ref + kRescaleLog2;
+            if (moved) {
+                alpha = m_ref == -INFINITY ? 0.f : fast_exp2(m_ref - m_tile);
+                m_ref = m_tile;
+            }
+            const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+            float rowsum = 0.f;
+            uint32_t pk[64];
+#pragma unroll
+            for (int c = 0; c < 128; c += 2) {
+                const float p0 = fast_exp2(fmaf(s[c], a.scale_log2, -m_use));
+                const float p1 = fast_exp2(fmaf(s[c + 1], a.scale_log2, -m_use));
+                rowsum += p0 + p1;
+                pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + rowsum;
+            if (j > 0) {
+                // P(j-1) V(j-1) must be complete: it reads sP and writes O
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done), (j - 1) & 1, abort_flag, a.status, 0x16));
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, moved)) {
+                    const float f = moved ? alpha : 1.f;
+#pragma unroll 1
+                    for (int c = 0; c < kDV / 32; ++c) {
+                        uint32_t raw[32];
+                        tmem_ld32(tO + c * 32 + lane_base, raw);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+                        tmem_st32(tO + c * 32 + lane_base, raw);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            // P row r -> sP (K-major, 128-byte swizzle): 16 chunks of 8 keys
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const uint32_t addr = sP + (u >> 3) * kSubBytes + sw128_offset(r, (u & 7) * 8);
+                st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(p_full));
+        }
+        // ---- epilogue: O / l -> bf16, lse -------------------------------------------------
+        if (ok) ok = mbar_wait(smem_u32(pv_done), (n - 1) & 1, abort_flag, a.status, 0x17);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_after();
+        if (ok) {
+            const bool row_ok = qi < L;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint16_t* orow = a.o + ((size_t)(a.cu_seqlens ? seq_start + qi : seq * a.S + qi) * a.Hq + h) * a.D + dv0;
+#pragma unroll 1
+            for (int c = 0; c < kDV / 32; ++c) {
+                uint32_t raw[32];
+                tmem_ld32(tO + c * 32 + lane_base, raw);
+                tmem_ld_wait();
+                if (row_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(raw[e]) * inv, __uint_as_float(raw[e + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(raw[e + 2]) * inv, __uint_as_float(raw[e + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(raw[e + 4]) * inv, __uint_as_float(raw[e + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(raw[e + 6]) * inv, __uint_as_float(raw[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+                    }
+                }
+            }
+            if (row_ok && split == 0) {
+                const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+                const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qi : ((size_t)seq * a.Hq + h) * a.S + qi;
+                a.lse[li] = lse;
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+template <int DQK>
+cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
+    using C = FwdCfg<DQK>;
+    FwdArgs a;
+    a.o = L.o, a.lse = L.lse, a.cu_seqlens = L.cu_seqlens, a.status = L.status;
+    a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.D = L.D, a.window = L.window;
+    a.n_qtiles = (L.S + kBQ - 1) / kBQ;
+    a.nsplit = DQK / kDV;
+    a.T = L.total_rows;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(L.Hq, L.nseq * a.nsplit, a.n_qtiles);
+    fwd_kernel<DQK><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
+    if (L.nseq == 0 || L.S == 0) return cudaSuccess;
+    if (L.D == 256) return launch_fwd_t<256>(L, stream);
+    if (L.D == 512) return launch_fwd_t<512>(L, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,173 @@
+/*
+ * attn.h -- C ABI of a fused flash-style attention library for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (the plain definition; the kernels reach it without ever forming
+ * the S x S score matrix):
+ *
+ *   s_ij = scale * q_i . k_j                      (query head h reads KV head h / (Hq/Hkv))
+ *   allowed(i,j) = j <= i  and  (window <= 0  or  i - j < window)
+ *   o_i = sum_j softmax_j(s_ij | allowed) v_j,    lse_i = ln sum_{allowed j} exp(s_ij)
+ *
+ * with bf16 inputs/outputs, fp32 accumulation and an fp32 log-sum-exp per query row.
+ * Passages that define the operation (web pages, by title and section):
+ *  - "Gemma4 FFPA attention backend support for accelerating Gemma4-family training"
+ *    (NeMo-Automodel discussion 2928): the operator table (fused attention replaces
+ *    the MATH path that materialises S x S), "Integration" (head_dim 512 causal full
+ *    attention; a 2-D padding mask is served by a varlen path; non-null scale; no
+ *    dropout, no softcap) and "Debugging notes" (GQA as repeat-KV).
+ *  - "Root cause analysis: Gemma4 sliding-window BF16 cuDNN SDPA NaN on H100"
+ *    (NeMo-Automodel issue 3232), "Summary" and "Debug and validation results":
+ *    head_dim 256 sliding-window attention whose backward must stay finite in bf16.
+ *  - "flex_attention + paged KV + CUDA graphs vs vLLM", "What each option did" and
+ *    "Architecture notes": single-token decode over a paged KV cache addressed by a
+ *    block table; "What broke correctness": rows with no allowed key must not NaN.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or retains them. They must be 16-byte aligned, contiguous, and
+ *    live until the work queued on `stream` completes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Calls only enqueue work: they return before the GPU finishes and never
+ *    synchronise the device.
+ *  - Arguments are checked on the host before anything is launched; on a bad
+ *    argument nothing is enqueued and an attn_status code is returned. Nothing
+ *    throws across this interface.
+ *  - Faults detected on the device (a page id outside the pool, a pipeline wait that
+ *    exceeded its time limit) do not trap: the kernel records a flag and finishes,
+ *    and attn_get_device_status() reports it.
+ *  - Supported shapes: D in {256, 512} for prefill/backward (D = 128 for decode),
+ *    Hq % Hkv == 0, causal = 1. bf16 values are passed as raw 16-bit patterns.
+ */
+#ifndef ATTN_GB300_ATTN_H
+#define ATTN_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t attn_bf16; /* raw bf16 bit pattern */
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* null pointer, negative size, Hq % Hkv != 0, bad scale ... */
+    ATTN_ERR_UNSUPPORTED = 2,    /* a legal problem this build has no kernel for (e.g. D = 64) */
+    ATTN_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
+    ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than attn_workspace_size() */
+    ATTN_ERR_LAUNCH = 5,         /* the CUDA runtime refused a launch or a tensor map */
+    ATTN_ERR_DEVICE_TIMEOUT = 6, /* a kernel pipeline wait gave up (reported by attn_get_device_status) */
+    ATTN_ERR_DEVICE_BOUNDS = 7,  /* a device-side index (page id, length) was out of range */
+    ATTN_ERR_NO_DEVICE = 8       /* no usable sm_103 device is current */
+} attn_status;
+
+/* Operation codes for attn_workspace_size(). */
+enum {
+    ATTN_OP_FWD = 0,
+    ATTN_OP_FWD_VARLEN = 1,
+    ATTN_OP_BWD = 2,
+    ATTN_OP_BWD_VARLEN = 3,
+    ATTN_OP_DECODE_PAGED = 4
+};
+
+/*
+ * attn_fwd -- causal (optionally sliding-window) attention forward, dense batch.
+ *   q   [B, S, Hq,  D] bf16      k, v [B, S, Hkv, D] bf16      (BSHD, contiguous)
+ *   o   [B, S, Hq,  D] bf16 out  lse  [B, Hq, S] fp32 out, natural log
+ *   scale: finite and > 0 (typically 1/sqrt(D)); causal must be 1; window <= 0 means no
+ *   window, otherwise query i sees keys i-window+1 .. i.
+ *   workspace: may be NULL (the forward needs none; attn_workspace_size returns 0).
+ * Defined by the Gemma4 FFPA page, "Integration" (dense no-mask path) and the
+ * sliding-window layers of the issue-3232 page.
+ */
+ATTN_API int attn_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse, int B, int Hq,
+             int Hkv, int S, int D, float scale, int causal, int window, void* workspace, size_t workspace_bytes,
+             void* stream);
+
+/*
+ * attn_fwd_varlen -- the same forward over packed sequences (the varlen path that
+ * replaces a 2-D bool padding mask: Gemma4 FFPA page, "Integration").
+ *   q [T, Hq, D], k, v [T, Hkv, D], o [T, Hq, D] bf16; lse [Hq, T] fp32.
+ *   cu_seqlens: DEVICE int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
+ *   cu_seqlens[num_seqs] = total_tokens. Each sequence is its own causal problem.
+ *   max_seqlen: an upper bound on every sequence length (sizes the grid without reading
+ *   cu_seqlens on the host). Rows of sequences longer than max_seqlen are not computed.
+ */
+ATTN_API int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
+                    const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
+                    float scale, int causal, int window, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_bwd -- gradient of the forward above with respect to q, k and v, given dO.
+ *   Inputs q, k, v, o (the forward's output), lse (the forward's log-sum-exp) and dO in
+ *   the forward's layouts; outputs dQ [.., Hq, D], dK, dV [.., Hkv, D] bf16 (dK/dV sum
+ *   the contributions of every query head of the KV head's group).
+ *   cu_seqlens == NULL: dense [B, S, ...] layout, lse [B, Hq, S].
+ *   cu_seqlens != NULL: packed layout with B == 1, S == total tokens, lse [Hq, S], and
+ *   num_seqs / max_seqlen as in attn_fwd_varlen.
+ *   workspace: at least attn_workspace_size(ATTN_OP_BWD[_VARLEN], ...) bytes, 256-byte
+ *   aligned; holds an fp32 dQ accumulator and per-row Delta = rowsum(dO * o). Contents on
+ *   entry do not matter.
+ * The backward recomputes P from lse, never stores it, and must stay finite in bf16
+ * (issue-3232 page, "Debug and validation results").
+ */
+ATTN_API int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const attn_bf16* o, const float* lse,
+             const attn_bf16* dO, attn_bf16* dQ, attn_bf16* dK, attn_bf16* dV, int B, int Hq, int Hkv, int S, int D,
+             float scale, int causal, int window, const int32_t* cu_seqlens, int num_seqs, int max_seqlen,
+             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_decode_paged -- one new query token per request over a paged KV cache
+ * ("flex_attention + paged KV ..." page, "Architecture notes").
+ *   q [B, Hq, D] bf16; k_cache, v_cache [num_pages, page_size, Hkv, D] bf16;
+ *   block_table DEVICE int32 [B, max_pages_per_seq]: page ids of request b in order;
+ *   seq_lens DEVICE int32 [B]: cached tokens of request b (the query is token L-1 and
+ *   sees all L of them). o [B, Hq, D] bf16 out, lse [B, Hq] fp32 out.
+ *   A request with L = 0 gets o = 0 and lse = -inf. Page ids outside [0, num_pages) or
+ *   lengths beyond max_pages_per_seq * page_size are not read: the affected tokens are
+ *   skipped and ATTN_ERR_DEVICE_BOUNDS is recorded for attn_get_device_status().
+ *   Supported: D = 128, page_size = 16, Hkv <= 8, Hq / Hkv in {1, 2, 4, 8}, B <= 4096.
+ *   workspace: at least attn_workspace_size(ATTN_OP_DECODE_PAGED, ...) bytes; it holds
+ *   split partials and per-request arrival counters. The counters must be zero before
+ *   the FIRST call on a workspace (e.g. cudaMemset); every call leaves them zero again.
+ *   Calls that share a workspace must not overlap on the GPU.
+ */
+ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                      const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
+                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_workspace_size -- bytes of workspace an operation needs (0 if none).
+ *   For ATTN_OP_BWD: B, Hq, S, D; for ATTN_OP_BWD_VARLEN pass B = 1 and S = total tokens.
+ *   For ATTN_OP_DECODE_PAGED: B, Hq, D. Unused arguments are ignored. Returns 0 for an
+ *   unknown op. Pure host arithmetic; needs no GPU.
+ */
+ATTN_API size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D, int num_seqs, int max_pages_per_seq);
+
+/*
+ * attn_get_device_status -- synchronise `stream`, then read and clear the device fault
+ * flags raised by kernels of this library on the current device. Returns ATTN_OK,
+ * ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_DEVICE_BOUNDS, or ATTN_ERR_LAUNCH if the stream
+ * itself reports a CUDA error.
+ */
+ATTN_API int attn_get_device_status(void* stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/* attn_version -- library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_ATTN_H */

@@ -660,35 +660,53 @@ int oracle_attn_dkv_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v
     }
     C.rows = rows, C.out_a = dk, C.out_b = dv;
     int nseq = C.P.nseq;
-    /* Mark which query rows are needed: all rows of (b, h in group of a requested g). */
+    /* Query rows that can see a requested key: for every (b, h) whose KV head is
+     * requested, the hull [min j, last row that sees max j] of the requested keys. */
     size_t nbh = (size_t)nseq * Hq;
     int64_t* first = (int64_t*)malloc(sizeof(int64_t) * nbh);
+    int64_t* ilo = (int64_t*)malloc(sizeof(int64_t) * nbh);
+    int64_t* ihi = (int64_t*)malloc(sizeof(int64_t) * nbh);
     char* need = (char*)calloc(nbh, 1);
-    if (!first || !need) {
-        free(first), free(need), free(offs);
+    if (!first || !need || !ilo || !ihi) {
+        free(first), free(need), free(ilo), free(ihi), free(offs);
         return -2;
     }
     seq_view sv0 = view_of(&C.P, 0);
     for (long r = 0; r < nrows; ++r) {
         int b = (int)rows[3 * r], g = (int)rows[3 * r + 1];
-        for (int h = 0; h < Hq; ++h)
-            if (kv_head_of(&sv0, h) == g) need[(size_t)b * Hq + h] = 1;
+        int64_t j = rows[3 * r + 2], L = C.P.len[b];
+        int64_t lo = C.P.causal ? j : 0;
+        int64_t hi = (window > 0) ? j + window - 1 : L - 1;
+        if (hi > L - 1) hi = L - 1;
+        if (!C.P.causal) lo = (window > 0 && j - window + 1 > 0) ? j - window + 1 : 0;
+        for (int h = 0; h < Hq; ++h) {
+            if (kv_head_of(&sv0, h) != g) continue;
+            size_t bh = (size_t)b * Hq + h;
+            if (!need[bh]) {
+                need[bh] = 1;
+                ilo[bh] = lo;
+                ihi[bh] = hi;
+            } else {
+                if (lo < ilo[bh]) ilo[bh] = lo;
+                if (hi > ihi[bh]) ihi[bh] = hi;
+            }
+        }
     }
     long nq = 0;
     for (size_t bh = 0; bh < nbh; ++bh) {
-        first[bh] = need[bh] ? nq : -1;
-        if (need[bh]) nq += (long)C.P.len[bh / Hq];
+        first[bh] = need[bh] ? nq - ilo[bh] : -1; /* index of row i is first[bh] + i */
+        if (need[bh] && ihi[bh] >= ilo[bh]) nq += (long)(ihi[bh] - ilo[bh] + 1);
     }
     int64_t* qrows = (int64_t*)malloc(sizeof(int64_t) * 3 * (size_t)(nq > 0 ? nq : 1));
     double* st = (double*)malloc(sizeof(double) * 3 * (size_t)(nq > 0 ? nq : 1));
     if (!qrows || !st) {
-        free(first), free(need), free(offs), free(qrows), free(st);
+        free(first), free(need), free(ilo), free(ihi), free(offs), free(qrows), free(st);
         return -2;
     }
     for (size_t bh = 0; bh < nbh; ++bh) {
         if (!need[bh]) continue;
         int b = (int)(bh / Hq), h = (int)(bh % Hq);
-        for (int i = 0; i < C.P.len[b]; ++i) {
+        for (int64_t i = ilo[bh]; i <= ihi[bh]; ++i) {
             long r = (long)(first[bh] + i);
             qrows[3 * r] = b, qrows[3 * r + 1] = h, qrows[3 * r + 2] = i;
         }
@@ -702,7 +720,7 @@ int oracle_attn_dkv_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v
         dkv_acc_ctx A = {&C, &X, first, Hq};
         rc = parallel_for(nrows, nthreads, 1, dkv_acc_item, &A);
     }
-    free(first), free(need), free(offs), free(qrows), free(st);
+    free(first), free(need), free(ilo), free(ihi), free(offs), free(qrows), free(st);
     return rc;
 }
 
