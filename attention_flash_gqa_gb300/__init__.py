@@ -27,6 +27,7 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
     "attn_get_device_status", "attn_status_string", "library_path", "load_library",
+    "attn_launch_count", "attn_profile_start", "attn_profile_stop",
     "ATTN_OP_FWD", "ATTN_OP_FWD_VARLEN", "ATTN_OP_BWD", "ATTN_OP_BWD_VARLEN", "ATTN_OP_DECODE_PAGED",
 ]
 
@@ -72,6 +73,10 @@ def load_library():
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_version.restype = I
+        lib.attn_launch_count.restype = ctypes.c_ulonglong
+        lib.attn_profile_start.restype = I
+        lib.attn_profile_stop.argtypes = [ctypes.c_char_p, Z]
+        lib.attn_profile_stop.restype = I
         for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_bwd, lib.attn_decode_paged, lib.attn_get_device_status):
             f.restype = I
         _lib = lib
@@ -85,6 +90,29 @@ def attn_status_string(status: int) -> str:
 def attn_workspace_size(op: int, B: int = 0, Hq: int = 0, Hkv: int = 0, S: int = 0, D: int = 0, num_seqs: int = 0,
                         max_pages_per_seq: int = 0) -> int:
     return int(load_library().attn_workspace_size(op, B, Hq, Hkv, S, D, num_seqs, max_pages_per_seq))
+
+
+def attn_launch_count() -> int:
+    """Kernel launches issued by the library in this process (monotonic)."""
+    return int(load_library().attn_launch_count())
+
+
+def attn_profile_start() -> None:
+    """Bracket every library kernel launch with CUDA events from now on (clears old records)."""
+    _check(load_library().attn_profile_start(), "attn_profile_start")
+
+
+def attn_profile_stop() -> dict:
+    """Stop profiling; returns {kernel name: (launches, total device ms)}."""
+    buf = ctypes.create_string_buffer(1 << 14)
+    n = load_library().attn_profile_stop(buf, len(buf))
+    if n < 0:
+        raise AttnError(-n, "attn_profile_stop")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, cnt, ms = line.split()
+        out[name] = (int(cnt), float(ms))
+    return out
 
 
 def _stream_ptr(stream, device):

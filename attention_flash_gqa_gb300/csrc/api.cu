@@ -9,7 +9,11 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "attn_internal.h"
@@ -122,9 +126,100 @@ int fwd_common(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_
     return attn::launch_fwd(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
+// ---- launch accounting and the optional event profiler ------------------------------------
+std::atomic<unsigned long long> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfRec {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+std::vector<ProfRec> g_prof;
+
+}  // namespace
+
+namespace attn {
+
+ProfMark prof_begin(cudaStream_t stream, const char* kernel) {
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    ProfMark m;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (!g_prof_on) return m;
+    ProfRec r{kernel, nullptr, nullptr};
+    if (cudaEventCreate(&r.start) != cudaSuccess) return m;
+    if (cudaEventCreate(&r.stop) != cudaSuccess) {
+        cudaEventDestroy(r.start);
+        return m;
+    }
+    cudaEventRecord(r.start, stream);
+    m.slot = (int)g_prof.size();
+    g_prof.push_back(r);
+    return m;
+}
+
+void prof_end(cudaStream_t stream, ProfMark m) {
+    if (m.slot < 0) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    if (m.slot < (int)g_prof.size()) cudaEventRecord(g_prof[m.slot].stop, stream);
+}
+
+}  // namespace attn
+
+namespace {
+void prof_clear_locked() {
+    for (auto& r : g_prof) {
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    g_prof.clear();
+}
 }  // namespace
 
 extern "C" {
+
+unsigned long long attn_launch_count(void) { return g_launches.load(); }
+
+int attn_profile_start(void) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof_clear_locked();
+    g_prof_on = true;
+    return ATTN_OK;
+}
+
+int attn_profile_stop(char* buf, size_t buf_bytes) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof_on = false;
+    struct Acc {
+        long long n = 0;
+        double ms = 0.0;
+    };
+    std::map<std::string, Acc> acc;
+    int rc = 0;
+    for (auto& r : g_prof) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) {
+            rc = -ATTN_ERR_LAUNCH;
+            continue;
+        }
+        Acc& a = acc[r.name];
+        a.n += 1;
+        a.ms += ms;
+    }
+    prof_clear_locked();
+    std::string out;
+    for (auto& kv : acc) {
+        char line[160];
+        std::snprintf(line, sizeof(line), "%s %lld %.6f\n", kv.first.c_str(), kv.second.n, kv.second.ms);
+        out += line;
+    }
+    if (buf && buf_bytes) {
+        const size_t n = out.size() < buf_bytes - 1 ? out.size() : buf_bytes - 1;
+        std::memcpy(buf, out.data(), n);
+        buf[n] = 0;
+    }
+    return rc ? rc : (int)acc.size();
+}
+
 
 int attn_version(void) { return 100; }
 

@@ -434,8 +434,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     {
         const long long threads = rh * 32;
         const unsigned blocks = (unsigned)((threads + 255) / 256);
+        const ProfMark m = prof_begin(stream, "bwd_prep");
         bwd_prep_kernel<D><<<blocks, 256, 0, stream>>>(L.o, L.dO, L.delta, L.dq_acc, L.cu_seqlens, L.nseq, L.S,
                                                        L.total_rows, L.Hq, rh);
+        prof_end(stream, m);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -452,14 +454,18 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
         cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         dim3 grid(L.Hkv * a.nslices, L.nseq, a.n_kvtiles);
+        const ProfMark m = prof_begin(stream, D == 256 ? "bwd_main_d256" : "bwd_main_d512");
         bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+        prof_end(stream, m);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     {
         const long long n8 = rh * D / 8;
         const unsigned blocks = (unsigned)std::min<long long>((n8 + 255) / 256, 152LL * 16);
+        const ProfMark m = prof_begin(stream, "bwd_finalize");
         bwd_finalize_kernel<<<blocks, 256, 0, stream>>>(L.dq_acc, L.dQ, n8);
+        prof_end(stream, m);
         return cudaGetLastError();
     }
 }

@@ -364,7 +364,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(fwd_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.Hq, L.nseq * a.nsplit, a.n_qtiles);
+    const ProfMark m = prof_begin(stream, DQK == 256 ? "fwd_d256" : "fwd_d512");
     fwd_kernel<DQK><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
+    prof_end(stream, m);
     return cudaGetLastError();
 }
 

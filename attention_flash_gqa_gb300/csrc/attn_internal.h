@@ -8,6 +8,15 @@
 
 namespace attn {
 
+// ---- launch accounting (api.cu) ------------------------------------------------------------
+// Every kernel launch of the library goes through these: a process-wide launch counter and,
+// when profiling is on, a CUDA event pair on the launching stream.
+struct ProfMark {
+    int slot = -1;
+};
+ProfMark prof_begin(cudaStream_t stream, const char* kernel);
+void prof_end(cudaStream_t stream, ProfMark m);
+
 // ---- paged decode -----------------------------------------------------------------------
 struct DecodeLaunch {
     const uint16_t *q, *k_cache, *v_cache;

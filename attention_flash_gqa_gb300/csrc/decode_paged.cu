@@ -436,7 +436,9 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     auto go = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        const ProfMark m = prof_begin(stream, "decode_paged");
         kern<<<L.grid, kThreads, smem, stream>>>(a);
+        prof_end(stream, m);
         return cudaGetLastError();
     };
     switch (G) {

@@ -1,0 +1,502 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention hot path on GB300.
+
+One step = one forward + backward pass (every step of the path: TMA staging, tile
+skipping, Q K^T, masking, online softmax, P V, epilogue; Delta, the backward main
+kernel, the dQ finalize) over the dense causal head_dim-512 workload
+B=2, Hq=32, Hkv=4, S=4096, scale 1/sqrt(512), seeded N(0,1) bf16 inputs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line. `value` is whole-job fwd+bwd TFLOP/s with inputs resident in
+HBM (causal-aware count: 4*D per unmasked (query, key) pair forward, 10*D backward);
+`e2e` is the same metric through the C ABI with host buffers (pinned host -> device
+copies of q, k, v, dO and device -> host copies of o, lse, dQ, dK, dV inside the timed
+region). Inputs (q, dO: 268 MB each) are larger than L2, so no flush is needed between
+steps. `roofline` is for the kernel with the largest device time, timed live with CUDA
+events bracketing each launch. `extra` holds the sliding-window (d256, W=1024),
+varlen (d512) and paged-decode (HBM GB/s) measurements. `cpu_baseline` is the fp64
+oracle timed on the host cores over a causal prefix of the same workload.
+
+Under torchrun (N > 1) every rank runs its own replica on its own batch (the
+workload shards by batch / head group with no exchange): "scaling": "weak".
+`--impl reference` times the fp64 oracle (the reference arm for this path) on a
+bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd+bwd TFLOP/s (d512 causal, d256 SWA) % BF16 peak; decode HBM GB/s"
+WORKLOAD = {"workload": "dense causal attention fwd+bwd, head_dim 512, GQA 8:1",
+            "B": 2, "Hq": 32, "Hkv": 4, "S": 4096, "D": 512, "causal": True, "window": 0,
+            "scale": "1/sqrt(512)", "inputs": "seeded N(0,1) bf16", "l2": "inputs larger than L2 (no flush)"}
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# dram bytes per launch (ncu: dram__bytes_read.sum + dram__bytes_write.sum) for kernels whose
+# counters were captured, keyed by kernel; valid only while the kernel's sources hash the same.
+TRAFFIC = {}
+
+
+def pairs_causal(S: int, W: int = 0) -> int:
+    if W <= 0 or W >= S:
+        return S * (S + 1) // 2
+    return W * (W + 1) // 2 + (S - W) * W
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_flash_gqa_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling every 200 ms; keeps samples inside [t0, t1]."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
+        except Exception:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [v for t, v in self.samples if any(a <= t <= b for a, b in self.windows)]
+        if not inside:
+            inside = [v for _, v in self.samples]
+        def num(x):
+            try:
+                return float(x.split()[0])
+            except Exception:
+                return None
+        sm = [num(v[0]) for v in inside if len(v) >= 8 and num(v[0]) is not None]
+        mx = [num(v[1]) for v in inside if len(v) >= 8 and num(v[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for v in inside if len(v) >= 8 for i in range(4) if v[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        pg = dist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float) -> float:
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def to_dev(bits, pin=False):
+    import numpy as np
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(bits).astype(np.int16)).view(torch.bfloat16)
+    return t.pin_memory() if pin else t.cuda()
+
+
+# ----------------------------------------------------------------------------------------------
+def bench_ours(args, rank, world, pg):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import attention_flash_gqa_gb300 as attn
+    import synth
+
+    __graft_entry__.build()
+    dev = torch.cuda.current_device()
+    props = torch.cuda.get_device_properties(dev)
+    peaks, peak_src = load_peaks()
+
+    p = synth.dense(2, 32, 4, 4096, 512, 0, seed=1000 + rank, name="dense_d512_causal")
+    flops_fwd = 4 * p.D * pairs_causal(p.S) * p.B * p.Hq
+    flops_bwd = 10 * p.D * pairs_causal(p.S) * p.B * p.Hq
+    flops_step = flops_fwd + flops_bwd
+
+    q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
+    o = torch.empty_like(q)
+    lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn.attn_workspace_size(attn.ATTN_OP_BWD, p.B, p.Hq, p.Hkv, p.S, p.D), dtype=torch.uint8,
+                     device="cuda")
+
+    def step():
+        attn.attn_fwd(q, k, v, o, lse, scale=p.scale)
+        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=p.scale, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = attn.attn_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {attn.attn_status_string(st)}")
+    finite = bool(torch.isfinite(o.float()).all() and torch.isfinite(dq.float()).all()
+                  and torch.isfinite(dk.float()).all() and torch.isfinite(dv.float()).all())
+
+    gpu_id = getattr(props, "uuid", None)
+    gpu_id = ("GPU-" + str(gpu_id)) if gpu_id is not None and not str(gpu_id).startswith("GPU-") else str(gpu_id or dev)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.5)
+
+    # ---- device-timed region: inputs resident in HBM ----------------------------------------
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(pg)
+    torch.cuda.synchronize()
+    launches0 = attn.attn_launch_count()
+    attn.attn_profile_start()
+    t0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(pg)
+    prof = attn.attn_profile_stop()
+    launches = attn.attn_launch_count() - launches0
+    clocks.mark(t0, t1)
+    ms_step = ev0.elapsed_time(ev1) / args.steps
+    ms_step_max = max_over_ranks(pg, ms_step)
+    value = flops_step * world / (ms_step_max * 1e-3) / 1e12
+
+    # ---- dominant kernel roofline --------------------------------------------------------------
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    name, (n_launch, total_ms) = dom
+    per_launch = {"fwd_d512": flops_fwd, "bwd_main_d512": flops_bwd}.get(name)
+    avg_ms = total_ms / n_launch
+    achieved = per_launch / (avg_ms * 1e-3) / 1e12 if per_launch else None
+    peak = peaks["bf16_tflops_sustained"]
+    tr = TRAFFIC.get(name)
+    traffic = tr["bytes"] if tr and tr.get("src") == kernel_sources_hash() else None
+    roofline = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak if achieved else None, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                "avg_launch_ms": avg_ms,
+                "kernels": {kname: {"launches": n, "total_ms": round(t, 4), "share": round(t / sum(
+                    x[1] for x in prof.values()), 4)} for kname, (n, t) in prof.items()}}
+
+    # ---- end to end through the C ABI with host buffers ---------------------------------------
+    hq, hk, hv, hdo = (to_dev(x, pin=True) for x in (p.q, p.k, p.v, p.do))
+    ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    hdq = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    hdk = torch.empty(k.shape, dtype=torch.bfloat16).pin_memory()
+    hdv = torch.empty(v.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, args.steps // 4)
+    barrier(pg)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(pg, ev0.elapsed_time(ev1) / e_steps)
+    e2e = {"value": flops_step * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    del hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv
+    if not args.no_extra:
+        extra = bench_extra(args, attn, synth, peaks, peak_src, clocks)
+    else:
+        extra = None
+    clocks.stop()
+    st = attn.attn_get_device_status()
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {**WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "frac_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
+                              "sustained": value / world / peaks["bf16_tflops_sustained"], "source": peak_src},
+        "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks.summary(),
+        "finite": finite, "device_status": attn.attn_status_string(st), "gpu": props.name,
+    }
+    if extra is not None:
+        out["extra"] = extra
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_seconds, problem=p)
+    return out
+
+
+def bench_extra(args, attn, synth, peaks, peak_src, clocks):
+    """Sliding-window d256 fwd+bwd, varlen d512 fwd+bwd, paged decode (GB/s)."""
+    import numpy as np
+    import torch
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(3, args.steps // 4)
+
+    def timed(fn, n):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        ev0.record(stream)
+        for _ in range(n):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        clocks.mark(t0, time.time())
+        return ev0.elapsed_time(ev1) / n
+
+    # sliding window, d256, W=1024, outliers
+    p = synth.swa_d256_w1024(seed=7)
+    q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
+    o = torch.empty_like(q)
+    lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ms = timed(lambda: (attn.attn_fwd(q, k, v, o, lse, window=p.window, scale=p.scale),
+                        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, window=p.window, scale=p.scale)), steps)
+    fl = 14 * p.D * pairs_causal(p.S, p.window) * p.B * p.Hq
+    fin = all(bool(torch.isfinite(t.float()).all()) for t in (o, dq, dk, dv))
+    res["swa_d256_w1024"] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+                             "frac_of_bf16_peak_sustained": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                             "all_grads_finite": fin}
+    del q, k, v, do, o, lse, dq, dk, dv
+
+    # varlen d512
+    vp = synth.varlen_d512_causal(seed=7)
+    q, k, v, do = (to_dev(x) for x in (vp.q, vp.k, vp.v, vp.do))
+    cu = torch.from_numpy(vp.cu_seqlens).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((vp.Hq, vp.total_tokens), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ms = timed(lambda: (attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, o, lse, scale=vp.scale),
+                        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=vp.scale, cu_seqlens=cu,
+                                      max_seqlen=vp.max_seqlen)), steps)
+    fl = 14 * vp.D * vp.Hq * sum(int(L) * (int(L) + 1) // 2 for L in vp.seqlens)
+    res["varlen_d512_causal"] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+                                 "seqlens": [int(x) for x in vp.seqlens]}
+    del q, k, v, do, o, lse, dq, dk, dv
+
+    # paged decode: time the kernel alone, flushing L2 (write > L2) between calls
+    pp = synth.decode_paged_d128(seed=7)
+    qd, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
+    bt = torch.from_numpy(pp.block_table).cuda()
+    sl = torch.from_numpy(pp.seq_lens).cuda()
+    od = torch.empty_like(qd)
+    ld = torch.empty((pp.B, pp.Hq), dtype=torch.float32, device="cuda")
+    wsd = torch.zeros(attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, pp.B, pp.Hq, pp.Hkv, 0, pp.D),
+                      dtype=torch.uint8, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    kv_bytes = int(sum(int(L) for L in pp.seq_lens)) * pp.Hkv * pp.D * 2 * 2
+    io_bytes = pp.B * pp.Hq * pp.D * 2 * 2 + pp.B * pp.Hq * 4
+    times = []
+    for i in range(max(20, args.steps) + 3):
+        flush.fill_(i & 0xff)
+        ev0.record(stream)
+        attn.attn_decode_paged(qd, kc, vc, bt, sl, od, ld, scale=pp.scale, workspace=wsd)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(ev0.elapsed_time(ev1))
+    med = statistics.median(times)
+    gbs = (kv_bytes + io_bytes) / (med * 1e-3) / 1e9
+    res["decode_paged_d128"] = {"value": gbs, "unit": "GB/s", "us_per_call_median": med * 1e3,
+                                "us_per_call_min": min(times) * 1e3, "bytes_per_call": kv_bytes + io_bytes,
+                                "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
+                                "l2": "flushed (512 MB write) before every call"}
+    return res
+
+
+class OracleSample:
+    """fp64 oracle fwd+bwd on the first `prefix` tokens of every sequence of the workload."""
+
+    def __init__(self, problem=None):
+        import oracle
+        import synth
+
+        self.orc = oracle.get()
+        self.p = problem if problem is not None else synth.dense(2, 32, 4, 4096, 512, 0, seed=1000)
+        self.nthreads = oracle.default_threads()
+
+    def run(self, S: int) -> float:
+        import numpy as np
+
+        p = self.p
+        sub = [np.ascontiguousarray(x[:, :S]) for x in (p.q, p.k, p.v, p.do)]
+        t = time.time()
+        self.orc.fwd(sub[0], sub[1], sub[2], p.scale, nthreads=self.nthreads)
+        self.orc.bwd(*sub, p.scale, nthreads=self.nthreads)
+        return time.time() - t
+
+    def pick_prefix(self, budget_s: float) -> int:
+        t_small = self.run(256)
+        # cost grows as S^2: the prefix that fills the budget, in 128-token multiples, <= 4096
+        prefix = int(min(4096, max(128, 256 * (budget_s / max(t_small, 1e-3)) ** 0.5)))
+        return max(128, prefix - prefix % 128)
+
+    def flops(self, S: int) -> int:
+        p = self.p
+        return 14 * p.D * pairs_causal(S) * p.B * p.Hq
+
+    def describe(self, S: int) -> str:
+        return (f"fp64 oracle fwd+bwd of the first {S} tokens of every sequence "
+                f"(B=2, Hq=32, Hkv=4, D=512, causal), {self.nthreads} threads")
+
+
+def cpu_baseline(budget_s: float = 20.0, problem=None):
+    sample = OracleSample(problem)
+    prefix = sample.pick_prefix(budget_s)
+    dt = sample.run(prefix)
+    return {"value": sample.flops(prefix) / dt / 1e12, "unit": "TFLOP/s", "cores": sample.nthreads,
+            "kind": "oracle", "seconds": dt, "sample": sample.describe(prefix)}
+
+
+def bench_reference(args, rank, world):
+    """The reference arm: the fp64 oracle as it stands, on the host cores."""
+    if rank != 0:
+        return None
+    sample = OracleSample()
+    total = 150.0  # seconds for the whole run
+    prefix = sample.pick_prefix(max(1.0, total / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        sample.run(prefix)
+    secs = [sample.run(prefix) for _ in range(args.steps)]
+    med = statistics.median(secs)
+    value = sample.flops(prefix) / med / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": med * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16)", "config": {**WORKLOAD, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample.nthreads, "kind": "oracle",
+                         "sample": sample.describe(prefix) + "; each step one such sample"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="skip the SWA / varlen / decode measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        out = bench_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    rank, world, _, pg = dist_setup(args.gpus)
+    out = bench_ours(args, rank, world, pg)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

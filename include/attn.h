@@ -166,6 +166,20 @@ ATTN_API const char* attn_status_string(int status);
 /* attn_version -- library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 ATTN_API int attn_version(void);
 
+/*
+ * Observability (no counterpart on the pages; used by the benchmark):
+ * attn_launch_count -- number of kernel launches this library has issued in this process.
+ * attn_profile_start -- from now on, bracket every kernel launch with a pair of CUDA events
+ *   on the launching stream (discards earlier records). Do not enable while capturing a
+ *   CUDA graph.
+ * attn_profile_stop -- stop recording, wait for the recorded events, and write one line per
+ *   kernel, "name launches total_ms\n", into buf (NUL-terminated, truncated to buf_bytes).
+ *   Returns the number of distinct kernels, or -ATTN_ERR_LAUNCH if an event failed.
+ */
+ATTN_API unsigned long long attn_launch_count(void);
+ATTN_API int attn_profile_start(void);
+ATTN_API int attn_profile_stop(char* buf, size_t buf_bytes);
+
 #ifdef __cplusplus
 }
 #endif
