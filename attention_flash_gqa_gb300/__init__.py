@@ -27,7 +27,7 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
     "attn_get_device_status", "attn_status_string", "library_path", "load_library",
-    "attn_launch_count", "attn_profile_start", "attn_profile_stop",
+    "attn_launch_count", "attn_profile_start", "attn_profile_stop", "attn_decode_paged_noalloc",
     "ATTN_OP_FWD", "ATTN_OP_FWD_VARLEN", "ATTN_OP_BWD", "ATTN_OP_BWD_VARLEN", "ATTN_OP_DECODE_PAGED",
 ]
 
@@ -73,6 +73,9 @@ def load_library():
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_version.restype = I
+        lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.attn_decode_paged_noalloc.restype = I
+        lib.attn_decode_paged_noalloc_max_bytes.restype = Z
         lib.attn_launch_count.restype = ctypes.c_ulonglong
         lib.attn_profile_start.restype = I
         lib.attn_profile_stop.argtypes = [ctypes.c_char_p, Z]
@@ -252,4 +255,28 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=No
                                           page_size, block_table.shape[1], num_pages, scale, _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device))
     _check(rc, "attn_decode_paged")
+    return o, lse
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse, *, scale: float | None = None,
+                              stream=None):
+    """attn_decode_paged without a workspace: the library's built-in scratch buffer is used.
+
+    For callers that cannot allocate device memory on their decode path, so the outputs
+    ``o`` [B,Hq,D] and ``lse`` [B,Hq] must be supplied by the caller. Calls that overlap
+    on the GPU share the buffer and race; see include/attn.h for the size limit.
+    """
+    import torch
+
+    B, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens")):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    rc = load_library().attn_decode_paged_noalloc(
+        _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
+        _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, scale,
+        _stream_ptr(stream, q.device))
+    _check(rc, "attn_decode_paged_noalloc")
     return o, lse

@@ -145,6 +145,35 @@ ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, con
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_decode_paged_noalloc -- attn_decode_paged for callers that cannot allocate device
+ * memory (no counterpart on the pages; added for integrators). Some callers cannot call
+ * cudaMalloc on their decode path: a plug-in inside a host application that owns the
+ * whole device-memory budget through its own pool, or a latency-critical token loop where
+ * cudaMalloc's implicit device synchronisation would stall other streams. This variant
+ * takes no workspace: the kernel's scratch comes from a 16 MiB buffer compiled into the
+ * library (attn_decode_paged_noalloc_max_bytes()), which every GPU that loads the library
+ * keeps until the process exits. It allocates nothing and calls no allocating routine.
+ *   Arguments, layouts and results are those of attn_decode_paged.
+ *   Limit: attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, 0, max_pages) must
+ *   not exceed attn_decode_paged_noalloc_max_bytes() (e.g. Hq = 32 allows B up to 480);
+ *   larger problems are rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
+ *   The first call made while a given device is current looks up the buffer's device
+ *   address (cudaGetSymbolAddress) for that device; make that first call before any
+ *   stream capture on the device.
+ *   All calls on a device share the one buffer, and it keeps the previous call's
+ *   contents; each call clears the parts that must start at zero on its own stream.
+ *   Calls whose execution overlaps on the GPU (different streams without ordering) race
+ *   on the buffer and give wrong results: order them.
+ */
+ATTN_API int attn_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                                       const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse,
+                                       int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
+                                       int num_pages, float scale, void* stream);
+
+/* attn_decode_paged_noalloc_max_bytes -- size of the built-in decode scratch buffer (bytes). */
+ATTN_API size_t attn_decode_paged_noalloc_max_bytes(void);
+
+/*
  * attn_workspace_size -- bytes of workspace an operation needs (0 if none).
  *   For ATTN_OP_BWD: B, Hq, S, D; for ATTN_OP_BWD_VARLEN pass B = 1 and S = total tokens.
  *   For ATTN_OP_DECODE_PAGED: B, Hq, D. Unused arguments are ignored. Returns 0 for an
