@@ -191,7 +191,7 @@ def bench_ours(args, rank, world, pg):
     props = torch.cuda.get_device_properties(dev)
     peaks, peak_src = load_peaks()
 
-    p = synth.dense(2, 32, 4, 4096, 512, 0, seed=1000 + rank, name="dense_d512_causal")
+    p = synth.dense(args.batch, 32, 4, 4096, 512, 0, seed=1000 + rank, name="dense_d512_causal")
     flops_fwd = 4 * p.D * pairs_causal(p.S) * p.B * p.Hq
     flops_bwd = 10 * p.D * pairs_causal(p.S) * p.B * p.Hq
     flops_step = flops_fwd + flops_bwd
@@ -261,6 +261,9 @@ def bench_ours(args, rank, world, pg):
                     x[1] for x in prof.values()), 4)} for kname, (n, t) in prof.items()}}
 
     # ---- end to end through the C ABI with host buffers ---------------------------------------
+    if args.no_e2e:
+        return finish(args, rank, world, p, attn, value, ms_step_max, roofline, None, launches, clocks, finite,
+                      props, peaks, peak_src, None)
     hq, hk, hv, hdo = (to_dev(x, pin=True) for x in (p.q, p.k, p.v, p.do))
     ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
@@ -296,18 +299,20 @@ def bench_ours(args, rank, world, pg):
     e2e = {"value": flops_step * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     del hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv
-    if not args.no_extra:
-        extra = bench_extra(args, attn, synth, peaks, peak_src, clocks)
-    else:
-        extra = None
+    extra = None if args.no_extra else bench_extra(args, attn, synth, peaks, peak_src, clocks)
+    return finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launches, clocks, finite, props,
+                  peaks, peak_src, extra)
+
+
+def finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launches, clocks, finite, props, peaks,
+           peak_src, extra):
     clocks.stop()
     st = attn.attn_get_device_status()
-
+    config = {**WORKLOAD, "B": p.B, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
     out = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {**WORKLOAD, "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16)", "config": config,
         "frac_of_bf16_peak": {"burst": value / world / peaks["bf16_tflops"],
                               "sustained": value / world / peaks["bf16_tflops_sustained"], "source": peak_src},
         "roofline": roofline, "e2e": e2e, "gpu_launches": launches, "clocks": clocks.summary(),
@@ -480,6 +485,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the SWA / varlen / decode measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--batch", type=int, default=2, help="batch of the dense workload (2 = the workload; 1 for "
+                                                          "smaller profiler captures)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
