@@ -83,6 +83,17 @@ bool make_map(CUtensorMap* m, const void* base, int D, int H, int rows, int batc
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over the fp32 dQ accumulator [batch, rows, heads, dim], box = 32 floats x 1 x 128 rows.
+bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int rows, int batch) {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4, (cuuint64_t)rows * H * D * 4};
+    cuuint32_t box[4] = {32, 1, 128, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int check_common(int Hq, int Hkv, float scale, int causal, int window) {
@@ -313,6 +324,7 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
     L.q = q, L.k = k, L.v = v, L.o = o, L.dO = dO, L.lse = lse, L.dQ = dQ, L.dK = dK, L.dV = dV;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     L.dq_acc = reinterpret_cast<float*>(ws);
+    if (!make_map_f32(&L.tdq, L.dq_acc, D, Hq, map_rows, batch)) return ATTN_ERR_LAUNCH;
     L.delta = reinterpret_cast<float*>(ws + align256((size_t)rows * Hq * D * 4));
     L.cu_seqlens = cu_seqlens, L.status = dev->status;
     L.nseq = varlen ? num_seqs : B;

@@ -15,7 +15,8 @@
 //     its keys (causal / window tile skipping), so dK and dV are summed over the group
 //     in tensor memory without atomics. Tensor memory (512 columns):
 //       [0, 128)   S = Q K^T (queries on lanes); reused for the dQ slice dS K_c
-//       [128, 256) dP = dO V^T
+//       [128, 256) dP = dO V^T; the softmax warps move dP(t) into registers first, so
+//                  the MMA can compute dP(t+1) while they work on step t
 //       [256, 384) dV_c accumulator (keys on lanes), [384, 512) dK_c accumulator
 //     S and dP contract over the full D, so each of the D/128 slice CTAs recomputes
 //     them; dV_c, dK_c and dQ_c are each computed once. dQ_c leaves TMEM after every
@@ -57,7 +58,8 @@ struct BwdArgs {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo, BwdArgs a) {
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tdq, BwdArgs a) {
     constexpr int kChunks = D / 128;  // 32 KB slots per full-width row tile
     const int g = blockIdx.x / a.nslices, cs = blockIdx.x % a.nslices;
     const int seq = blockIdx.y;
@@ -84,11 +86,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
-    uint64_t* sdp_full = bars + 2 * kStages;
-    uint64_t* p_full = sdp_full + 1;
+    uint64_t* s_full = bars + 2 * kStages;  // S(t) complete
+    uint64_t* dp_full = s_full + 1;          // dP(t) complete
+    uint64_t* dp_free = dp_full + 1;         // dP(t) read out of TMEM by the softmax warps
+    uint64_t* p_full = dp_free + 1;
     uint64_t* dq_full = p_full + 1;
     uint64_t* dq_free = dq_full + 1;
-    uint64_t* mma_idle = dq_free + 1;
+    uint64_t* stage_full = dq_free + 1;   // all 128 dQ rows staged in smem
+    uint64_t* stage_free = stage_full + 1; // the previous step's reduce has read the staging smem
+    uint64_t* mma_idle = stage_free + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -98,10 +104,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        mbar_init(smem_u32(sdp_full), 1);
+        mbar_init(smem_u32(s_full), 1);
+        mbar_init(smem_u32(dp_full), 1);
+        mbar_init(smem_u32(dp_free), 128);
         mbar_init(smem_u32(p_full), 128);
         mbar_init(smem_u32(dq_full), 1);
         mbar_init(smem_u32(dq_free), 128);
+        mbar_init(smem_u32(stage_full), 128);
+        mbar_init(smem_u32(stage_free), 1);
         mbar_init(smem_u32(mma_idle), 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -134,12 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++slot == kStages) slot = 0, ++round;
                 return true;
             };
-            auto load_sdp = [&](int t) -> bool {  // dP operands, then S operands
+            auto load_dp = [&](int t) -> bool {  // dP = dO V^T operands, chunk pairs
                 const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
                 for (int c = 0; c < kChunks; ++c) {
                     if (!load(&tdo, h, c * 128, qrow)) return false;
                     if (!load(&tv, g, c * 128, krow)) return false;
                 }
+                return true;
+            };
+            auto load_s = [&](int t) -> bool {  // S = Q K^T operands, chunk pairs
+                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
                 for (int c = 0; c < kChunks; ++c) {
                     if (!load(&tq, h, c * 128, qrow)) return false;
                     if (!load(&tk, g, c * 128, krow)) return false;
@@ -150,10 +164,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
                 return load(&tdo, h, c0, qrow) && load(&tq, h, c0, qrow) && load(&tk, g, c0, krow);
             };
-            bool ok = load_sdp(0);
+            // Q and dO tiles are new every step and mostly miss L2 (they are re-read by every
+            // key tile of the head group, long after): warm L2 with them two steps ahead so the
+            // ring's copies find them there.
+            constexpr int kAhead = 2;
+            auto prefetch_q_do = [&](int t) {
+                if (t >= n) return;
+                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
+                for (int c = 0; c < D; c += 64) {
+                    tma_prefetch_4d(&tq, c, h, qrow, bcoord);
+                    tma_prefetch_4d(&tdo, c, h, qrow, bcoord);
+                }
+            };
+            for (int t = 1; t <= kAhead; ++t) prefetch_q_do(t);
+            // the UMMA issuer's consumption order: dP(0) S(0) | dP(t+1) grad(t) S(t+1) | ...
+            bool ok = load_dp(0) && load_s(0);
             for (int t = 0; ok && t < n; ++t) {
-                ok = load_grad(t);
-                if (ok && t + 1 < n) ok = load_sdp(t + 1);
+                prefetch_q_do(t + 1 + kAhead);
+                if (t + 1 < n) ok = load_dp(t + 1);
+                ok = ok && load_grad(t);
+                if (ok && t + 1 < n) ok = load_s(t + 1);
             }
             const int issued = round * kStages + slot;
             for (int s = 0; s < kStages && s < issued; ++s) {
@@ -199,13 +229,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 return true;
             };
-            auto issue_sdp = [&]() -> bool {
-                if (!contract(tDP)) return false;
-                return contract(tS);
-            };
-            ok = issue_sdp();
-            if (ok) umma_commit(smem_u32(sdp_full));
+            ok = contract(tDP);
+            if (ok) umma_commit(smem_u32(dp_full));
+            ok = ok && contract(tS);
+            if (ok) umma_commit(smem_u32(s_full));
             for (int t = 0; ok && t < n; ++t) {
+                if (t + 1 < n) {
+                    // dP(t+1) overwrites the dP columns as soon as the softmax warps hold dP(t)
+                    // in registers, overlapping their work on step t.
+                    ok = mbar_wait(smem_u32(dp_free), t & 1, abort_flag, a.status, 0x29);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (!contract(tDP)) { ok = false; break; }
+                    umma_commit(smem_u32(dp_full));
+                }
                 ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x23);
                 if (!ok) break;
                 tc_fence_after();
@@ -236,14 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 release();
                 umma_commit(smem_u32(dq_full));
                 if (t + 1 < n) {
-                    // dP(t+1) may overwrite its columns now (read before p_full(t));
-                    // S(t+1) must wait until dQ(t) has been read out.
-                    if (!contract(tDP)) { ok = false; break; }
+                    // S(t+1) reuses the S columns once dQ(t) has been read out
                     ok = mbar_wait(smem_u32(dq_free), t & 1, abort_flag, a.status, 0x24);
                     if (!ok) break;
                     tc_fence_after();
                     if (!contract(tS)) { ok = false; break; }
-                    umma_commit(smem_u32(sdp_full));
+                    umma_commit(smem_u32(s_full));
                 }
             }
             umma_commit(smem_u32(mma_idle));
@@ -266,16 +301,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lse2 = a.lse[li] * 1.4426950408889634f;
                 dlt = a.delta[li];
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(sdp_full), t & 1, abort_flag, a.status, 0x25));
+            // dP(t) first, whole row into registers, then hand its columns back to the MMA
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x2a));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t rdp[128];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t tmp[32];
+                tmem_ld32(tDP + c4 * 32 + lane_base, tmp);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rdp[c4 * 32 + e] = tmp[e];
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(dp_free));
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full), t & 1, abort_flag, a.status, 0x25));
             if (!ok) break;
             tc_fence_after();
             const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) && q0 + kB <= L &&
                                 k0 + kB <= L);
-#pragma unroll 1
+            if (t > 0) {
+                // sP/sdS double as the dQ staging tile of step t-1: wait until its reduce has read it
+                if (tid == 64) {
+                    bulk_wait_group_read0();
+                    mbar_arrive(smem_u32(stage_free));
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(stage_free), (t - 1) & 1, abort_flag, a.status, 0x2b));
+                if (!ok) break;
+            }
+#pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t rs[32], rdp[32];
+                uint32_t rs[32];
                 tmem_ld32(tS + c4 * 32 + lane_base, rs);
-                tmem_ld32(tDP + c4 * 32 + lane_base, rdp);
                 tmem_ld_wait();
                 uint32_t pk[16], dk[16];
 #pragma unroll
@@ -288,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (edge) allowed = allowed && key <= qi && key < L && (a.window <= 0 || qi - key < a.window);
                         const float sv = __uint_as_float(rs[e + u]);
                         p[u] = allowed ? fast_exp2(fmaf(sv, a.scale_log2, -lse2)) : 0.f;
-                        ds[u] = p[u] * (__uint_as_float(rdp[e + u]) - dlt);
+                        ds[u] = p[u] * (__uint_as_float(rdp[c4 * 32 + e + u]) - dlt);
                     }
                     pk[e >> 1] = pack_bf16x2(p[0], p[1]);
                     dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
@@ -304,29 +362,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(smem_u32(p_full));
-            // dQ_c rows: scale and add into the fp32 accumulator
+            // dQ_c rows: scale and stage in shared memory (the P/dS tiles, free once dQ(t) is
+            // done), then one thread adds the tile into the fp32 accumulator with TMA bulk
+            // reduce-adds that complete in the background.
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x26));
             if (!ok) break;
             tc_fence_after();
-            float* dq_row = a.dq_acc + ((size_t)(a.cu_seqlens ? seq_start + qi : seq * a.S + qi) * a.Hq + h) * D + c0;
+            const float f = row_ok ? a.scale : 0.f;  // rows past the sequence end add zeros
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t rq[32];
                 tmem_ld32(tS + c4 * 32 + lane_base, rq);
                 tmem_ld_wait();
-                if (row_ok) {
+                // box c4: columns 32*c4 .. +31 (128 bytes per row), 128-byte swizzle
+                const uint32_t box = sP + c4 * kSubBytes;
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 v = make_float4(__uint_as_float(rq[e]) * a.scale, __uint_as_float(rq[e + 1]) * a.scale,
-                                                     __uint_as_float(rq[e + 2]) * a.scale,
-                                                     __uint_as_float(rq[e + 3]) * a.scale);
-                        atomicAdd(reinterpret_cast<float4*>(dq_row + c4 * 32 + e), v);
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = box + r * 128 + (((uint32_t)j ^ (uint32_t)(r & 7)) << 4);
+                    st_shared_v4(addr, __float_as_uint(__uint_as_float(rq[4 * j]) * f),
+                                 __float_as_uint(__uint_as_float(rq[4 * j + 1]) * f),
+                                 __float_as_uint(__uint_as_float(rq[4 * j + 2]) * f),
+                                 __float_as_uint(__uint_as_float(rq[4 * j + 3]) * f));
                 }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(dq_free));
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(stage_full));
+            if (tid == 64) {
+                ok = mbar_wait(smem_u32(stage_full), t & 1, abort_flag, a.status, 0x2c);
+                if (ok) {
+                    const int qrow = a.cu_seqlens ? seq_start + q0 : q0;
+                    for (int c4 = 0; c4 < 4; ++c4)
+                        tma_reduce_add_4d(&tdq, sP + c4 * kSubBytes, c0 + 32 * c4, h, qrow, bcoord);
+                    bulk_commit_group();
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
         }
+        if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
         // ---- epilogue: dV_c, dK_c rows (keys on lanes) -> bf16 -----------------------------
         // dq_full of the last step implies every earlier UMMA (all dV/dK updates) is done.
         tc_fence_after();
@@ -455,7 +530,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         dim3 grid(L.Hkv * a.nslices, L.nseq, a.n_kvtiles);
         const ProfMark m = prof_begin(stream, D == 256 ? "bwd_main_d256" : "bwd_main_d512");
-        bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, a);
+        bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
         prof_end(stream, m);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
