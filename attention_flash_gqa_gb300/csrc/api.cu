@@ -117,7 +117,8 @@ size_t bwd_ws(long long rows, int Hq, int D) {
 }
 
 size_t decode_ws(int B, int Hq, int D) {
-    return align256((size_t)B * 4) + align256((size_t)(B + attn::decode_max_grid()) * Hq * attn::decode_row_floats() * 4);
+    return align256((size_t)B * 4) +
+           align256((size_t)(B + attn::decode_max_grid()) * 2 * Hq * attn::decode_row_floats() * 4);
 }
 
 int fwd_common(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
@@ -341,7 +342,8 @@ int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_b
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (D != 128 || page_size != 16 || Hkv > 8 || (G != 1 && G != 2 && G != 4 && G != 8) || B > 4096)
+    if (D != 128 || page_size != 16 || Hkv > 8 || (G != 1 && G != 2 && G != 4 && G != 8) || B > 4096 ||
+        num_pages > (1 << 26))
         return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
         (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))

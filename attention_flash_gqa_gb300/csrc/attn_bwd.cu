@@ -290,22 +290,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-            const int h = g * G + t / n_qt;
-            const int q0 = (i_begin + t % n_qt) * kB;
-            const int qi = q0 + r;
-            const bool row_ok = qi < L;
-            float lse2 = INFINITY, dlt = 0.f;
-            if (row_ok) {
-                const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qi : ((size_t)seq * a.Hq + h) * a.S + qi;
-                lse2 = a.lse[li] * 1.4426950408889634f;
-                dlt = a.delta[li];
-            }
-            // dP(t) first, whole row into registers, then hand its columns back to the MMA
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x2a));
-            if (!ok) break;
+        uint32_t rdp[128];
+        // dP of a step: whole row into registers, then hand the columns back to the MMA
+        auto load_dp = [&](int t) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x2a))) return false;
             tc_fence_after();
-            uint32_t rdp[128];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t tmp[32];
@@ -316,6 +305,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(dp_free));
+            return true;
+        };
+        if (n > 0) ok = load_dp(0);
+        for (int t = 0; ok && t < n; ++t) {
+            const int h = g * G + t / n_qt;
+            const int q0 = (i_begin + t % n_qt) * kB;
+            const int qi = q0 + r;
+            const bool row_ok = qi < L;
+            float lse2 = INFINITY, dlt = 0.f;
+            if (row_ok) {
+                const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qi : ((size_t)seq * a.Hq + h) * a.S + qi;
+                lse2 = a.lse[li] * 1.4426950408889634f;
+                dlt = a.delta[li];
+            }
+            // dP(t) is already in registers (loaded right after step t-1's P/dS, or in the
+            // prologue below for t = 0), so the MMA can compute dP(t+1) meanwhile.
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full), t & 1, abort_flag, a.status, 0x25));
             if (!ok) break;
             tc_fence_after();
@@ -362,6 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(smem_u32(p_full));
+            // next step's dP first (its columns are then free for dP(t+2)), then the dQ(t) readout
+            if (t + 1 < n) {
+                ok = load_dp(t + 1);
+                if (!ok) break;
+            }
             // dQ_c rows: scale and stage in shared memory (the P/dS tiles, free once dQ(t) is
             // done), then one thread adds the tile into the fp32 accumulator with TMA bulk
             // reduce-adds that complete in the background.

@@ -11,11 +11,12 @@
 //  * Work is balanced by pages, not by requests: the pages of all requests are laid
 //    end to end and CTA k takes the k-th equal share. A CTA may cover the tail of one
 //    request and the head of the next.
-//  * Warp w handles KV head w for every query head of its group (the GQA group shares
-//    each K/V row). Lane l owns dims 4l..4l+3; per-token dot products are finished by a
-//    butterfly reduce-scatter across the warp.
-//  * fp32 online softmax in the log2 domain. A request split over several CTAs leaves
-//    unnormalised partials (o, m, l) in the workspace; the last CTA to finish that
+//  * 16 consumer warps, two per KV head: each serves all query heads of the head's GQA
+//    group (one K/V row read feeds all of them) on one half of the page's 16 tokens, with
+//    its own running softmax state. Lane l owns dims 4l..4l+3; per-token dot products are
+//    finished by a butterfly reduce-scatter across the warp.
+//  * fp32 online softmax in the log2 domain. Every (CTA, token half) touching a request
+//    leaves unnormalised partials (o, m, l) in the workspace; the last CTA to finish that
 //    request (arrival counter) merges them and resets the counter to zero.
 #include <cuda_runtime.h>
 
@@ -28,10 +29,11 @@ namespace {
 constexpr int kD = 128;
 constexpr int kPage = 16;
 constexpr int kStages = 3;
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kMaxB = 4096;
-constexpr int kRowF = kD + 4;  // partial row: o[kD], m, l, 2 pad floats (keeps float4 alignment)
+constexpr int kRowF = kD + 4;
+constexpr int kMaxUnits = 2048;  // page-table entries of a CTA's range staged in shared memory  // partial row: o[kD], m, l, 2 pad floats (keeps float4 alignment)
 
 struct DecodeArgs {
     const uint16_t* q;
@@ -41,7 +43,7 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     uint16_t* o;
     float* lse;
-    float* part;       // [(B + grid) slots][Hq][kRowF]
+    float* part;       // [(B + grid) * 2 slots][Hq][kRowF]
     int32_t* counters; // [B]
     unsigned* status;
     int B, Hq, Hkv, max_pages, num_pages;
@@ -75,13 +77,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
     const int page_bytes = kPage * a.Hkv * kD * 2;
     uint8_t* stage_base = smem;  // kStages x (K page, V page)
     int32_t* start = reinterpret_cast<int32_t*>(smem + kStages * 2 * page_bytes);  // [B + 1]
-    float* scratch = reinterpret_cast<float*>(start + kMaxB + 8);                  // per warp: sc[16G], sp[16G]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kConsumerWarps * 32 * G);
+    float* scratch = reinterpret_cast<float*>(start + kMaxB + 8);                  // per warp: sc[8G], sp[8G]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kConsumerWarps * 16 * 8);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
     int* last_flag = const_cast<int*>(abort_flag) + 1;
-    int* warp_sums = last_flag + 1;  // [kConsumerWarps]
+    int* warp_sums = last_flag + 1;  // [8]
+    int32_t* unit_tab = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [kMaxUnits]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
@@ -164,6 +167,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
         while (b_first < B && start[b_first + 1] <= u0) ++b_first;
     }
 
+    // Page table of this CTA's range, gathered once by all threads: entry = page id << 5 |
+    // valid tokens in the page (1..16), or -1 for a page id outside the pool. The loops below
+    // then never wait on a dependent global load.
+    const int n_units = (int)(u1 - u0);
+    auto make_entry = [&](int kk) -> int32_t {
+        const long long u = u0 + kk;
+        int lo = b_first, hi = B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (start[mid] <= u) lo = mid;
+            else hi = mid - 1;
+        }
+        const int p = (int)(u - start[lo]);
+        const int page = a.block_table[(size_t)lo * a.max_pages + p];
+        if (page < 0 || page >= a.num_pages) {
+            atomicOr(a.status, DEVSTAT_BOUNDS);
+            return -1;
+        }
+        const int nt = min(kPage, req_len(a, lo) - p * kPage);
+        return (page << 5) | nt;
+    };
+    for (int kk = tid; kk < n_units && kk < kMaxUnits; kk += kThreads) unit_tab[kk] = make_entry(kk);
+    __syncthreads();
+    auto unit_entry = [&](int kk) -> int32_t { return kk < kMaxUnits ? unit_tab[kk] : make_entry(kk); };
+
     if (warp == kConsumerWarps) {
         // ---------------------------- producer ------------------------------------------
         if (lane == 0) {
@@ -173,16 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
                 while (start[b + 1] <= u) ++b;
                 const int s = i % kStages, r = i / kStages;
                 if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1, abort_flag, a.status, 0x31)) break;
-                const int p = (int)(u - start[b]);
-                const int page = a.block_table[(size_t)b * a.max_pages + p];
+                const int32_t entry = unit_entry(i);
                 const uint32_t fb = smem_u32(&full[s]);
-                if (page >= 0 && page < a.num_pages) {
+                if (entry >= 0) {
                     mbar_expect_tx(fb, 2u * page_bytes);
-                    const size_t off = (size_t)page * kPage * a.Hkv * kD;
+                    const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * kD;
                     bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes), a.kc + off, page_bytes, fb);
                     bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes + page_bytes), a.vc + off, page_bytes, fb);
                 } else {
-                    atomicOr(a.status, DEVSTAT_BOUNDS);
                     mbar_arrive(fb);
                 }
             }
@@ -197,19 +223,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
     }
 
     // ---------------------------------- consumers ----------------------------------------
-    const int g = warp;  // KV head of this warp
+    // Warp w serves KV head w / 2 for all G query heads of its group, on tokens
+    // 8 * (w % 2) .. 8 * (w % 2) + 7 of every page: the two warps of a head keep separate
+    // running softmax states and are merged like split partials at the end.
+    const int g = warp >> 1, half = warp & 1;
     const bool active = g < a.Hkv;
-    float* sc = scratch + warp * 32 * G;  // [16 * G] scores (log2 domain)
-    float* sp = sc + 16 * G;              // [16 * G] probabilities
-    constexpr int NV = 16 * G;            // (token, head) values per page
+    float* sc = scratch + warp * 16 * G;  // [8 * G] scores (log2 domain)
+    float* sp = sc + 8 * G;               // [8 * G] probabilities
+    constexpr int NV = 8 * G;             // (token, head) values per half page
     constexpr int NF = NV >= 32 ? NV / 32 : 1;
-    constexpr int NH = NV >= 32 ? NV / 32 : (NV + 31) / 32;  // values per lane in softmax layout
+    constexpr int KH = NV >= 32 ? 5 : (NV == 16 ? 4 : (NV == 8 ? 3 : 2));  // halving steps
+    constexpr int NH = NV >= 32 ? NV / 32 : 1;  // values per lane in the softmax layout
 
-    // Query rows of this group: lane holds dims 4*lane .. 4*lane+3 of each of the G heads.
+    // Query rows: lane holds dims 4*lane .. 4*lane+3 of each of the G heads.
     float qv[G][4];  // loaded when the request changes
     for (int hh = 0; hh < G; ++hh)
         for (int e = 0; e < 4; ++e) qv[hh][e] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G) of this group
+    float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G)
     float acc_o[G][4];
     for (int hh = 0; hh < G; ++hh)
         for (int e = 0; e < 4; ++e) acc_o[hh][e] = 0.f;
@@ -232,56 +262,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
         const int s = i % kStages, r = i / kStages;
         ok = mbar_wait(smem_u32(&full[s]), r & 1, abort_flag, a.status, 0x32);
         if (!ok) break;
-        const int p = (int)(u - start[b]);
-        const int L = req_len(a, b);
-        const int page = a.block_table[(size_t)b * a.max_pages + p];
-        const bool page_ok = page >= 0 && page < a.num_pages;
-        const int nt = page_ok ? min(kPage, L - p * kPage) : 0;
-        if (active) {
-            const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes;
+        const int32_t entry = unit_entry(i);
+        const int nt = (entry >= 0 ? (entry & 31) : 0) - 8 * half;  // valid tokens of this half (may be <= 0)
+        if (active && nt > 0) {
+            const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes + (size_t)8 * half * a.Hkv * kD * 2;
             const uint8_t* vp = kp + page_bytes;
-            // scores: v[t*G + hh] partial over this lane's 4 dims
+            // scores: v[t*G + hh], partial over this lane's 4 dims
             float v[NV];
 #pragma unroll
-            for (int t = 0; t < kPage; ++t) {
+            for (int t = 0; t < 8; ++t) {
                 const uint2 w = *reinterpret_cast<const uint2*>(kp + ((size_t)(t * a.Hkv + g) * kD + 4 * lane) * 2);
                 const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh)
                     v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
             }
-            // butterfly reduce-scatter: halve the value set at lane offsets 16, 8, 4, 2, 1
+            // butterfly reduce-scatter over lane offsets 16, 8, 4, 2, 1: after KH halvings a lane
+            // holds NF values, index (lane >> (5 - KH)) * NF + j; remaining offsets all-reduce.
             int count = NV;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) {
                 if (count > 1) {
-                    const int half = count >> 1;
+                    const int hf = count >> 1;
                     const bool upper = (lane & off) != 0;
 #pragma unroll
                     for (int j = 0; j < NV / 2; ++j) {
-                        if (j < half) {
-                            const float send = upper ? v[j] : v[half + j];
-                            const float keep = upper ? v[half + j] : v[j];
+                        if (j < hf) {
+                            const float send = upper ? v[j] : v[hf + j];
+                            const float keep = upper ? v[hf + j] : v[j];
                             v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
                         }
                     }
-                    count = half;
+                    count = hf;
                 } else {
                     v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
                 }
             }
-            // kept values: index lane*NF + j (NV >= 32) or lane >> 1 (NV == 16)
-            if (NV >= 32) {
+            if ((lane & ((1 << (5 - KH)) - 1)) == 0) {
 #pragma unroll
                 for (int j = 0; j < NF; ++j) {
-                    const int idx = lane * NF + j;
-                    const int t = idx / G;
-                    sc[idx] = t < nt ? v[j] * a.scale_log2 : -INFINITY;
+                    const int idx = (lane >> (5 - KH)) * NF + j;
+                    sc[idx] = idx / G < nt ? v[j] * a.scale_log2 : -INFINITY;
                 }
-            } else if ((lane & 1) == 0) {
-                const int idx = lane >> 1;
-                const int t = idx / G;
-                sc[idx] = t < nt ? v[0] * a.scale_log2 : -INFINITY;
             }
             __syncwarp();
             // softmax layout: lane holds idx = lane + 32*j (head lane % G, token idx / G)
@@ -312,14 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
             m_run = m_new;
             __syncwarp();
             // o update: lane's 4 dims for all G heads
-            float al[G];
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) al[hh] = __shfl_sync(0xffffffffu, alpha, hh);
+            for (int hh = 0; hh < G; ++hh) {
+                const float al = __shfl_sync(0xffffffffu, alpha, hh);
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc_o[hh][e] *= al[hh];
-            for (int t = 0; t < nt; ++t) {
+                for (int e = 0; e < 4; ++e) acc_o[hh][e] *= al;
+            }
+            const int tmax = nt < 8 ? nt : 8;
+            for (int t = 0; t < tmax; ++t) {
                 const uint2 w = *reinterpret_cast<const uint2*>(vp + ((size_t)(t * a.Hkv + g) * kD + 4 * lane) * 2);
                 const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
 #pragma unroll
@@ -332,82 +354,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
 
-        // ---- end of this request inside this CTA: flush -----------------------------
+        // ---- end of this request inside this CTA: write partials, last CTA merges -------
         const long long req_end = start[b + 1];
         if (u + 1 == req_end || u + 1 == u1) {
             const int kf = owner_of(start[b], P, Gc), kl = owner_of(req_end - 1, P, Gc);
-            if (kf == kl) {
-                // the whole request lives in this CTA: normalise and write the output
-                if (active) {
+            // slot of (request b, CTA k, token half): (b + k) * 2 + half
+            float* slot = a.part + ((size_t)(b + k) * 2 + half) * a.Hq * kRowF;
+            if (active) {
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float lh = __shfl_sync(0xffffffffu, l_run, hh);
-                        const float mh = __shfl_sync(0xffffffffu, m_run, hh);
-                        const float inv = lh > 0.f ? 1.f / lh : 0.f;
-                        const int h = g * G + hh;
-                        uint2 w;
-                        w.x = pack_bf16x2(acc_o[hh][0] * inv, acc_o[hh][1] * inv);
-                        w.y = pack_bf16x2(acc_o[hh][2] * inv, acc_o[hh][3] * inv);
-                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + h) * kD + 4 * lane) = w;
-                        if (lane == 0)
-                            a.lse[(size_t)b * a.Hq + h] = lh > 0.f ? (mh + __log2f(lh)) * 0.69314718055994531f : -INFINITY;
+                for (int hh = 0; hh < G; ++hh) {
+                    float* row = slot + (size_t)(g * G + hh) * kRowF;
+                    *reinterpret_cast<float4*>(row + 4 * lane) =
+                        make_float4(acc_o[hh][0], acc_o[hh][1], acc_o[hh][2], acc_o[hh][3]);
+                    if (lane == hh) {
+                        row[kD] = m_run;
+                        row[kD + 1] = l_run;
                     }
                 }
-            } else {
-                float* slot = a.part + (size_t)(b + k) * a.Hq * kRowF;
-                if (active) {
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const int h = g * G + hh;
-                        float* row = slot + (size_t)h * kRowF;
-                        *reinterpret_cast<float4*>(row + 4 * lane) =
-                            make_float4(acc_o[hh][0], acc_o[hh][1], acc_o[hh][2], acc_o[hh][3]);
-                        if (lane == hh) {
-                            row[kD] = m_run;
-                            row[kD + 1] = l_run;
-                        }
-                    }
-                }
-                __threadfence();
-                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-                if (tid == 0) {
-                    const int prev = atomicAdd(&a.counters[b], 1);
-                    *last_flag = prev == kl - kf;
-                }
-                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-                if (*last_flag) {
-                    __threadfence();
-                    // merge the partials of CTAs kf..kl for every (head, dim)
-                    for (int idx = tid; idx < a.Hq * (kD / 4); idx += kConsumerWarps * 32) {
-                        const int h = idx / (kD / 4), d4 = idx % (kD / 4);
-                        float M = -INFINITY;
-                        for (int kk = kf; kk <= kl; ++kk) {
-                            const float* row = a.part + ((size_t)(b + kk) * a.Hq + h) * kRowF;
-                            M = fmaxf(M, __ldcg(row + kD));
-                        }
-                        const float Mu = M == -INFINITY ? 0.f : M;
-                        float Ls = 0.f;
-                        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int kk = kf; kk <= kl; ++kk) {
-                            const float* row = a.part + ((size_t)(b + kk) * a.Hq + h) * kRowF;
-                            const float mk = __ldcg(row + kD);
-                            const float wgt = mk == -INFINITY ? 0.f : fast_exp2(mk - Mu);
-                            Ls += wgt * __ldcg(row + kD + 1);
-                            const float4 ov = __ldcg(reinterpret_cast<const float4*>(row) + d4);
-                            O.x += wgt * ov.x, O.y += wgt * ov.y, O.z += wgt * ov.z, O.w += wgt * ov.w;
-                        }
-                        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                        uint2 w;
-                        w.x = pack_bf16x2(O.x * inv, O.y * inv);
-                        w.y = pack_bf16x2(O.z * inv, O.w * inv);
-                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + h) * kD + 4 * d4) = w;
-                        if (d4 == 0)
-                            a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-                    }
-                    if (tid == 0) a.counters[b] = 0;
-                }
-                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             }
+            __threadfence();
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            if (tid == 0) {
+                const int prev = atomicAdd(&a.counters[b], 1);
+                *last_flag = prev == kl - kf;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+            if (*last_flag) {
+                __threadfence();
+                // merge the partials of CTAs kf..kl (both token halves) for every (head, dim)
+                const int nslots = 2 * (kl - kf + 1);
+                for (int idx = tid; idx < a.Hq * (kD / 4); idx += kConsumerWarps * 32) {
+                    const int h = idx / (kD / 4), d4 = idx % (kD / 4);
+                    float M = -INFINITY;
+                    for (int q = 0; q < nslots; ++q) {
+                        const float* row = a.part + ((size_t)(b + kf) * 2 + q) * a.Hq * kRowF + (size_t)h * kRowF;
+                        M = fmaxf(M, __ldcg(row + kD));
+                    }
+                    const float Mu = M == -INFINITY ? 0.f : M;
+                    float Ls = 0.f;
+                    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int q = 0; q < nslots; ++q) {
+                        const float* row = a.part + ((size_t)(b + kf) * 2 + q) * a.Hq * kRowF + (size_t)h * kRowF;
+                        const float mk = __ldcg(row + kD);
+                        const float wgt = mk == -INFINITY ? 0.f : fast_exp2(mk - Mu);
+                        Ls += wgt * __ldcg(row + kD + 1);
+                        const float4 ov = __ldcg(reinterpret_cast<const float4*>(row) + d4);
+                        O.x += wgt * ov.x, O.y += wgt * ov.y, O.z += wgt * ov.z, O.w += wgt * ov.w;
+                    }
+                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+                    uint2 w;
+                    w.x = pack_bf16x2(O.x * inv, O.y * inv);
+                    w.y = pack_bf16x2(O.z * inv, O.w * inv);
+                    *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + h) * kD + 4 * d4) = w;
+                    if (d4 == 0)
+                        a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                }
+                if (tid == 0) a.counters[b] = 0;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             // reset the running state for the next request
             m_run = -INFINITY, l_run = 0.f;
             for (int hh = 0; hh < G; ++hh)
@@ -419,10 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
 }  // namespace
 
 size_t decode_smem_bytes(int Hkv) {
-    return 1024 + (size_t)kStages * 2 * kPage * Hkv * kD * 2 + (kMaxB + 8) * 4 + kConsumerWarps * 32 * 8 * 4 + 256;
+    return 1024 + (size_t)kStages * 2 * kPage * Hkv * kD * 2 + (kMaxB + 8) * 4 + (size_t)kConsumerWarps * 16 * 8 * 4 +
+           256 + kMaxUnits * 4;
 }
 
-int decode_max_grid() { return 512; }
+int decode_max_grid() { return 256; }
 int decode_row_floats() { return kRowF; }
 
 cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {

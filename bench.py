@@ -262,8 +262,9 @@ def bench_ours(args, rank, world, pg):
 
     # ---- end to end through the C ABI with host buffers ---------------------------------------
     if args.no_e2e:
+        extra = None if args.no_extra else bench_extra(args, attn, synth, peaks, peak_src, clocks)
         return finish(args, rank, world, p, attn, value, ms_step_max, roofline, None, launches, clocks, finite,
-                      props, peaks, peak_src, None)
+                      props, peaks, peak_src, extra)
     hq, hk, hv, hdo = (to_dev(x, pin=True) for x in (p.q, p.k, p.v, p.do))
     ho = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()

@@ -155,7 +155,7 @@ ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, con
  * keeps until the process exits. It allocates nothing and calls no allocating routine.
  *   Arguments, layouts and results are those of attn_decode_paged.
  *   Limit: attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, 0, max_pages) must
- *   not exceed attn_decode_paged_noalloc_max_bytes() (e.g. Hq = 32 allows B up to 480);
+ *   not exceed attn_decode_paged_noalloc_max_bytes() (e.g. Hq = 32 allows B up to 240);
  *   larger problems are rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
  *   The first call made while a given device is current looks up the buffer's device
  *   address (cudaGetSymbolAddress) for that device; make that first call before any
