@@ -9,18 +9,21 @@
 // 256-wide half of the output columns (D = 512 runs two CTAs per tile, each recomputing
 // the full-width scores; D = 256 runs one). Tensor memory (512 columns x 128 lanes):
 //   cols [0, 256)   O accumulator, fp32, row i = lane i
-//   cols [256, 384) S buffer 0, [384, 512) S buffer 1 (double-buffered scores)
-// Shared memory: the Q tile (resident), a ring of 32 KB slots (one slot = 128 rows x
-// 128 columns of K or V as two 128-byte-swizzled 64-column sub-tiles, filled by TMA),
-// and the bf16 P tile written by the softmax warps.
+//   cols [256, 384) S buffer 0, [384, 512) S buffer 1 (double-buffered scores); once a
+//                   buffer's scores are in registers, the bf16 P tile of that step is written
+//                   over its first 64 columns and read from there as the A operand of P V
+// Shared memory: the Q tile (resident) and a ring of 32 KB slots (one slot = 128 rows x
+// 128 columns of K or V as two 128-byte-swizzled 64-column sub-tiles, filled by TMA):
+// 5 slots at D = 256, 3 at D = 512.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer (one thread): Q once, then K/V slots in MMA order
 //   warp 1      TMEM owner; one thread issues every UMMA and commit
 //   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Masking, fp32 online
 //               softmax in the log2 domain with lazy rescaling (the running max moves
-//               only when a tile's max exceeds it by more than 2^8), P -> smem, O
-//               rescale in TMEM, and the epilogue (O / l -> bf16, lse).
+//               only when a tile's max exceeds it by more than 2^8), P -> TMEM, O
+//               rescale in TMEM (only then do they wait for the previous P V), and the
+//               epilogue (O / l -> bf16, lse).
 // KV tiles outside the causal / window range are never loaded (tile-granular skipping);
 // only tiles that straddle the diagonal, the window edge or the sequence end are masked.
 #include <cuda_runtime.h>
@@ -41,11 +44,10 @@ template <int DQK>
 struct FwdCfg {
     static constexpr int kQChunks = DQK / 128;  // 32 KB slots per K tile
     static constexpr int kVChunks = kDV / 128;  // 32 KB slots per V half-tile
-    static constexpr int kStages = DQK == 256 ? 4 : 2;
+    static constexpr int kStages = DQK == 256 ? 5 : 3;
     static constexpr uint32_t kQBytes = DQK * 256;  // 128 rows x DQK bf16
     static constexpr uint32_t kOffSlots = kQBytes;
-    static constexpr uint32_t kOffP = kOffSlots + kStages * kSlotBytes;
-    static constexpr uint32_t kOffBar = kOffP + kSlotBytes;
+    static constexpr uint32_t kOffBar = kOffSlots + kStages * kSlotBytes;
     static constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
 };
 
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sQ = sbase, sSlots = sbase + C::kOffSlots, sP = sbase + C::kOffP;
+    const uint32_t sQ = sbase, sSlots = sbase + C::kOffSlots;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* full = bars;                     // [kStages]
     uint64_t* empty = bars + C::kStages;       // [kStages]
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------- UMMA issuer -----------------------------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // Q K^T: both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);   // P V: V is N-major
+            constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);   // P (TMEM) V: V is N-major
             int slot = 0, round = 0;
             bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.status, 0x12);
             tc_fence_after();
@@ -205,10 +207,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kVChunks; ++c) {
                     if (!next_slot()) return false;
                     const uint32_t vslot = sSlots + slot * kSlotBytes;
-                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-                        const uint64_t ad = sdesc_sw128(sP + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024);
+                    const uint32_t tP = tS0 + (j & 1) * 128;  // P of step j, packed bf16 pairs
+                    for (int kk = 0; kk < 8; ++kk) {          // 16 keys per step
                         const uint64_t bd = sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
-                        umma_bf16_ss(tO + c * 128, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(tO + c * 128, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     release_slot();
                 }
@@ -282,36 +284,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c >> 1] = pack_bf16x2(p0, p1);
             }
             l = l * alpha + rowsum;
-            if (j > 0) {
-                // P(j-1) V(j-1) must be complete: it reads sP and writes O
+            if (j > 0 && __any_sync(0xffffffffu, moved)) {
+                // rescale O: P(j-1) V(j-1) must be complete (phase j-2 is, by s_full(j))
                 ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done), (j - 1) & 1, abort_flag, a.status, 0x16));
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, moved)) {
-                    const float f = moved ? alpha : 1.f;
+                const float f = moved ? alpha : 1.f;
 #pragma unroll 1
-                    for (int c = 0; c < kDV / 32; ++c) {
-                        uint32_t raw[32];
-                        tmem_ld32(tO + c * 32 + lane_base, raw);
-                        tmem_ld_wait();
+                for (int c = 0; c < kDV / 32; ++c) {
+                    uint32_t raw[32];
+                    tmem_ld32(tO + c * 32 + lane_base, raw);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
-                        tmem_st32(tO + c * 32 + lane_base, raw);
-                    }
-                    tmem_st_wait();
+                    for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
+                    tmem_st32(tO + c * 32 + lane_base, raw);
                 }
             }
-            // P row r -> sP (K-major, 128-byte swizzle): 16 chunks of 8 keys
+            // P row r -> the first 64 columns of this step's S buffer (S is in registers)
+            {
+                uint32_t w[32];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const uint32_t addr = sP + (u >> 3) * kSubBytes + sw128_offset(r, (u & 7) * 8);
-                st_shared_v4(addr, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                for (int e = 0; e < 32; ++e) w[e] = pk[e];
+                tmem_st32(tS0 + buf * 128 + lane_base, w);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) w[e] = pk[32 + e];
+                tmem_st32(tS0 + buf * 128 + 32 + lane_base, w);
             }
-            fence_proxy_async_smem();
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(p_full));
         }
         // ---- epilogue: O / l -> bf16, lse -------------------------------------------------
+        // the last two P V (phases n-2, n-1); earlier ones are complete by s_full(n-1)
+        if (ok && n >= 2) ok = mbar_wait(smem_u32(pv_done), (n - 2) & 1, abort_flag, a.status, 0x17);
         if (ok) ok = mbar_wait(smem_u32(pv_done), (n - 1) & 1, abort_flag, a.status, 0x17);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
