@@ -72,11 +72,11 @@ const DeviceInfo* device_info() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 4-D map over a [batch, rows, heads, dim] bf16 tensor, box = 64 dims x 1 head x 128 rows.
-bool make_map(CUtensorMap* m, const void* base, int D, int H, int rows, int batch) {
+// 4-D map over a [batch, rows, heads, dim] bf16 tensor, box = 64 dims x 1 head x box_rows rows.
+bool make_map(CUtensorMap* m, const void* base, int D, int H, int rows, int batch, int box_rows = 128) {
     cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)rows, (cuuint64_t)batch};
     cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)rows * H * D * 2};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -320,7 +320,9 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
     std::memset(&L, 0, sizeof(L));
     const int map_rows = varlen ? (int)rows : S, batch = varlen ? 1 : B;
     if (!make_map(&L.tq, q, D, Hq, map_rows, batch) || !make_map(&L.tk, k, D, Hkv, map_rows, batch) ||
-        !make_map(&L.tv, v, D, Hkv, map_rows, batch) || !make_map(&L.tdo, dO, D, Hq, map_rows, batch))
+        !make_map(&L.tv, v, D, Hkv, map_rows, batch) || !make_map(&L.tdo, dO, D, Hq, map_rows, batch) ||
+        !make_map(&L.tqh, q, D, Hq, map_rows, batch, 256 * 128 / D) ||
+        !make_map(&L.tdoh, dO, D, Hq, map_rows, batch, 256 * 128 / D))
         return ATTN_ERR_LAUNCH;
     L.q = q, L.k = k, L.v = v, L.o = o, L.dO = dO, L.lse = lse, L.dQ = dQ, L.dK = dK, L.dV = dV;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

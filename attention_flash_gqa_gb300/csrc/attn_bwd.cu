@@ -10,19 +10,25 @@
 //
 // Kernels:
 //  1. bwd_prep: Delta per query row (fp32) and zeroing of the fp32 dQ accumulator.
-//  2. bwd_main: one CTA per (KV tile of 128 keys, KV head, 128-wide slice of D). It
-//     loops over every query head of the GQA group and every query tile that can see
-//     its keys (causal / window tile skipping), so dK and dV are summed over the group
-//     in tensor memory without atomics. Tensor memory (512 columns):
-//       [0, 128)   S = Q K^T (queries on lanes); reused for the dQ slice dS K_c
-//       [128, 256) dP = dO V^T; the softmax warps move dP(t) into registers first, so
-//                  the MMA can compute dP(t+1) while they work on step t
-//       [256, 384) dV_c accumulator (keys on lanes), [384, 512) dK_c accumulator
-//     S and dP contract over the full D, so each of the D/128 slice CTAs recomputes
-//     them; dV_c, dK_c and dQ_c are each computed once. dQ_c leaves TMEM after every
-//     query tile and is added into the fp32 accumulator with vector atomics.
-//     The softmax warps write P and dS (bf16) to shared memory; the same tiles serve
-//     as the MN-major A operand of P^T dO_c / dS^T Q_c and the K-major A of dS K_c.
+//  2. bwd_main: one thread-block cluster per (KV tile of 128 keys, KV head); its
+//     NC = D / 128 CTAs each own one 128-wide column slice c of D and accumulate dV_c
+//     and dK_c for the tile in tensor memory while looping over every query head of the
+//     GQA group and every query tile that can see the keys (causal / window tile
+//     skipping), so dK and dV are summed over the group without atomics.
+//     The two full-width contractions of a step are split across the cluster instead of
+//     being recomputed per slice: the first NC/2 CTAs ("S role") compute
+//     S^T = K Q^T, the other NC/2 ("dP role") dP^T = V dO^T, each for its own share of
+//     the step's 128 query columns (keys on TMEM lanes). An S-role CTA turns its share
+//     into P^T (bf16) and copies it into every CTA of the cluster; its dP-role partner
+//     (same query share) reads that P^T, forms dS^T = P^T (dP^T - Delta) and copies it
+//     to every CTA. Each CTA then runs its slice of the three gradient products from the
+//     assembled P^T / dS^T tiles in shared memory:
+//       dV_c += P^T dO_c,   dK_c += dS^T Q_c,   dQ_c = dS K_c
+//     dQ_c leaves tensor memory after every step and is added into an fp32 accumulator
+//     with TMA bulk reduce-adds. Consumption of the exchanged tiles is signalled back to
+//     their writers with multicast tcgen05.commit arrivals.
+//     Tensor memory (512 columns): [0,128) dV_c, [128,256) dK_c, [256,384) dQ_c,
+//     [384,512) the role result (two 64-column buffers when NC = 4, one of 128 when 2).
 //  3. bwd_finalize: dQ accumulator -> bf16.
 #include <cuda_runtime.h>
 
@@ -36,22 +42,40 @@ namespace {
 
 constexpr int kB = 128;  // query tile = key tile = 128 rows
 constexpr int kThreads = 192;
-constexpr uint32_t kSlotBytes = 32768;
-constexpr uint32_t kSubBytes = 16384;
-constexpr int kStages = 5;
-constexpr uint32_t kOffP = kStages * kSlotBytes;
-constexpr uint32_t kOffDS = kOffP + kSlotBytes;
-constexpr uint32_t kOffBar = kOffDS + kSlotBytes;
-constexpr uint32_t kSmem = kOffBar + 256 + 1024;
+constexpr uint32_t kSlot = 16384;   // ring slot: one 128 x 64 bf16 sub-tile
+constexpr uint32_t kSub = 16384;    // 128 rows x 128 bytes, 128-byte swizzle
+constexpr int kStages = 6;
+constexpr uint32_t kOffP = 0;                      // P^T   [128 keys x 128 queries] bf16, 2 sub-tiles
+constexpr uint32_t kOffDS = kOffP + 2 * kSub;      // dS^T  same layout
+constexpr uint32_t kOffKc = kOffDS + 2 * kSub;     // K_c   [128 keys x 128 dims], resident
+constexpr uint32_t kOffStage = kOffKc + 2 * kSub;  // dQ staging: 2 x (128 rows x 32 fp32)
+constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
+constexpr uint32_t kOffVec = kOffRing + kStages * kSlot;  // lse / Delta of the step, 2 x 128 fp32
+constexpr uint32_t kOffBar = kOffVec + 1024;
+constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // + slack for the 1024-byte alignment
+static_assert(kSmem <= 232448, "shared memory budget");
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+    static constexpr int NC = D / 128;        // cluster size = slices of D
+    static constexpr int NHALF = NC / 2;      // CTAs per role
+    static constexpr int NQ = 128 / NHALF;    // query columns of one role share (128 or 64)
+    static constexpr int RB = NQ == 64 ? 2 : 1;  // role result buffers in tensor memory
+    static constexpr int YPS = 128 / NQ;      // role B-operand sub-tiles per ring slot
+    static constexpr int NSUB = D / 64;       // 64-wide sub-tiles across D
+    static constexpr uint32_t kPieceBytes = 128u * NQ * 2u;  // one role share of P^T or dS^T
+    static constexpr uint32_t kRemoteBytes = (NHALF - 1) * kPieceBytes;  // from the other writers
+};
 
 struct BwdArgs {
     const float* lse;
     const float* delta;
-    float* dq_acc;
     uint16_t *dK, *dV;
     const int32_t* cu_seqlens;
     unsigned* status;
-    int Hq, Hkv, S, D, window, n_kvtiles, nslices, T;
+    int Hq, Hkv, S, window, T;
     float scale, scale_log2;
 };
 
@@ -59,9 +83,15 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tqh, const __grid_constant__ CUtensorMap tdoh,
                     const __grid_constant__ CUtensorMap tdq, BwdArgs a) {
-    constexpr int kChunks = D / 128;  // 32 KB slots per full-width row tile
-    const int g = blockIdx.x / a.nslices, cs = blockIdx.x % a.nslices;
+    using C = Cfg<D>;
+    const uint32_t rank = cluster_ctarank();
+    const int g = blockIdx.x / C::NC;  // KV head
+    const bool s_role = rank < (uint32_t)C::NHALF;
+    const int share = s_role ? (int)rank : (int)rank - C::NHALF;  // query share of the role work
+    const uint32_t partner = s_role ? rank + C::NHALF : rank - C::NHALF;
+    const int c0 = (int)rank * 128;  // this CTA's column slice of D
     const int seq = blockIdx.y;
     const int kv_tile = blockIdx.z;  // tile 0 sees the most queries: launched first
     int seq_start = 0, L = a.S, bcoord = seq;
@@ -71,30 +101,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         bcoord = 0;
     }
     const int k0 = kv_tile * kB;
-    if (k0 >= L) return;
+    if (k0 >= L) return;  // the same for every CTA of the cluster
     const int G = a.Hq / a.Hkv;
     const int q_last = a.window > 0 ? min(L, k0 + kB - 1 + a.window) : L;  // exclusive bound on queries
     const int i_begin = k0 / kB, i_end = (q_last + kB - 1) / kB;
     const int n_qt = i_end - i_begin;
     const int n = G * n_qt;  // steps: (head, query tile)
-    const int c0 = cs * 128;  // this CTA's column slice of D
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sSlots = sbase, sP = sbase + kOffP, sDS = sbase + kOffDS;
+    const uint32_t sP = sbase + kOffP, sDS = sbase + kOffDS, sKc = sbase + kOffKc, sStage = sbase + kOffStage;
+    const uint32_t sRing = sbase + kOffRing;
+    float* vec = reinterpret_cast<float*>(smem + kOffVec);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
-    uint64_t* s_full = bars + 2 * kStages;  // S(t) complete
-    uint64_t* dp_full = s_full + 1;          // dP(t) complete
-    uint64_t* dp_free = dp_full + 1;         // dP(t) read out of TMEM by the softmax warps
-    uint64_t* p_full = dp_free + 1;
-    uint64_t* dq_full = p_full + 1;
+    uint64_t* r_full = bars + 2 * kStages;  // role result in TMEM complete [RB]
+    uint64_t* r_free = r_full + 2;          // role result read out by the softmax warps [RB]
+    uint64_t* p_full = r_free + 2;          // all of P^T(t) present in this CTA's shared memory
+    uint64_t* ds_full = p_full + 1;         // all of dS^T(t) present
+    uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share is done
+    uint64_t* ds_free = p_free + 1;         // (dP role) every reader of this CTA's dS^T share is done
+    uint64_t* dq_full = ds_free + 1;
     uint64_t* dq_free = dq_full + 1;
-    uint64_t* stage_full = dq_free + 1;   // all 128 dQ rows staged in smem
-    uint64_t* stage_free = stage_full + 1; // the previous step's reduce has read the staging smem
-    uint64_t* mma_idle = stage_free + 1;
+    uint64_t* kc_full = dq_free + 1;
+    uint64_t* mma_idle = kc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -104,27 +136,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        mbar_init(smem_u32(s_full), 1);
-        mbar_init(smem_u32(dp_full), 1);
-        mbar_init(smem_u32(dp_free), 128);
-        mbar_init(smem_u32(p_full), 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&r_full[b]), 1);
+            mbar_init(smem_u32(&r_free[b]), 128);
+        }
+        // exchange barriers: one arming arrive (with the bytes expected from other CTAs)
+        // plus, for the share this CTA writes itself, its 128 writer threads
+        mbar_init(smem_u32(p_full), 1 + (s_role ? 128 : 0));
+        mbar_init(smem_u32(ds_full), 1 + (s_role ? 0 : 128));
+        // one multicast commit from every CTA's MMA, plus the partner's 128 readers of P^T
+        mbar_init(smem_u32(p_free), C::NC + 128);
+        mbar_init(smem_u32(ds_free), C::NC);
         mbar_init(smem_u32(dq_full), 1);
         mbar_init(smem_u32(dq_free), 128);
-        mbar_init(smem_u32(stage_full), 128);
-        mbar_init(smem_u32(stage_free), 1);
+        mbar_init(smem_u32(kc_full), 1);
         mbar_init(smem_u32(mma_idle), 1);
         *abort_flag = 0;
         fence_mbar_init();
+        // arm phase 0 of the exchange barriers (later phases are armed by the MMA issuer)
+        mbar_expect_tx(smem_u32(p_full), s_role ? C::kRemoteBytes : C::NHALF * C::kPieceBytes);
+        mbar_expect_tx(smem_u32(ds_full), s_role ? C::NHALF * C::kPieceBytes : C::kRemoteBytes);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     __syncthreads();
+    cluster_sync_all();  // every CTA's barriers are initialised before any peer signals them
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t tS = tbase, tDP = tbase + 128, tDV = tbase + 256, tDK = tbase + 384;
+    const uint32_t tDV = tbase, tDK = tbase + 128, tDQ = tbase + 256, tR = tbase + 384;
     const int krow = seq_start + k0;
+    const uint32_t p_rem = s_role ? C::kRemoteBytes : C::NHALF * C::kPieceBytes;
+    const uint32_t ds_rem = s_role ? C::NHALF * C::kPieceBytes : C::kRemoteBytes;
 
     if (warp == 0) {
         // ---------------------------------- producer -------------------------------------
@@ -133,292 +177,338 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             prefetch_tmap(&tdo);
+            prefetch_tmap(&tqh);
+            prefetch_tmap(&tdoh);
+            // resident K_c (B operand of dQ_c = dS K_c)
+            mbar_expect_tx(smem_u32(kc_full), 2 * kSub);
+            tma_load_4d(sKc, &tk, smem_u32(kc_full), c0, g, krow, bcoord);
+            tma_load_4d(sKc + kSub, &tk, smem_u32(kc_full), c0 + 64, g, krow, bcoord);
             int slot = 0, round = 0;
-            auto load = [&](const CUtensorMap* map, int head, int col0, int row0) -> bool {
-                if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x21)) return false;
-                const uint32_t fb = smem_u32(&full[slot]);
-                mbar_expect_tx(fb, kSlotBytes);
-                const uint32_t dst = sSlots + slot * kSlotBytes;
-                tma_load_4d(dst, map, fb, col0, head, row0, bcoord);
-                tma_load_4d(dst + kSubBytes, map, fb, col0 + 64, head, row0, bcoord);
+            auto next = [&](uint32_t& dst, uint32_t& fb) -> bool {
+                if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x21))
+                    return false;
+                fb = smem_u32(&full[slot]);
+                mbar_expect_tx(fb, kSlot);
+                dst = sRing + slot * kSlot;
                 if (++slot == kStages) slot = 0, ++round;
                 return true;
             };
-            auto load_dp = [&](int t) -> bool {  // dP = dO V^T operands, chunk pairs
-                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
-                for (int c = 0; c < kChunks; ++c) {
-                    if (!load(&tdo, h, c * 128, qrow)) return false;
-                    if (!load(&tv, g, c * 128, krow)) return false;
+            const CUtensorMap* X = s_role ? &tk : &tv;    // role A operand: the key tile, full width
+            const CUtensorMap* Y = s_role ? &tqh : &tdoh; // role B operand: this share's query rows
+            auto load_role = [&](int t) -> bool {
+                const int h = g * G + t / n_qt;
+                const int yrow = seq_start + (i_begin + t % n_qt) * kB + share * C::NQ;
+                for (int u = 0; u < C::NSUB; ++u) {
+                    uint32_t dst, fb;
+                    if (!next(dst, fb)) return false;
+                    tma_load_4d(dst, X, fb, 64 * u, g, krow, bcoord);
+                    if (u % C::YPS == 0) {
+                        if (!next(dst, fb)) return false;
+                        for (int v = 0; v < C::YPS; ++v)
+                            tma_load_4d(dst + v * (C::NQ * 128), Y, fb, 64 * (u + v), h, yrow, bcoord);
+                    }
                 }
                 return true;
             };
-            auto load_s = [&](int t) -> bool {  // S = Q K^T operands, chunk pairs
+            auto load_grad = [&](int t) -> bool {  // B operands of dV_c and dK_c
                 const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
-                for (int c = 0; c < kChunks; ++c) {
-                    if (!load(&tq, h, c * 128, qrow)) return false;
-                    if (!load(&tk, g, c * 128, krow)) return false;
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t dst, fb;
+                    if (!next(dst, fb)) return false;
+                    tma_load_4d(dst, &tdo, fb, c0 + 64 * e, h, qrow, bcoord);
+                }
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t dst, fb;
+                    if (!next(dst, fb)) return false;
+                    tma_load_4d(dst, &tq, fb, c0 + 64 * e, h, qrow, bcoord);
                 }
                 return true;
             };
-            auto load_grad = [&](int t) -> bool {  // B operands of dV_c, dK_c, dQ_c
-                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
-                return load(&tdo, h, c0, qrow) && load(&tq, h, c0, qrow) && load(&tk, g, c0, krow);
-            };
-            // Q and dO tiles are new every step and mostly miss L2 (they are re-read by every
-            // key tile of the head group, long after): warm L2 with them two steps ahead so the
-            // ring's copies find them there.
+            // Q and dO tiles are new every step and mostly miss L2: warm it with this CTA's
+            // future operands two steps ahead.
             constexpr int kAhead = 2;
-            auto prefetch_q_do = [&](int t) {
+            auto prefetch = [&](int t) {
                 if (t >= n) return;
                 const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
-                for (int c = 0; c < D; c += 64) {
-                    tma_prefetch_4d(&tq, c, h, qrow, bcoord);
-                    tma_prefetch_4d(&tdo, c, h, qrow, bcoord);
-                }
+                const CUtensorMap* Ym = s_role ? &tq : &tdo;
+                for (int c = 0; c < D; c += 64) tma_prefetch_4d(Ym, c, h, qrow, bcoord);
+                tma_prefetch_4d(s_role ? &tdo : &tq, c0, h, qrow, bcoord);
+                tma_prefetch_4d(s_role ? &tdo : &tq, c0 + 64, h, qrow, bcoord);
             };
-            for (int t = 1; t <= kAhead; ++t) prefetch_q_do(t);
-            // the UMMA issuer's consumption order: dP(0) S(0) | dP(t+1) grad(t) S(t+1) | ...
-            bool ok = load_dp(0) && load_s(0);
+            for (int t = 1; t <= kAhead; ++t) prefetch(t);
+            // consumption order of the UMMA issuer: role(0) | role(t+1) grad(t) | ...
+            bool ok = load_role(0);
             for (int t = 0; ok && t < n; ++t) {
-                prefetch_q_do(t + 1 + kAhead);
-                if (t + 1 < n) ok = load_dp(t + 1);
+                prefetch(t + 1 + kAhead);
+                if (t + 1 < n) ok = load_role(t + 1);
                 ok = ok && load_grad(t);
-                if (ok && t + 1 < n) ok = load_s(t + 1);
             }
             const int issued = round * kStages + slot;
             for (int s = 0; s < kStages && s < issued; ++s) {
                 const int last = s + ((issued - 1 - s) / kStages) * kStages;
                 mbar_drain(smem_u32(&full[s]), (last / kStages) & 1, a.status, 0x27);
             }
+            mbar_drain(smem_u32(kc_full), 0, a.status, 0x2e);
         }
     } else if (warp == 1) {
         // --------------------------------- UMMA issuer -----------------------------------
         if (lane == 0) {
-            constexpr uint32_t idKK = idesc_bf16_f32(128, 128, false, false);  // S, dP, (dQ uses idKN)
-            constexpr uint32_t idMN = idesc_bf16_f32(128, 128, true, true);    // dV, dK: A^T and B N-major
-            constexpr uint32_t idKN = idesc_bf16_f32(128, 128, false, true);   // dQ: dS K-major, K_c N-major
+            constexpr uint32_t idRole = idesc_bf16_f32(128, C::NQ, false, false);  // K tile x query rows
+            constexpr uint32_t idG = idesc_bf16_f32(128, 64, false, true);  // P^T / dS^T K-major, B N-major
+            constexpr uint32_t idQ = idesc_bf16_f32(128, 128, true, true);  // dS (MN-major) x K_c (N-major)
+            const uint16_t mask_s = (uint16_t)((1u << C::NHALF) - 1u);       // writers of P^T
+            const uint16_t mask_d = (uint16_t)(mask_s << C::NHALF);          // writers of dS^T
             int slot = 0, round = 0;
-            bool ok = true;
-            // Waits for the current slot; on success returns true and its address in `addr`.
-            auto acquire = [&](uint32_t& addr) -> bool {
+            auto acquire = [&](uint32_t& addr, int& s) -> bool {
                 if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x22)) return false;
                 tc_fence_after();
-                addr = sSlots + slot * kSlotBytes;
-                return true;
-            };
-            auto release = [&]() {
-                umma_commit(smem_u32(&empty[slot]));
+                addr = sRing + slot * kSlot;
+                s = slot;
                 if (++slot == kStages) slot = 0, ++round;
-            };
-            // full-width contraction of two row tiles streamed as (A chunk, B chunk) pairs
-            auto contract = [&](uint32_t dst) -> bool {
-                for (int c = 0; c < kChunks; ++c) {
-                    uint32_t sa, sb;
-                    if (!acquire(sa)) return false;
-                    const int sa_slot = slot;
-                    if (++slot == kStages) slot = 0, ++round;
-                    if (!acquire(sb)) return false;
-                    for (int sub = 0; sub < 2; ++sub)
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sdesc_sw128(sa + sub * kSubBytes + kk * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(sb + sub * kSubBytes + kk * 32, 16, 1024);
-                            umma_bf16_ss(dst, ad, bd, idKK, (c | sub | kk) ? 1u : 0u);
-                        }
-                    umma_commit(smem_u32(&empty[sa_slot]));
-                    release();
-                }
                 return true;
             };
-            ok = contract(tDP);
-            if (ok) umma_commit(smem_u32(dp_full));
-            ok = ok && contract(tS);
-            if (ok) umma_commit(smem_u32(s_full));
-            for (int t = 0; ok && t < n; ++t) {
-                if (t + 1 < n) {
-                    // dP(t+1) overwrites the dP columns as soon as the softmax warps hold dP(t)
-                    // in registers, overlapping their work on step t.
-                    ok = mbar_wait(smem_u32(dp_free), t & 1, abort_flag, a.status, 0x29);
-                    if (!ok) break;
+            auto role = [&](int t) -> bool {
+                const int b = t % C::RB;
+                if (t >= C::RB) {
+                    if (!mbar_wait(smem_u32(&r_free[b]), ((t / C::RB) - 1) & 1, abort_flag, a.status, 0x29))
+                        return false;
                     tc_fence_after();
-                    if (!contract(tDP)) { ok = false; break; }
-                    umma_commit(smem_u32(dp_full));
                 }
-                ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x23);
-                if (!ok) break;
+                const uint32_t d = tR + b * C::NQ;
+                uint32_t ya = 0;
+                int ys = 0;
+                for (int u = 0; u < C::NSUB; ++u) {
+                    uint32_t xa;
+                    int xs;
+                    if (!acquire(xa, xs)) return false;
+                    if (u % C::YPS == 0 && !acquire(ya, ys)) return false;
+                    const uint32_t yb = ya + (u % C::YPS) * (C::NQ * 128);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ss(d, sdesc_sw128(xa + kk * 32, 16, 1024), sdesc_sw128(yb + kk * 32, 16, 1024),
+                                     idRole, (u | kk) ? 1u : 0u);
+                    umma_commit(smem_u32(&empty[xs]));
+                    if (u % C::YPS == C::YPS - 1) umma_commit(smem_u32(&empty[ys]));
+                }
+                umma_commit(smem_u32(&r_full[b]));
+                return true;
+            };
+            // acc += A x B over 128 query rows, B = one 128-column slice held as two 64-column
+            // ring sub-tiles (N-major): two N = 64 products per K step of 16 rows
+            auto grad_pair = [&](uint32_t dacc, uint32_t sa, bool acc_in) -> bool {
+                uint32_t b0, b1;
+                int s0, s1;
+                if (!acquire(b0, s0) || !acquire(b1, s1)) return false;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    const uint32_t accf = (acc_in || kk > 0) ? 1u : 0u;
+                    umma_bf16_ss(dacc, ad, sdesc_sw128(b0 + kk * 2048, kSub, 1024), idG, accf);
+                    umma_bf16_ss(dacc + 64, ad, sdesc_sw128(b1 + kk * 2048, kSub, 1024), idG, accf);
+                }
+                umma_commit(smem_u32(&empty[s0]));
+                umma_commit(smem_u32(&empty[s1]));
+                return true;
+            };
+            auto grads = [&](int t) -> bool {
+                if (!mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x23)) return false;
                 tc_fence_after();
-                // dV_c += P^T dO_c
-                uint32_t sb;
-                if (!acquire(sb)) { ok = false; break; }
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sP + kk * 2048, kSubBytes, 1024);
-                    const uint64_t bd = sdesc_sw128(sb + kk * 2048, kSubBytes, 1024);
-                    umma_bf16_ss(tDV, ad, bd, idMN, (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                release();
-                // dK_c += dS^T Q_c
-                if (!acquire(sb)) { ok = false; break; }
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sDS + kk * 2048, kSubBytes, 1024);
-                    const uint64_t bd = sdesc_sw128(sb + kk * 2048, kSubBytes, 1024);
-                    umma_bf16_ss(tDK, ad, bd, idMN, (t > 0 || kk > 0) ? 1u : 0u);
-                }
-                release();
-                // dQ_c = dS K_c  (into the S columns, already read by the softmax warps)
-                if (!acquire(sb)) { ok = false; break; }
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sDS + (kk >> 2) * kSubBytes + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sb + kk * 2048, kSubBytes, 1024);
-                    umma_bf16_ss(tS, ad, bd, idKN, kk > 0 ? 1u : 0u);
-                }
-                release();
+                mbar_expect_tx(smem_u32(p_full), p_rem);  // arm phase t+1
+                if (!grad_pair(tDV, sP, t > 0)) return false;  // dV_c += P^T dO_c
+                umma_commit_multicast(smem_u32(p_free), mask_s);
+                if (!mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x24)) return false;
+                tc_fence_after();
+                mbar_expect_tx(smem_u32(ds_full), ds_rem);
+                if (!grad_pair(tDK, sDS, t > 0)) return false;  // dK_c += dS^T Q_c
+                if (t == 0 && !mbar_wait(smem_u32(kc_full), 0, abort_flag, a.status, 0x2d)) return false;
+                if (t > 0 && !mbar_wait(smem_u32(dq_free), (t - 1) & 1, abort_flag, a.status, 0x25)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)  // dQ_c = dS K_c: queries on lanes, K = keys
+                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024), sdesc_sw128(sKc + kk * 2048, kSub, 1024),
+                                 idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
-                if (t + 1 < n) {
-                    // S(t+1) reuses the S columns once dQ(t) has been read out
-                    ok = mbar_wait(smem_u32(dq_free), t & 1, abort_flag, a.status, 0x24);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (!contract(tS)) { ok = false; break; }
-                    umma_commit(smem_u32(s_full));
-                }
+                umma_commit_multicast(smem_u32(ds_free), mask_d);
+                return true;
+            };
+            bool ok = role(0);
+            for (int t = 0; ok && t < n; ++t) {
+                if (t + 1 < n) ok = role(t + 1);
+                ok = ok && grads(t);
             }
             umma_commit(smem_u32(mma_idle));
             mbar_drain(smem_u32(mma_idle), 0, a.status, 0x28);
         }
     } else {
-        // --------------------------- softmax-gradient warps ------------------------------
+        // ------------------------- elementwise / dQ readout warps ----------------------------
         const int quad = warp & 3;
-        const int r = quad * 32 + lane;
+        const int j = quad * 32 + lane;  // TMEM lane: key row (role, dV, dK) or query row (dQ)
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int kabs = k0 + j;
+        const bool key_ok = kabs < L;
+        const uint32_t partner_p_free = mapa_shared(smem_u32(p_free), partner);
         bool ok = true;
-        uint32_t rdp[128];
-        // dP of a step: whole row into registers, then hand the columns back to the MMA
-        auto load_dp = [&](int t) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x2a))) return false;
+
+        // dQ_c(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory
+        // and add into the fp32 accumulator with TMA bulk reduce-adds (two staging buffers).
+        auto drain_dq = [&](int t) -> bool {
+            bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x26));
             tc_fence_after();
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t tmp[32];
-                tmem_ld32(tDP + c4 * 32 + lane_base, tmp);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) rdp[c4 * 32 + e] = tmp[e];
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(smem_u32(dp_free));
-            return true;
-        };
-        if (n > 0) ok = load_dp(0);
-        for (int t = 0; ok && t < n; ++t) {
             const int h = g * G + t / n_qt;
             const int q0 = (i_begin + t % n_qt) * kB;
-            const int qi = q0 + r;
-            const bool row_ok = qi < L;
-            float lse2 = INFINITY, dlt = 0.f;
-            if (row_ok) {
-                const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qi : ((size_t)seq * a.Hq + h) * a.S + qi;
-                lse2 = a.lse[li] * 1.4426950408889634f;
-                dlt = a.delta[li];
-            }
-            // dP(t) is already in registers (loaded right after step t-1's P/dS, or in the
-            // prologue below for t = 0), so the MMA can compute dP(t+1) meanwhile.
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full), t & 1, abort_flag, a.status, 0x25));
-            if (!ok) break;
-            tc_fence_after();
-            const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) && q0 + kB <= L &&
-                                k0 + kB <= L);
-            if (t > 0) {
-                // sP/sdS double as the dQ staging tile of step t-1: wait until its reduce has read it
-                if (tid == 64) {
-                    bulk_wait_group_read0();
-                    mbar_arrive(smem_u32(stage_free));
-                }
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(stage_free), (t - 1) & 1, abort_flag, a.status, 0x2b));
-                if (!ok) break;
-            }
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t rs[32];
-                tmem_ld32(tS + c4 * 32 + lane_base, rs);
-                tmem_ld_wait();
-                uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p[2], ds[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int key = k0 + c4 * 32 + e + u;
-                        bool allowed = row_ok;
-                        if (edge) allowed = allowed && key <= qi && key < L && (a.window <= 0 || qi - key < a.window);
-                        const float sv = __uint_as_float(rs[e + u]);
-                        p[u] = allowed ? fast_exp2(fmaf(sv, a.scale_log2, -lse2)) : 0.f;
-                        ds[u] = p[u] * (__uint_as_float(rdp[c4 * 32 + e + u]) - dlt);
-                    }
-                    pk[e >> 1] = pack_bf16x2(p[0], p[1]);
-                    dk[e >> 1] = pack_bf16x2(ds[0], ds[1]);
-                }
-                // keys c4*32 .. c4*32+31 -> sub-tile (c4 >> 1), columns (c4 & 1) * 32 ..
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t off = (c4 >> 1) * kSubBytes + sw128_offset(r, (c4 & 1) * 32 + u * 8);
-                    st_shared_v4(sP + off, pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                    st_shared_v4(sDS + off, dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-                }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(smem_u32(p_full));
-            // next step's dP first (its columns are then free for dP(t+2)), then the dQ(t) readout
-            if (t + 1 < n) {
-                ok = load_dp(t + 1);
-                if (!ok) break;
-            }
-            // dQ_c rows: scale and stage in shared memory (the P/dS tiles, free once dQ(t) is
-            // done), then one thread adds the tile into the fp32 accumulator with TMA bulk
-            // reduce-adds that complete in the background.
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x26));
-            if (!ok) break;
-            tc_fence_after();
-            const float f = row_ok ? a.scale : 0.f;  // rows past the sequence end add zeros
+            const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t rq[32];
-                tmem_ld32(tS + c4 * 32 + lane_base, rq);
-                tmem_ld_wait();
-                // box c4: columns 32*c4 .. +31 (128 bytes per row), 128-byte swizzle
-                const uint32_t box = sP + c4 * kSubBytes;
+                const uint32_t buf = sStage + (c4 & 1) * kSub;
+                if (tid == 64) bulk_wait_group_read1();  // the reduce that last read `buf` is done
+                named_bar_sync(2, 128);
+                if (w) {
+                    uint32_t rq[32];
+                    tmem_ld32(tDQ + c4 * 32 + lane_base, rq);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t addr = box + r * 128 + (((uint32_t)j ^ (uint32_t)(r & 7)) << 4);
-                    st_shared_v4(addr, __float_as_uint(__uint_as_float(rq[4 * j]) * f),
-                                 __float_as_uint(__uint_as_float(rq[4 * j + 1]) * f),
-                                 __float_as_uint(__uint_as_float(rq[4 * j + 2]) * f),
-                                 __float_as_uint(__uint_as_float(rq[4 * j + 3]) * f));
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(buf + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 1]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 2]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 3]) * f));
+                }
+                fence_proxy_async_smem();
+                w = named_bar_and(2, 128, w);
+                if (w && tid == 64) {
+                    tma_reduce_add_4d(&tdq, buf, c0 + 32 * c4, h, seq_start + q0, bcoord);
+                    bulk_commit_group();
                 }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(dq_free));
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(stage_full));
-            if (tid == 64) {
-                ok = mbar_wait(smem_u32(stage_full), t & 1, abort_flag, a.status, 0x2c);
-                if (ok) {
-                    const int qrow = a.cu_seqlens ? seq_start + q0 : q0;
-                    for (int c4 = 0; c4 < 4; ++c4)
-                        tma_reduce_add_4d(&tdq, sP + c4 * kSubBytes, c0 + 32 * c4, h, qrow, bcoord);
-                    bulk_commit_group();
+            return w;
+        };
+
+        for (int t = 0; t < n; ++t) {
+            const int h = g * G + t / n_qt;
+            const int q0 = (i_begin + t % n_qt) * kB;
+            const int qb = q0 + share * C::NQ;  // first query of this CTA's share
+            // the share's lse (log2 units; +inf past the end -> P = 0) or Delta
+            float* v = vec + (t & 1) * 128;
+            if (j < C::NQ) {
+                const int qa = qb + j;
+                float x = s_role ? INFINITY : 0.f;
+                if (qa < L) {
+                    const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qa : ((size_t)seq * a.Hq + h) * a.S + qa;
+                    x = s_role ? a.lse[li] * kLog2e : a.delta[li];
                 }
+                v[j] = x;
             }
-            ok = __all_sync(0xffffffffu, ok);
+            named_bar_sync(1, 128);
+            // role result of this step -> registers, then hand its columns back to the MMA
+            const int b = t % C::RB;
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&r_full[b]), (t / C::RB) & 1, abort_flag, a.status, 0x2a));
+            uint32_t rr[C::NQ];
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < C::NQ / 32; ++c) {
+                    uint32_t tmp[32];
+                    tmem_ld32(tR + b * C::NQ + c * 32 + lane_base, tmp);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(&r_free[b]));
+            }
+            uint32_t pk[C::NQ / 2];
+            if (s_role) {
+                // P^T(key j, query qb + c) = exp2(S^T * scale * log2 e - lse2)
+                const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) &&
+                                    q0 + kB <= L && k0 + kB <= L);
+#pragma unroll
+                for (int c = 0; c < C::NQ; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(v + c);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    float p[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int qa = qb + c + u;
+                        bool allowed = true;
+                        if (edge) allowed = key_ok && qa < L && kabs <= qa && (a.window <= 0 || qa - kabs < a.window);
+                        p[u] = allowed ? fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv[u])) : 0.f;
+                    }
+                    pk[c / 2] = pack_bf16x2(p[0], p[1]);
+                    pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
+                }
+                if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(p_free), (t - 1) & 1, abort_flag, a.status, 0x2b));
+            } else {
+                // dS^T = P^T (dP^T - Delta), P^T from the S-role partner
+                ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x2c));
+                if (ok) {
+#pragma unroll
+                    for (int st = 0; st < C::NQ / 64; ++st) {
+                        const uint32_t tile = sP + (share * (C::NQ / 64) + st) * kSub;
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            uint32_t x0, x1, x2, x3;
+                            ld_shared_v4(tile + sw128_offset(j, ch * 8), x0, x1, x2, x3);
+                            const uint32_t pw[4] = {x0, x1, x2, x3};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int c = st * 64 + ch * 8 + 2 * e;
+                                const float p0 = __uint_as_float(pw[e] << 16), p1 = __uint_as_float(pw[e] & 0xffff0000u);
+                                pk[c / 2] = pack_bf16x2(p0 * (__uint_as_float(rr[c]) - v[c]),
+                                                        p1 * (__uint_as_float(rr[c + 1]) - v[c + 1]));
+                            }
+                        }
+                    }
+                }
+                // this thread is done with P^T(t): tell the partner that owns the share
+                mbar_arrive_cluster(partner_p_free);
+                if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
+            }
+            // write this thread's row of the share, then copy the warp's 32 rows to every peer
+            const uint32_t dst = s_role ? sP : sDS;
+            const uint32_t fbar = smem_u32(s_role ? p_full : ds_full);
+            if (ok) {
+#pragma unroll
+                for (int st = 0; st < C::NQ / 64; ++st) {
+                    const uint32_t tile = dst + (share * (C::NQ / 64) + st) * kSub;
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(tile + sw128_offset(j, ch * 8), pk[st * 32 + ch * 4], pk[st * 32 + ch * 4 + 1],
+                                     pk[st * 32 + ch * 4 + 2], pk[st * 32 + ch * 4 + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (uint32_t peer = 0; peer < (uint32_t)C::NC; ++peer) {
+                        if (peer == rank) continue;
+#pragma unroll
+                        for (int st = 0; st < C::NQ / 64; ++st) {
+                            const uint32_t rows = dst + (share * (C::NQ / 64) + st) * kSub + quad * 4096;
+                            bulk_copy_to_peer(mapa_shared(rows, peer), rows, 4096, mapa_shared(fbar, peer));
+                        }
+                    }
+                }
+                mbar_arrive(fbar);
+            }
+            if (t > 0) ok = drain_dq(t - 1) && ok;
+            ok = named_bar_and(3, 128, ok);
             if (!ok) break;
         }
+        if (ok) ok = drain_dq(n - 1);
         if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
+        // every arrival owed to this CTA's exchange barriers has landed before it exits
+        if (ok) {
+            if (s_role) mbar_drain(smem_u32(p_free), (n - 1) & 1, a.status, 0x30);
+            else mbar_drain(smem_u32(ds_free), (n - 1) & 1, a.status, 0x31);
+        }
         // ---- epilogue: dV_c, dK_c rows (keys on lanes) -> bf16 -----------------------------
         // dq_full of the last step implies every earlier UMMA (all dV/dK updates) is done.
         tc_fence_after();
-        const int kj = k0 + r;
-        const bool key_ok = kj < L;
+        ok = __all_sync(0xffffffffu, ok);
         if (ok) {  // warp-uniform: the TMEM loads below are warp collectives
-            const size_t row = (size_t)(a.cu_seqlens ? seq_start + kj : seq * a.S + kj) * a.Hkv + g;
+            const size_t row = (size_t)(a.cu_seqlens ? seq_start + kabs : seq * a.S + kabs) * a.Hkv + g;
             uint16_t* dv_row = a.dV + row * D + c0;
             uint16_t* dk_row = a.dK + row * D + c0;
 #pragma unroll 1
@@ -451,6 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
+    }
+    // no CTA leaves while a peer may still address its shared memory
+    cluster_sync_all();
+    if (*abort_flag) {
+        // after a give-up a peer's copy into this CTA may still be in flight: let it land
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
     }
 }
 
@@ -528,20 +625,31 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
     }
     {
         BwdArgs a;
-        a.lse = L.lse, a.delta = L.delta, a.dq_acc = L.dq_acc, a.dK = L.dK, a.dV = L.dV;
+        a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV;
         a.cu_seqlens = L.cu_seqlens, a.status = L.status;
-        a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.D = D, a.window = L.window;
-        a.n_kvtiles = (L.S + kB - 1) / kB;
-        a.nslices = D / 128;
+        a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.window = L.window;
         a.T = L.total_rows;
         a.scale = L.scale;
-        a.scale_log2 = L.scale * 1.4426950408889634f;
+        a.scale_log2 = L.scale * kLog2e;
         cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
-        dim3 grid(L.Hkv * a.nslices, L.nseq, a.n_kvtiles);
+        constexpr int NC = Cfg<D>::NC;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = NC;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(L.Hkv * NC, L.nseq, (L.S + kB - 1) / kB);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         const ProfMark m = prof_begin(stream, D == 256 ? "bwd_main_d256" : "bwd_main_d512");
-        bwd_main_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+        e = cudaLaunchKernelEx(&cfg, bwd_main_kernel<D>, L.tq, L.tk, L.tv, L.tdo, L.tqh, L.tdoh, L.tdq, a);
         prof_end(stream, m);
+        if (e != cudaSuccess) return e;
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -54,6 +54,7 @@ cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 // ---- backward ---------------------------------------------------------------------------
 struct BwdLaunch {
     CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tqh, tdoh;  // q / dO with a 64 x 1 x (256*128/D) x 1 box: one cluster CTA's query share
     CUtensorMap tdq;  // fp32 dQ accumulator, 4-D [D, Hq, S, B], box 32 x 1 x 128 x 1, 128-byte swizzle
     const uint16_t *q, *k, *v, *o, *dO;
     const float* lse;
