@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "attn_internal.h"
 #include "ptx.cuh"
@@ -50,8 +51,7 @@ constexpr uint32_t kOffDS = kOffP + 2 * kSub;      // dS^T  same layout
 constexpr uint32_t kOffKc = kOffDS + 2 * kSub;     // K_c   [128 keys x 128 dims], resident
 constexpr uint32_t kOffStage = kOffKc + 2 * kSub;  // dQ staging: 2 x (128 rows x 32 fp32)
 constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
-constexpr uint32_t kOffVec = kOffRing + kStages * kSlot;  // lse / Delta of the step, 2 x 128 fp32
-constexpr uint32_t kOffBar = kOffVec + 1024;
+constexpr uint32_t kOffBar = kOffRing + kStages * kSlot;
 constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // + slack for the 1024-byte alignment
 static_assert(kSmem <= 232448, "shared memory budget");
 
@@ -90,7 +90,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int g = blockIdx.x / C::NC;  // KV head
     const bool s_role = rank < (uint32_t)C::NHALF;
     const int share = s_role ? (int)rank : (int)rank - C::NHALF;  // query share of the role work
-    const uint32_t partner = s_role ? rank + C::NHALF : rank - C::NHALF;
     const int c0 = (int)rank * 128;  // this CTA's column slice of D
     const int seq = blockIdx.y;
     const int kv_tile = blockIdx.z;  // tile 0 sees the most queries: launched first
@@ -113,7 +112,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sP = sbase + kOffP, sDS = sbase + kOffDS, sKc = sbase + kOffKc, sStage = sbase + kOffStage;
     const uint32_t sRing = sbase + kOffRing;
-    float* vec = reinterpret_cast<float*>(smem + kOffVec);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
@@ -123,7 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* ds_full = p_full + 1;         // all of dS^T(t) present
     uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share is done
     uint64_t* ds_free = p_free + 1;         // (dP role) every reader of this CTA's dS^T share is done
-    uint64_t* dq_full = ds_free + 1;
+    uint64_t* p_read = ds_free + 1;         // (dP role) the elementwise warps have read P^T(t)
+    uint64_t* dq_full = p_read + 1;
     uint64_t* dq_free = dq_full + 1;
     uint64_t* kc_full = dq_free + 1;
     uint64_t* mma_idle = kc_full + 1;
@@ -144,9 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // plus, for the share this CTA writes itself, its 128 writer threads
         mbar_init(smem_u32(p_full), 1 + (s_role ? 128 : 0));
         mbar_init(smem_u32(ds_full), 1 + (s_role ? 0 : 128));
-        // one multicast commit from every CTA's MMA, plus the partner's 128 readers of P^T
-        mbar_init(smem_u32(p_free), C::NC + 128);
+        // one multicast commit from every CTA's MMA (a dP-role CTA commits only after its
+        // elementwise warps have also read P^T)
+        mbar_init(smem_u32(p_free), C::NC);
         mbar_init(smem_u32(ds_free), C::NC);
+        mbar_init(smem_u32(p_read), 128);
         mbar_init(smem_u32(dq_full), 1);
         mbar_init(smem_u32(dq_free), 128);
         mbar_init(smem_u32(kc_full), 1);
@@ -312,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto grads = [&](int t) -> bool {
                 if (!mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x23)) return false;
+                if (!s_role && !mbar_wait(smem_u32(p_read), t & 1, abort_flag, a.status, 0x32)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(p_full), p_rem);  // arm phase t+1
                 if (!grad_pair(tDV, sP, t > 0)) return false;  // dV_c += P^T dO_c
@@ -346,7 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         const int kabs = k0 + j;
         const bool key_ok = kabs < L;
-        const uint32_t partner_p_free = mapa_shared(smem_u32(p_free), partner);
         bool ok = true;
 
         // dQ_c(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory
@@ -390,18 +391,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int h = g * G + t / n_qt;
             const int q0 = (i_begin + t % n_qt) * kB;
             const int qb = q0 + share * C::NQ;  // first query of this CTA's share
-            // the share's lse (log2 units; +inf past the end -> P = 0) or Delta
-            float* v = vec + (t & 1) * 128;
-            if (j < C::NQ) {
-                const int qa = qb + j;
-                float x = s_role ? INFINITY : 0.f;
-                if (qa < L) {
-                    const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qa : ((size_t)seq * a.Hq + h) * a.S + qa;
-                    x = s_role ? a.lse[li] * kLog2e : a.delta[li];
+            // the share's lse (log2 units; +inf past the end -> P = 0) or Delta: lane l of every
+            // warp holds queries qb + 32 i + l; columns are broadcast with shuffles
+            float vreg[C::NQ / 32];
+            {
+                const float* src = s_role ? a.lse : a.delta;
+                const size_t lbase = a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S;
+#pragma unroll
+                for (int i = 0; i < C::NQ / 32; ++i) {
+                    const int qa = qb + 32 * i + lane;
+                    vreg[i] = qa < L ? (s_role ? src[lbase + qa] * kLog2e : src[lbase + qa]) : (s_role ? INFINITY : 0.f);
                 }
-                v[j] = x;
             }
-            named_bar_sync(1, 128);
             // role result of this step -> registers, then hand its columns back to the MMA
             const int b = t % C::RB;
             ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&r_full[b]), (t / C::RB) & 1, abort_flag, a.status, 0x2a));
@@ -424,21 +425,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P^T(key j, query qb + c) = exp2(S^T * scale * log2 e - lse2)
                 const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) &&
                                     q0 + kB <= L && k0 + kB <= L);
+                // on edge tiles key j sees the queries qa with 0 <= qa - kabs < span
+                int qhi = key_ok ? L : kabs;
+                if (a.window > 0) qhi = min(qhi, kabs + a.window);
+                const unsigned span = qhi > kabs ? (unsigned)(qhi - kabs) : 0u;
+                auto p_row = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < C::NQ; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(v + c);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    float p[4];
+                    for (int c = 0; c < C::NQ; c += 2) {
+                        float p[2];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int qa = qb + c + u;
-                        bool allowed = true;
-                        if (edge) allowed = key_ok && qa < L && kabs <= qa && (a.window <= 0 || qa - kabs < a.window);
-                        p[u] = allowed ? fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv[u])) : 0.f;
+                        for (int u = 0; u < 2; ++u) {
+                            const float lv = __shfl_sync(0xffffffffu, vreg[(c + u) >> 5], (c + u) & 31);
+                            p[u] = fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv));
+                            if (decltype(masked)::value && (unsigned)(qb + c + u - kabs) >= span) p[u] = 0.f;
+                        }
+                        pk[c / 2] = pack_bf16x2(p[0], p[1]);
                     }
-                    pk[c / 2] = pack_bf16x2(p[0], p[1]);
-                    pk[c / 2 + 1] = pack_bf16x2(p[2], p[3]);
-                }
+                };
+                if (edge) p_row(std::true_type{});
+                else p_row(std::false_type{});
                 if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(p_free), (t - 1) & 1, abort_flag, a.status, 0x2b));
             } else {
                 // dS^T = P^T (dP^T - Delta), P^T from the S-role partner
@@ -456,14 +461,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int e = 0; e < 4; ++e) {
                                 const int c = st * 64 + ch * 8 + 2 * e;
                                 const float p0 = __uint_as_float(pw[e] << 16), p1 = __uint_as_float(pw[e] & 0xffff0000u);
-                                pk[c / 2] = pack_bf16x2(p0 * (__uint_as_float(rr[c]) - v[c]),
-                                                        p1 * (__uint_as_float(rr[c + 1]) - v[c + 1]));
+                                const float d0 = __shfl_sync(0xffffffffu, vreg[c >> 5], c & 31);
+                                const float d1 = __shfl_sync(0xffffffffu, vreg[(c + 1) >> 5], (c + 1) & 31);
+                                pk[c / 2] = pack_bf16x2(p0 * (__uint_as_float(rr[c]) - d0),
+                                                        p1 * (__uint_as_float(rr[c + 1]) - d1));
                             }
                         }
                     }
                 }
-                // this thread is done with P^T(t): tell the partner that owns the share
-                mbar_arrive_cluster(partner_p_free);
+                // this thread is done with P^T(t); the MMA issuer waits for all 128 before the
+                // dV product whose commit releases the share to its writer
+                mbar_arrive(smem_u32(p_read));
                 if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
             }
             // write this thread's row of the share, then copy the warp's 32 rows to every peer
