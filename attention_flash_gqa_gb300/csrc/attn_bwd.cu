@@ -26,7 +26,8 @@
 //       dV_c += P^T dO_c,   dK_c += dS^T Q_c,   dQ_c = dS K_c
 //     dQ_c leaves tensor memory after every step and is added into an fp32 accumulator
 //     with TMA bulk reduce-adds. Consumption of the exchanged tiles is signalled back to
-//     their writers with multicast tcgen05.commit arrivals.
+//     their writers with multicast tcgen05.commit arrivals. P^T is double-buffered, so a
+//     share for step t can be written while step t-1's dV products are still pending.
 //     Tensor memory (512 columns): [0,128) dV_c, [128,256) dK_c, [256,384) dQ_c,
 //     [384,512) the role result (two 64-column buffers when NC = 4, one of 128 when 2).
 //  3. bwd_finalize: dQ accumulator -> bf16.
@@ -45,15 +46,7 @@ constexpr int kB = 128;  // query tile = key tile = 128 rows
 constexpr int kThreads = 192;
 constexpr uint32_t kSlot = 16384;   // ring slot: one 128 x 64 bf16 sub-tile
 constexpr uint32_t kSub = 16384;    // 128 rows x 128 bytes, 128-byte swizzle
-constexpr int kStages = 6;
-constexpr uint32_t kOffP = 0;                      // P^T   [128 keys x 128 queries] bf16, 2 sub-tiles
-constexpr uint32_t kOffDS = kOffP + 2 * kSub;      // dS^T  same layout
-constexpr uint32_t kOffKc = kOffDS + 2 * kSub;     // K_c   [128 keys x 128 dims], resident
-constexpr uint32_t kOffStage = kOffKc + 2 * kSub;  // dQ staging: 2 x (128 rows x 32 fp32)
-constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
-constexpr uint32_t kOffBar = kOffRing + kStages * kSlot;
-constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // + slack for the 1024-byte alignment
-static_assert(kSmem <= 232448, "shared memory budget");
+constexpr uint32_t kSmemMax = 232448;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -67,6 +60,20 @@ struct Cfg {
     static constexpr int NSUB = D / 64;       // 64-wide sub-tiles across D
     static constexpr uint32_t kPieceBytes = 128u * NQ * 2u;  // one role share of P^T or dS^T
     static constexpr uint32_t kRemoteBytes = (NHALF - 1) * kPieceBytes;  // from the other writers
+    // Shared memory. At D = 512 the P^T tile is double-buffered (a share for step t can be
+    // written while step t-1's dV products are pending), paid for with one ring slot and one
+    // dQ staging buffer; at D = 256 the deeper ring pays more.
+    static constexpr int PBUF = D == 512 ? 2 : 1;    // P^T buffers
+    static constexpr int STAGEBUF = D == 512 ? 1 : 2;  // dQ staging buffers (128 rows x 32 fp32 each)
+    static constexpr int kStages = D == 512 ? 5 : 6;  // ring slots
+    static constexpr uint32_t kOffP = 0;                              // P^T [128 keys x 128 queries] bf16
+    static constexpr uint32_t kOffDS = kOffP + PBUF * 2 * kSub;       // dS^T, same layout
+    static constexpr uint32_t kOffKc = kOffDS + 2 * kSub;             // K_c [128 keys x 128 dims], resident
+    static constexpr uint32_t kOffStage = kOffKc + 2 * kSub;          // dQ staging
+    static constexpr uint32_t kOffRing = kOffStage + STAGEBUF * kSub;
+    static constexpr uint32_t kOffBar = kOffRing + kStages * kSlot;
+    static constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // + slack for the 1024-byte alignment
+    static_assert(kSmem <= kSmemMax, "shared memory budget");
 };
 
 struct BwdArgs {
@@ -110,17 +117,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t sP = sbase + kOffP, sDS = sbase + kOffDS, sKc = sbase + kOffKc, sStage = sbase + kOffStage;
-    const uint32_t sRing = sbase + kOffRing;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+    const uint32_t sP = sbase + C::kOffP, sDS = sbase + C::kOffDS, sKc = sbase + C::kOffKc, sStage = sbase + C::kOffStage;
+    const uint32_t sRing = sbase + C::kOffRing;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* full = bars;
-    uint64_t* empty = bars + kStages;
-    uint64_t* r_full = bars + 2 * kStages;  // role result in TMEM complete [RB]
+    uint64_t* empty = bars + C::kStages;
+    uint64_t* r_full = bars + 2 * C::kStages;  // role result in TMEM complete [RB]
     uint64_t* r_free = r_full + 2;          // role result read out by the softmax warps [RB]
-    uint64_t* p_full = r_free + 2;          // all of P^T(t) present in this CTA's shared memory
-    uint64_t* ds_full = p_full + 1;         // all of dS^T(t) present
-    uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share is done
-    uint64_t* ds_free = p_free + 1;         // (dP role) every reader of this CTA's dS^T share is done
+    uint64_t* p_full = r_free + 2;          // all of P^T(t) present in buffer t & 1 [2]
+    uint64_t* ds_full = p_full + 2;         // all of dS^T(t) present
+    uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share in buffer b is done [2]
+    uint64_t* ds_free = p_free + 2;         // (dP role) every reader of this CTA's dS^T share is done
     uint64_t* p_read = ds_free + 1;         // (dP role) the elementwise warps have read P^T(t)
     uint64_t* dq_full = p_read + 1;
     uint64_t* dq_free = dq_full + 1;
@@ -131,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
@@ -141,11 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // exchange barriers: one arming arrive (with the bytes expected from other CTAs)
         // plus, for the share this CTA writes itself, its 128 writer threads
-        mbar_init(smem_u32(p_full), 1 + (s_role ? 128 : 0));
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_full[b]), 1 + (s_role ? 128 : 0));
         mbar_init(smem_u32(ds_full), 1 + (s_role ? 0 : 128));
         // one multicast commit from every CTA's MMA (a dP-role CTA commits only after its
         // elementwise warps have also read P^T)
-        mbar_init(smem_u32(p_free), C::NC);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_free[b]), C::NC);
         mbar_init(smem_u32(ds_free), C::NC);
         mbar_init(smem_u32(p_read), 128);
         mbar_init(smem_u32(dq_full), 1);
@@ -155,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
         // arm phase 0 of the exchange barriers (later phases are armed by the MMA issuer)
-        mbar_expect_tx(smem_u32(p_full), s_role ? C::kRemoteBytes : C::NHALF * C::kPieceBytes);
+        for (int b = 0; b < 2; ++b)
+            mbar_expect_tx(smem_u32(&p_full[b]), s_role ? C::kRemoteBytes : C::NHALF * C::kPieceBytes);
         mbar_expect_tx(smem_u32(ds_full), s_role ? C::NHALF * C::kPieceBytes : C::kRemoteBytes);
     }
     if (warp == 1) {
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fb = smem_u32(&full[slot]);
                 mbar_expect_tx(fb, kSlot);
                 dst = sRing + slot * kSlot;
-                if (++slot == kStages) slot = 0, ++round;
+                if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
             const CUtensorMap* X = s_role ? &tk : &tv;    // role A operand: the key tile, full width
@@ -244,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t + 1 < n) ok = load_role(t + 1);
                 ok = ok && load_grad(t);
             }
-            const int issued = round * kStages + slot;
-            for (int s = 0; s < kStages && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / kStages) * kStages;
-                mbar_drain(smem_u32(&full[s]), (last / kStages) & 1, a.status, 0x27);
+            const int issued = round * C::kStages + slot;
+            for (int s = 0; s < C::kStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x27);
             }
             mbar_drain(smem_u32(kc_full), 0, a.status, 0x2e);
         }
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 addr = sRing + slot * kSlot;
                 s = slot;
-                if (++slot == kStages) slot = 0, ++round;
+                if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
             auto role = [&](int t) -> bool {
@@ -312,12 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto grads = [&](int t) -> bool {
-                if (!mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x23)) return false;
+                const int pb = t % C::PBUF;
+                if (!mbar_wait(smem_u32(&p_full[pb]), (t / C::PBUF) & 1, abort_flag, a.status, 0x23)) return false;
                 if (!s_role && !mbar_wait(smem_u32(p_read), t & 1, abort_flag, a.status, 0x32)) return false;
                 tc_fence_after();
-                mbar_expect_tx(smem_u32(p_full), p_rem);  // arm phase t+1
-                if (!grad_pair(tDV, sP, t > 0)) return false;  // dV_c += P^T dO_c
-                umma_commit_multicast(smem_u32(p_free), mask_s);
+                mbar_expect_tx(smem_u32(&p_full[pb]), p_rem);  // arm the buffer's next use
+                if (!grad_pair(tDV, sP + pb * 2 * kSub, t > 0)) return false;  // dV_c += P^T dO_c
+                umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 if (!mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x24)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(ds_full), ds_rem);
@@ -351,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         // dQ_c(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory
-        // and add into the fp32 accumulator with TMA bulk reduce-adds (two staging buffers).
+        // and add into the fp32 accumulator with TMA bulk reduce-adds.
         auto drain_dq = [&](int t) -> bool {
             bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x26));
             tc_fence_after();
@@ -360,8 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                const uint32_t buf = sStage + (c4 & 1) * kSub;
-                if (tid == 64) bulk_wait_group_read1();  // the reduce that last read `buf` is done
+                const uint32_t buf = sStage + (c4 % C::STAGEBUF) * kSub;
+                if (tid == 64) {  // the reduce that last read `buf` is done
+                    if (C::STAGEBUF == 2) bulk_wait_group_read1();
+                    else bulk_wait_group_read0();
+                }
                 named_bar_sync(2, 128);
                 if (w) {
                     uint32_t rq[32];
@@ -444,14 +456,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 if (edge) p_row(std::true_type{});
                 else p_row(std::false_type{});
-                if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(p_free), (t - 1) & 1, abort_flag, a.status, 0x2b));
+                // buffer t % PBUF was last read at step t - PBUF
+                if (t >= C::PBUF) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_free[t % C::PBUF]), ((t / C::PBUF) - 1) & 1, abort_flag, a.status, 0x2b));
             } else {
                 // dS^T = P^T (dP^T - Delta), P^T from the S-role partner
-                ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x2c));
+                ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[t % C::PBUF]), (t / C::PBUF) & 1, abort_flag, a.status, 0x2c));
                 if (ok) {
 #pragma unroll
                     for (int st = 0; st < C::NQ / 64; ++st) {
-                        const uint32_t tile = sP + (share * (C::NQ / 64) + st) * kSub;
+                        const uint32_t tile = sP + (t % C::PBUF) * 2 * kSub + (share * (C::NQ / 64) + st) * kSub;
 #pragma unroll
                         for (int ch = 0; ch < 8; ++ch) {
                             uint32_t x0, x1, x2, x3;
@@ -475,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
             }
             // write this thread's row of the share, then copy the warp's 32 rows to every peer
-            const uint32_t dst = s_role ? sP : sDS;
-            const uint32_t fbar = smem_u32(s_role ? p_full : ds_full);
+            const uint32_t dst = s_role ? sP + (t % C::PBUF) * 2 * kSub : sDS;
+            const uint32_t fbar = smem_u32(s_role ? &p_full[t % C::PBUF] : ds_full);
             if (ok) {
 #pragma unroll
                 for (int st = 0; st < C::NQ / 64; ++st) {
@@ -508,7 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
         // every arrival owed to this CTA's exchange barriers has landed before it exits
         if (ok) {
-            if (s_role) mbar_drain(smem_u32(p_free), (n - 1) & 1, a.status, 0x30);
+            if (s_role) {
+                for (int t = max(0, n - C::PBUF); t < n; ++t)
+                    mbar_drain(smem_u32(&p_free[t % C::PBUF]), (t / C::PBUF) & 1, a.status, 0x30);
+            }
             else mbar_drain(smem_u32(ds_free), (n - 1) & 1, a.status, 0x31);
         }
         // ---- epilogue: dV_c, dK_c rows (keys on lanes) -> bf16 -----------------------------
@@ -639,6 +655,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
         a.T = L.total_rows;
         a.scale = L.scale;
         a.scale_log2 = L.scale * kLog2e;
+        constexpr uint32_t kSmem = Cfg<D>::kSmem;
         cudaError_t e = cudaFuncSetAttribute(bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
         if (e != cudaSuccess) return e;
         constexpr int NC = Cfg<D>::NC;
