@@ -128,8 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* ds_full = p_full + 2;         // all of dS^T(t) present
     uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share in buffer b is done [2]
     uint64_t* ds_free = p_free + 2;         // (dP role) every reader of this CTA's dS^T share is done
-    uint64_t* p_read = ds_free + 1;         // (dP role) the elementwise warps have read P^T(t)
-    uint64_t* dq_full = p_read + 1;
+    uint64_t* dq_full = ds_free + 1;
     uint64_t* dq_free = dq_full + 1;
     uint64_t* kc_full = dq_free + 1;
     uint64_t* mma_idle = kc_full + 1;
@@ -154,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // elementwise warps have also read P^T)
         for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_free[b]), C::NC);
         mbar_init(smem_u32(ds_free), C::NC);
-        mbar_init(smem_u32(p_read), 128);
         mbar_init(smem_u32(dq_full), 1);
         mbar_init(smem_u32(dq_free), 128);
         mbar_init(smem_u32(kc_full), 1);
@@ -322,11 +320,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto grads = [&](int t) -> bool {
                 const int pb = t % C::PBUF;
                 if (!mbar_wait(smem_u32(&p_full[pb]), (t / C::PBUF) & 1, abort_flag, a.status, 0x23)) return false;
-                if (!s_role && !mbar_wait(smem_u32(p_read), t & 1, abort_flag, a.status, 0x32)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(&p_full[pb]), p_rem);  // arm the buffer's next use
                 if (!grad_pair(tDV, sP + pb * 2 * kSub, t > 0)) return false;  // dV_c += P^T dO_c
-                umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
+                // an S-role CTA is done with P^T(t) here; a dP-role CTA also reads it in its
+                // elementwise warps (before writing dS^T(t)), so it releases the buffer after
+                // the dS^T products below
+                if (s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 if (!mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x24)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(ds_full), ds_rem);
@@ -340,6 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 umma_commit_multicast(smem_u32(ds_free), mask_d);
+                if (!s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 return true;
             };
             bool ok = role(0);
@@ -482,9 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                // this thread is done with P^T(t); the MMA issuer waits for all 128 before the
-                // dV product whose commit releases the share to its writer
-                mbar_arrive(smem_u32(p_read));
                 if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
             }
             // write this thread's row of the share, then copy the warp's 32 rows to every peer
