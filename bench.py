@@ -46,8 +46,11 @@ WORKLOAD = {"workload": "dense causal attention fwd+bwd, head_dim 512, GQA 8:1",
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # dram bytes per launch (ncu: dram__bytes_read.sum + dram__bytes_write.sum) for kernels whose
-# counters were captured, keyed by kernel; valid only while the kernel's sources hash the same.
-TRAFFIC = {}
+# counters were captured, keyed by kernel; valid only while the kernel's own sources hash the same.
+# bwd_main_d512: captured at B=1 (half the workload, same per-cluster work) and doubled.
+KERNEL_SOURCES = {"bwd_main_d512": ["attn_bwd.cu", "ptx.cuh", "attn_internal.h"],
+                  "fwd_d512": ["attn_fwd.cu", "ptx.cuh", "attn_internal.h"]}
+TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (2.443940e9 + 1.310306e9), "src": "d86f41fffc1bbd60"}}
 
 
 def pairs_causal(S: int, W: int = 0) -> int:
@@ -56,12 +59,11 @@ def pairs_causal(S: int, W: int = 0) -> int:
     return W * (W + 1) // 2 + (S - W) * W
 
 
-def kernel_sources_hash() -> str:
+def kernel_sources_hash(files) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_flash_gqa_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in files:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -252,7 +254,8 @@ def bench_ours(args, rank, world, pg):
     achieved = per_launch / (avg_ms * 1e-3) / 1e12 if per_launch else None
     peak = peaks["bf16_tflops_sustained"]
     tr = TRAFFIC.get(name)
-    traffic = tr["bytes"] if tr and tr.get("src") == kernel_sources_hash() else None
+    traffic = tr["bytes"] if tr and name in KERNEL_SOURCES and tr.get("src") == kernel_sources_hash(
+        KERNEL_SOURCES[name]) else None
     roofline = {"bound": "tensor", "kernel": name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak if achieved else None, "traffic": traffic,
                 "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
@@ -480,7 +483,7 @@ def bench_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="skip the SWA / varlen / decode measurements")
