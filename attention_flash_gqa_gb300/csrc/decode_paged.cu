@@ -13,8 +13,10 @@
 //    request and the head of the next.
 //  * 16 consumer warps, two per KV head: each serves all query heads of the head's GQA
 //    group (one K/V row read feeds all of them) on one half of the page's 16 tokens, with
-//    its own running softmax state. Lane l owns dims 4l..4l+3; per-token dot products are
-//    finished by a butterfly reduce-scatter across the warp.
+//    its own running softmax state. For GQA groups up to 4 each half-warp takes 4 of the
+//    warp's tokens with 8 dims per lane and paired fp32 FMAs; for a group of 8, lane l owns
+//    dims 4l..4l+3 of all 8. Per-token dot products are finished by a butterfly
+//    reduce-scatter across the lanes that split a token.
 //  * fp32 online softmax in the log2 domain. Every (CTA, token half) touching a request
 //    leaves unnormalised partials (o, m, l) in the workspace; the last CTA to finish that
 //    request (arrival counter) merges them and resets the counter to zero.
@@ -29,8 +31,18 @@ namespace {
 constexpr int kD = 128;
 constexpr int kPage = 16;
 constexpr int kStages = 3;
-constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxConsumerWarps = 16;
+// GQA groups up to 4 use one consumer warp per KV head (8 warps: fewer warps per scheduler,
+// so each thread can hold its 8 query dims and 8 output dims per head in registers); a group
+// of 8 uses two warps per head.
+template <int G>
+struct DecCfg {
+    static constexpr bool PACKED = G <= 4;
+    static constexpr int CW = PACKED ? 8 : 16;     // consumer warps
+    static constexpr int WPH = PACKED ? 1 : 2;     // consumer warps per KV head
+    static constexpr int TPW = 16 / WPH;           // page tokens per warp
+    static constexpr int kThreads = (CW + 1) * 32;  // + one producer warp
+};
 constexpr int kMaxB = 4096;
 constexpr int kRowF = kD + 4;
 constexpr int kMaxUnits = 2048;  // page-table entries of a CTA's range staged in shared memory  // partial row: o[kD], m, l, 2 pad floats (keeps float4 alignment)
@@ -71,14 +83,17 @@ __device__ __forceinline__ int owner_of(long long u, long long P, int G) {
 }
 
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(DecodeArgs a) {
+    using DC = DecCfg<G>;
+    constexpr int kThreads = DC::kThreads;
+    constexpr int kConsumerWarps = DC::CW;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int page_bytes = kPage * a.Hkv * kD * 2;
     uint8_t* stage_base = smem;  // kStages x (K page, V page)
     int32_t* start = reinterpret_cast<int32_t*>(smem + kStages * 2 * page_bytes);  // [B + 1]
     float* scratch = reinterpret_cast<float*>(start + kMaxB + 8);                  // per warp: sc[8G], sp[8G]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kConsumerWarps * 16 * 8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(scratch + kMaxConsumerWarps * 16 * 8);
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
@@ -223,26 +238,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
     }
 
     // ---------------------------------- consumers ----------------------------------------
-    // Warp w serves KV head w / 2 for all G query heads of its group, on tokens
-    // 8 * (w % 2) .. 8 * (w % 2) + 7 of every page: the two warps of a head keep separate
-    // running softmax states and are merged like split partials at the end.
-    const int g = warp >> 1, half = warp & 1;
+    // Every consumer warp serves one KV head for all G query heads of its group (one K/V
+    // row read feeds all of them) with its own running softmax state; when two warps share
+    // a head (token halves), they are merged like split partials at the end.
+    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): half-warp s
+    //    takes tokens 8s .. 8s+7; lane l owns dims 8 (l % 16) .. +7, so a 16-lane butterfly
+    //    finishes the dot products, and the products use paired fp32 FMAs. The half-warps'
+    //    o accumulators are summed once per request.
+    //  * G = 8 (two warps per KV head, 8 tokens each): lane l owns dims 4l .. 4l+3 of the
+    //    warp's 8 tokens (32-lane butterfly).
+    constexpr bool PACKED = DC::PACKED;
+    constexpr int TPW = DC::TPW;
+    const int g = warp / DC::WPH, half = warp % DC::WPH;
     const bool active = g < a.Hkv;
-    float* sc = scratch + warp * 16 * G;  // [8 * G] scores (log2 domain)
-    float* sp = sc + 8 * G;               // [8 * G] probabilities
-    constexpr int NV = 8 * G;             // (token, head) values per half page
-    constexpr int NF = NV >= 32 ? NV / 32 : 1;
-    constexpr int KH = NV >= 32 ? 5 : (NV == 16 ? 4 : (NV == 8 ? 3 : 2));  // halving steps
+    float* sc = scratch + warp * 2 * TPW * G;  // [TPW * G] scores (log2 domain), index token * G + head
+    float* sp = sc + TPW * G;                  // [TPW * G] probabilities
+    constexpr int QD = PACKED ? 8 : 4;    // dims per lane
+    constexpr int NT = 8;                 // tokens per lane group (half-warp when packed)
+    constexpr int NL = PACKED ? 16 : 32;  // lanes that split one token's dims
+    constexpr int NV = TPW * G;           // (token, head) values of the warp's tokens
+    constexpr int NVL = NT * G;           // partial values per lane
+    constexpr int NF = NVL >= NL ? NVL / NL : 1;  // finished values per lane after the butterfly
+    constexpr int KH = NVL >= NL ? (PACKED ? 4 : 5) : (NVL == 16 ? 4 : (NVL == 8 ? 3 : (NVL == 4 ? 2 : 1)));
     constexpr int NH = NV >= 32 ? NV / 32 : 1;  // values per lane in the softmax layout
+    const int sub = PACKED ? (lane >> 4) : 0;   // half-warp (packed layout)
+    const int ln = PACKED ? (lane & 15) : lane; // lane within the group that splits a token
+    const int dim0 = QD * ln;
+    const int tok0 = TPW * half + NT * sub;     // first page token of this lane's tokens
 
-    // Query rows: lane holds dims 4*lane .. 4*lane+3 of each of the G heads.
-    float qv[G][4];  // loaded when the request changes
+    float qv[G][QD];  // this lane's query dims, loaded when the request changes
+    float acc_o[G][QD];
+#pragma unroll
     for (int hh = 0; hh < G; ++hh)
-        for (int e = 0; e < 4; ++e) qv[hh][e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < QD; ++e) qv[hh][e] = 0.f, acc_o[hh][e] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G)
-    float acc_o[G][4];
-    for (int hh = 0; hh < G; ++hh)
-        for (int e = 0; e < 4; ++e) acc_o[hh][e] = 0.f;
 
     int b = b_first;
     int i = 0;
@@ -253,9 +283,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
         if (b != cur_b) {
             cur_b = b;
             if (active) {
+#pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(a.q + ((size_t)b * a.Hq + g * G + hh) * kD + 4 * lane);
-                    qv[hh][0] = bf16_lo(w.x), qv[hh][1] = bf16_hi(w.x), qv[hh][2] = bf16_lo(w.y), qv[hh][3] = bf16_hi(w.y);
+                    const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + hh) * kD + dim0;
+                    if constexpr (PACKED) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(qrow);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) qv[hh][2 * e] = bf16_lo(ws[e]), qv[hh][2 * e + 1] = bf16_hi(ws[e]);
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2*>(qrow);
+                        qv[hh][0] = bf16_lo(w.x), qv[hh][1] = bf16_hi(w.x), qv[hh][2] = bf16_lo(w.y), qv[hh][3] = bf16_hi(w.y);
+                    }
                 }
             }
         }
@@ -263,30 +302,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
         ok = mbar_wait(smem_u32(&full[s]), r & 1, abort_flag, a.status, 0x32);
         if (!ok) break;
         const int32_t entry = unit_entry(i);
-        const int nt = (entry >= 0 ? (entry & 31) : 0) - 8 * half;  // valid tokens of this half (may be <= 0)
+        const int nt = (entry >= 0 ? (entry & 31) : 0) - TPW * half;  // valid tokens of this warp's (may be <= 0)
         if (active && nt > 0) {
-            const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes + (size_t)8 * half * a.Hkv * kD * 2;
+            const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes;
             const uint8_t* vp = kp + page_bytes;
-            // scores: v[t*G + hh], partial over this lane's 4 dims
-            float v[NV];
+            // partial scores over this lane's dims: v[t * G + hh] for its NT tokens
+            float v[NVL];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint2 w = *reinterpret_cast<const uint2*>(kp + ((size_t)(t * a.Hkv + g) * kD + 4 * lane) * 2);
-                const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
+            for (int t = 0; t < NT; ++t) {
+                const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.Hkv + g) * kD + dim0) * 2;
+                if constexpr (PACKED) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(krow);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    float2 k2[4];
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
+                    for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
+#pragma unroll
+                        for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
+                        v[t * G + hh] = acc.x + acc.y;
+                    }
+                } else {
+                    const uint2 w = *reinterpret_cast<const uint2*>(krow);
+                    const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh)
+                        v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
+                }
             }
-            // butterfly reduce-scatter over lane offsets 16, 8, 4, 2, 1: after KH halvings a lane
-            // holds NF values, index (lane >> (5 - KH)) * NF + j; remaining offsets all-reduce.
-            int count = NV;
+            // butterfly reduce-scatter over the NL lanes of a token group (offsets NL/2 .. 1):
+            // after KH halvings a lane holds NF values, index (ln >> (log2 NL - KH)) * NF + j;
+            // remaining offsets all-reduce.
+            int count = NVL;
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) {
+            for (int off = NL / 2; off >= 1; off >>= 1) {
                 if (count > 1) {
                     const int hf = count >> 1;
                     const bool upper = (lane & off) != 0;
 #pragma unroll
-                    for (int j = 0; j < NV / 2; ++j) {
+                    for (int j = 0; j < NVL / 2; ++j) {
                         if (j < hf) {
                             const float send = upper ? v[j] : v[hf + j];
                             const float keep = upper ? v[hf + j] : v[j];
@@ -298,11 +354,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
                     v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
                 }
             }
-            if ((lane & ((1 << (5 - KH)) - 1)) == 0) {
+            constexpr int LOGNL = PACKED ? 4 : 5;
+            if ((ln & ((1 << (LOGNL - KH)) - 1)) == 0) {
 #pragma unroll
                 for (int j = 0; j < NF; ++j) {
-                    const int idx = (lane >> (5 - KH)) * NF + j;
-                    sc[idx] = idx / G < nt ? v[j] * a.scale_log2 : -INFINITY;
+                    const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
+                    const int tw = NT * sub + idx / G;               // token within the warp's 8
+                    sc[tw * G + idx % G] = tw < nt ? v[j] * a.scale_log2 : -INFINITY;
                 }
             }
             __syncwarp();
@@ -333,21 +391,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
             l_run = l_run * alpha + psum;
             m_run = m_new;
             __syncwarp();
-            // o update: lane's 4 dims for all G heads
+            // o update: rescale, then add this lane's tokens
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 const float al = __shfl_sync(0xffffffffu, alpha, hh);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc_o[hh][e] *= al;
+                for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
             }
-            const int tmax = nt < 8 ? nt : 8;
-            for (int t = 0; t < tmax; ++t) {
-                const uint2 w = *reinterpret_cast<const uint2*>(vp + ((size_t)(t * a.Hkv + g) * kD + 4 * lane) * 2);
-                const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
+            if constexpr (PACKED) {
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float pt = sp[t * G + hh];
-                    acc_o[hh][0] += pt * v0, acc_o[hh][1] += pt * v1, acc_o[hh][2] += pt * v2, acc_o[hh][3] += pt * v3;
+                for (int t = 0; t < NT; ++t) {
+                    const int tw = NT * sub + t;
+                    const uint4 w = *reinterpret_cast<const uint4*>(vp + ((size_t)((tok0 + t) * a.Hkv + g) * kD + dim0) * 2);
+                    // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
+                    const bool valid = tw < nt;
+                    const uint32_t ws[4] = {valid ? w.x : 0u, valid ? w.y : 0u, valid ? w.z : 0u, valid ? w.w : 0u};
+                    float2 v2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
+                    float pt[G];
+                    if constexpr (G == 4) {
+                        const float4 p4 = *reinterpret_cast<const float4*>(sp + tw * 4);
+                        pt[0] = p4.x, pt[1] = p4.y, pt[2] = p4.z, pt[3] = p4.w;
+                    } else {
+#pragma unroll
+                        for (int hh = 0; hh < G; ++hh) pt[hh] = sp[tw * G + hh];
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float2 pp = make_float2(pt[hh], pt[hh]);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float2 o2 = __ffma2_rn(pp, v2[e], make_float2(acc_o[hh][2 * e], acc_o[hh][2 * e + 1]));
+                            acc_o[hh][2 * e] = o2.x, acc_o[hh][2 * e + 1] = o2.y;
+                        }
+                    }
+                }
+            } else {
+                const int tmax = nt < 8 ? nt : 8;
+                for (int t = 0; t < tmax; ++t) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(vp + ((size_t)((TPW * half + t) * a.Hkv + g) * kD + dim0) * 2);
+                    const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float pt = sp[t * G + hh];
+                        acc_o[hh][0] += pt * v0, acc_o[hh][1] += pt * v1, acc_o[hh][2] += pt * v2, acc_o[hh][3] += pt * v3;
+                    }
                 }
             }
         }
@@ -361,11 +450,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
             // slot of (request b, CTA k, token half): (b + k) * 2 + half
             float* slot = a.part + ((size_t)(b + k) * 2 + half) * a.Hq * kRowF;
             if (active) {
+                if constexpr (PACKED) {
+                    // the two half-warps hold the same dims for different tokens: sum them
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+                        for (int e = 0; e < QD; ++e) acc_o[hh][e] += __shfl_xor_sync(0xffffffffu, acc_o[hh][e], 16);
+                }
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float* row = slot + (size_t)(g * G + hh) * kRowF;
-                    *reinterpret_cast<float4*>(row + 4 * lane) =
-                        make_float4(acc_o[hh][0], acc_o[hh][1], acc_o[hh][2], acc_o[hh][3]);
+                    if (sub == 0) {
+#pragma unroll
+                        for (int e = 0; e < QD; e += 4)
+                            *reinterpret_cast<float4*>(row + dim0 + e) =
+                                make_float4(acc_o[hh][e], acc_o[hh][e + 1], acc_o[hh][e + 2], acc_o[hh][e + 3]);
+                    }
                     if (lane == hh) {
                         row[kD] = m_run;
                         row[kD + 1] = l_run;
@@ -381,41 +481,97 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             if (*last_flag) {
                 __threadfence();
-                // merge the partials of CTAs kf..kl (both token halves) for every (head, dim)
-                const int nslots = 2 * (kl - kf + 1);
-                for (int idx = tid; idx < a.Hq * (kD / 4); idx += kConsumerWarps * 32) {
-                    const int h = idx / (kD / 4), d4 = idx % (kD / 4);
-                    float M = -INFINITY;
-                    for (int q = 0; q < nslots; ++q) {
-                        const float* row = a.part + ((size_t)(b + kf) * 2 + q) * a.Hq * kRowF + (size_t)h * kRowF;
-                        M = fmaxf(M, __ldcg(row + kD));
+                // merge the partials of CTAs kf..kl (both token halves) for every (head, dim):
+                // slots (b + kk) * 2 + hf for kk in kf..kl and hf < WPH. Pass 1: per head the
+                // running max and sum over the slots (online rescaling, one thread per head);
+                // pass 2: every thread combines IPT (head, 4-dim) items, issuing the loads of all
+                // its items for a slot together. The consumer warps' score scratch is free here.
+                const int nslots = DC::WPH * (kl - kf + 1);
+                auto slot_row = [&](int q, int h) -> const float* {
+                    return a.part + ((size_t)(b + kf + q / DC::WPH) * 2 + q % DC::WPH) * a.Hq * kRowF + (size_t)h * kRowF;
+                };
+                float* mM = scratch;          // [Hq] max over the slots
+                float* mI = scratch + a.Hq;   // [Hq] 1 / sum
+                for (int h = tid; h < a.Hq; h += kConsumerWarps * 32) {
+                    float M = -INFINITY, Ls = 0.f;
+                    for (int q0 = 0; q0 < nslots; q0 += 8) {  // 8 slots' loads in flight at once
+                        float mk[8], lk[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            mk[j] = -INFINITY, lk[j] = 0.f;
+                            if (q0 + j < nslots) {
+                                const float* row = slot_row(q0 + j, h);
+                                mk[j] = __ldcg(row + kD), lk[j] = __ldcg(row + kD + 1);
+                            }
+                        }
+                        float Mc = M;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) Mc = fmaxf(Mc, mk[j]);
+                        if (Mc == -INFINITY) continue;
+                        Ls = M == -INFINITY ? 0.f : Ls * fast_exp2(M - Mc);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) Ls += mk[j] == -INFINITY ? 0.f : lk[j] * fast_exp2(mk[j] - Mc);
+                        M = Mc;
                     }
-                    const float Mu = M == -INFINITY ? 0.f : M;
-                    float Ls = 0.f;
-                    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int q = 0; q < nslots; ++q) {
-                        const float* row = a.part + ((size_t)(b + kf) * 2 + q) * a.Hq * kRowF + (size_t)h * kRowF;
-                        const float mk = __ldcg(row + kD);
-                        const float wgt = mk == -INFINITY ? 0.f : fast_exp2(mk - Mu);
-                        Ls += wgt * __ldcg(row + kD + 1);
-                        const float4 ov = __ldcg(reinterpret_cast<const float4*>(row) + d4);
-                        O.x += wgt * ov.x, O.y += wgt * ov.y, O.z += wgt * ov.z, O.w += wgt * ov.w;
+                    mM[h] = M;
+                    mI[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+                    a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+                constexpr int IPT = 4;
+                const int nitems = a.Hq * (kD / 4);
+                for (int base = tid; base < nitems; base += kConsumerWarps * 32 * IPT) {
+                    float4 O[IPT];
+                    int hI[IPT], dI[IPT];
+#pragma unroll
+                    for (int k2 = 0; k2 < IPT; ++k2) {
+                        const int idx = min(base + k2 * kConsumerWarps * 32, nitems - 1);
+                        hI[k2] = idx / (kD / 4), dI[k2] = idx % (kD / 4);
+                        O[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
-                    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-                    uint2 w;
-                    w.x = pack_bf16x2(O.x * inv, O.y * inv);
-                    w.y = pack_bf16x2(O.z * inv, O.w * inv);
-                    *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + h) * kD + 4 * d4) = w;
-                    if (d4 == 0)
-                        a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
+                    for (int q0 = 0; q0 < nslots; q0 += 2) {  // loads of 2 slots x IPT items in flight
+                        float mk[2][IPT];
+                        float4 ov[2][IPT];
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int k2 = 0; k2 < IPT; ++k2) {
+                                mk[j][k2] = -INFINITY;
+                                ov[j][k2] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (q0 + j < nslots) {
+                                    const float* row = slot_row(q0 + j, hI[k2]);
+                                    mk[j][k2] = __ldcg(row + kD);
+                                    ov[j][k2] = __ldcg(reinterpret_cast<const float4*>(row) + dI[k2]);
+                                }
+                            }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j)
+#pragma unroll
+                            for (int k2 = 0; k2 < IPT; ++k2) {
+                                const float wgt = mk[j][k2] == -INFINITY ? 0.f : fast_exp2(mk[j][k2] - mM[hI[k2]]);
+                                O[k2].x += wgt * ov[j][k2].x, O[k2].y += wgt * ov[j][k2].y;
+                                O[k2].z += wgt * ov[j][k2].z, O[k2].w += wgt * ov[j][k2].w;
+                            }
+                    }
+#pragma unroll
+                    for (int k2 = 0; k2 < IPT; ++k2) {
+                        if (base + k2 * kConsumerWarps * 32 >= nitems) break;
+                        const float inv = mI[hI[k2]];
+                        uint2 w;
+                        w.x = pack_bf16x2(O[k2].x * inv, O[k2].y * inv);
+                        w.y = pack_bf16x2(O[k2].z * inv, O[k2].w * inv);
+                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + hI[k2]) * kD + 4 * dI[k2]) = w;
+                    }
                 }
                 if (tid == 0) a.counters[b] = 0;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             // reset the running state for the next request
             m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
             for (int hh = 0; hh < G; ++hh)
-                for (int e = 0; e < 4; ++e) acc_o[hh][e] = 0.f;
+#pragma unroll
+                for (int e = 0; e < QD; ++e) acc_o[hh][e] = 0.f;
         }
     }
 }
@@ -423,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_paged_kernel(DecodeArgs a)
 }  // namespace
 
 size_t decode_smem_bytes(int Hkv) {
-    return 1024 + (size_t)kStages * 2 * kPage * Hkv * kD * 2 + (kMaxB + 8) * 4 + (size_t)kConsumerWarps * 16 * 8 * 4 +
+    return 1024 + (size_t)kStages * 2 * kPage * Hkv * kD * 2 + (kMaxB + 8) * 4 + (size_t)kMaxConsumerWarps * 16 * 8 * 4 +
            256 + kMaxUnits * 4;
 }
 
@@ -438,19 +594,19 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     a.scale_log2 = L.scale * 1.4426950408889634f;
     const int G = L.Hq / L.Hkv;
     const size_t smem = decode_smem_bytes(L.Hkv);
-    auto go = [&](auto kern) -> cudaError_t {
+    auto go = [&](auto kern, int threads) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         const ProfMark m = prof_begin(stream, "decode_paged");
-        kern<<<L.grid, kThreads, smem, stream>>>(a);
+        kern<<<L.grid, threads, smem, stream>>>(a);
         prof_end(stream, m);
         return cudaGetLastError();
     };
     switch (G) {
-        case 1: return go(decode_paged_kernel<1>);
-        case 2: return go(decode_paged_kernel<2>);
-        case 4: return go(decode_paged_kernel<4>);
-        case 8: return go(decode_paged_kernel<8>);
+        case 1: return go(decode_paged_kernel<1>, DecCfg<1>::kThreads);
+        case 2: return go(decode_paged_kernel<2>, DecCfg<2>::kThreads);
+        case 4: return go(decode_paged_kernel<4>, DecCfg<4>::kThreads);
+        case 8: return go(decode_paged_kernel<8>, DecCfg<8>::kThreads);
         default: return cudaErrorInvalidValue;
     }
 }
