@@ -203,29 +203,40 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
         const int nt = min(kPage, req_len(a, lo) - p * kPage);
         return (page << 5) | nt;
     };
-    for (int kk = tid; kk < n_units && kk < kMaxUnits; kk += kThreads) unit_tab[kk] = make_entry(kk);
+    // The producer warp stages the first units itself and issues their pages at once, so
+    // the copies are in flight while the rest of the table is staged.
+    const int n_pre = min(n_units, kStages);
+    auto issue = [&](int i, int32_t entry) {
+        const int s = i % kStages;
+        const uint32_t fb = smem_u32(&full[s]);
+        if (entry >= 0) {
+            mbar_expect_tx(fb, 2u * page_bytes);
+            const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * kD;
+            bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes), a.kc + off, page_bytes, fb);
+            bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes + page_bytes), a.vc + off, page_bytes, fb);
+        } else {
+            mbar_arrive(fb);
+        }
+    };
+    const int rot = (tid + kThreads - kConsumerWarps * 32) % kThreads;  // producer warp stages units 0..31
+    for (int kk = rot; kk < n_units && kk < kMaxUnits; kk += kThreads) unit_tab[kk] = make_entry(kk);
+    if (warp == kConsumerWarps) {
+        __syncwarp();
+        if (lane == 0)
+            for (int i = 0; i < n_pre; ++i) issue(i, unit_tab[i]);
+    }
     __syncthreads();
     auto unit_entry = [&](int kk) -> int32_t { return kk < kMaxUnits ? unit_tab[kk] : make_entry(kk); };
 
     if (warp == kConsumerWarps) {
         // ---------------------------- producer ------------------------------------------
         if (lane == 0) {
-            int b = b_first;
             int i = 0;
             for (long long u = u0; u < u1; ++u, ++i) {
-                while (start[b + 1] <= u) ++b;
+                if (i < n_pre) continue;  // issued before the table was staged
                 const int s = i % kStages, r = i / kStages;
                 if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1, abort_flag, a.status, 0x31)) break;
-                const int32_t entry = unit_entry(i);
-                const uint32_t fb = smem_u32(&full[s]);
-                if (entry >= 0) {
-                    mbar_expect_tx(fb, 2u * page_bytes);
-                    const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * kD;
-                    bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes), a.kc + off, page_bytes, fb);
-                    bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes + page_bytes), a.vc + off, page_bytes, fb);
-                } else {
-                    mbar_arrive(fb);
-                }
+                issue(i, unit_entry(i));
             }
             // Drain: every issued copy completes before this CTA may exit.
             const int issued = i;

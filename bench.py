@@ -11,8 +11,9 @@ B=2, Hq=32, Hkv=4, S=4096, scale 1/sqrt(512), seeded N(0,1) bf16 inputs.
 Prints one JSON line. `value` is whole-job fwd+bwd TFLOP/s with inputs resident in
 HBM (causal-aware count: 4*D per unmasked (query, key) pair forward, 10*D backward);
 `e2e` is the same metric through the C ABI with host buffers (pinned host -> device
-copies of q, k, v, dO and device -> host copies of o, lse, dQ, dK, dV inside the timed
-region). Inputs (q, dO: 268 MB each) are larger than L2, so no flush is needed between
+copies of q, k, v, dO and device -> host copies of o, lse, dQ, dK, dV of every step inside
+the timed region; the copies of neighbouring steps overlap the compute on two copy
+streams, with two device buffer sets). Inputs (q, dO: 268 MB each) are larger than L2, so no flush is needed between
 steps. `roofline` is for the kernel with the largest device time, timed live with CUDA
 events bracketing each launch. `extra` holds the sliding-window (d256, W=1024),
 varlen (d512) and paged-decode (HBM GB/s) measurements. `cpu_baseline` is the fp64
@@ -276,33 +277,65 @@ def bench_ours(args, rank, world, pg):
     hdv = torch.empty(v.shape, dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    # Every step copies its inputs host -> device and its results device -> host. The steps
+    # are pipelined like an input pipeline would: two device buffer sets, the inputs of step
+    # i+1 are copied in on one stream while step i computes, and step i's results are copied
+    # out on another stream while step i+1 computes. The timed region runs from the first
+    # input copy to the last result copy.
+    bufs = [dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv)]
+    bufs.append({name: torch.empty_like(t) for name, t in bufs[0].items()})
+    ws2 = torch.empty_like(ws)
+    wss = [ws, ws2]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    inputs_free = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        step()
-        ho.copy_(o, non_blocking=True)
-        hlse.copy_(lse, non_blocking=True)
-        hdq.copy_(dq, non_blocking=True)
-        hdk.copy_(dk, non_blocking=True)
-        hdv.copy_(dv, non_blocking=True)
+    def e2e_run(n):
+        for ev in computed + out_done + inputs_free:
+            ev.record(stream)
+        for i in range(n + 1):
+            if i < n:  # inputs of step i
+                bs = bufs[i % 2]
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(inputs_free[i % 2])
+                    for name, h in (("q", hq), ("k", hk), ("v", hv), ("do", hdo)):
+                        bs[name].copy_(h, non_blocking=True)
+                    in_ready[i % 2].record(s_in)
+            if i >= 1:  # compute of step i-1 was enqueued last iteration; copy its results out
+                bs = bufs[(i - 1) % 2]
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(computed[(i - 1) % 2])
+                    for name, h in (("o", ho), ("lse", hlse), ("dq", hdq), ("dk", hdk), ("dv", hdv)):
+                        h.copy_(bs[name], non_blocking=True)
+                    out_done[(i - 1) % 2].record(s_out)
+            if i < n:  # compute of step i
+                bs = bufs[i % 2]
+                stream.wait_event(in_ready[i % 2])
+                stream.wait_event(out_done[i % 2])  # step i-2's results have left this buffer set
+                attn.attn_fwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], scale=p.scale)
+                attn.attn_bwd(bs["q"], bs["k"], bs["v"], bs["o"], bs["lse"], bs["do"], bs["dq"], bs["dk"], bs["dv"],
+                              scale=p.scale, workspace=wss[i % 2])
+                computed[i % 2].record(stream)
+                inputs_free[i % 2].record(stream)
+        stream.wait_event(out_done[(n - 1) % 2])
 
-    e2e_step()
+    e2e_run(2)
     torch.cuda.synchronize()
     e_steps = max(3, args.steps // 4)
     barrier(pg)
     torch.cuda.synchronize()
     ev0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    e2e_run(e_steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(pg, ev0.elapsed_time(ev1) / e_steps)
     e2e = {"value": flops_step * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    del hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "pipelining": "inputs of step i+1 copied in and results of step i-1 copied out during step i "
+                         "(two device buffer sets, separate copy streams)"}
+    del hq, hk, hv, hdo, ho, hlse, hdq, hdk, hdv, bufs, ws2, wss
     extra = None if args.no_extra else bench_extra(args, attn, synth, peaks, peak_src, clocks)
     return finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launches, clocks, finite, props,
                   peaks, peak_src, extra)
