@@ -172,6 +172,12 @@ def max_over_ranks(pg, x: float) -> float:
     return float(t.item())
 
 
+def aggregate_tflops(flops_per_rank_step: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job rate: every rank runs its own replica of the step (weak scaling), the step time
+    is the slowest rank's."""
+    return flops_per_rank_step * world / (ms_per_step_max * 1e-3) / 1e12
+
+
 def to_dev(bits, pin=False):
     import numpy as np
     import torch
@@ -245,7 +251,7 @@ def bench_ours(args, rank, world, pg):
     clocks.mark(t0, t1)
     ms_step = ev0.elapsed_time(ev1) / args.steps
     ms_step_max = max_over_ranks(pg, ms_step)
-    value = flops_step * world / (ms_step_max * 1e-3) / 1e12
+    value = aggregate_tflops(flops_step, world, ms_step_max)
 
     # ---- dominant kernel roofline --------------------------------------------------------------
     dom = max(prof.items(), key=lambda kv: kv[1][1])
@@ -331,7 +337,7 @@ def bench_ours(args, rank, world, pg):
     ev1.record(stream)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(pg, ev0.elapsed_time(ev1) / e_steps)
-    e2e = {"value": flops_step * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e_ms,
+    e2e = {"value": aggregate_tflops(flops_step, world, e_ms), "unit": "TFLOP/s", "ms_per_step": e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "pipelining": "inputs of step i+1 copied in and results of step i-1 copied out during step i "
                          "(two device buffer sets, separate copy streams)"}
@@ -385,19 +391,28 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
         clocks.mark(t0, time.time())
         return ev0.elapsed_time(ev1) / n
 
+    def per_kernel(fn, n=3):  # a separate, profiled pass: average ms per launch of each kernel
+        attn.attn_profile_start()
+        for _ in range(n):
+            fn()
+        prof = attn.attn_profile_stop()
+        return {kname: round(t / cnt, 4) for kname, (cnt, t) in prof.items()}
+
     # sliding window, d256, W=1024, outliers
     p = synth.swa_d256_w1024(seed=7)
     q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
     o = torch.empty_like(q)
     lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ms = timed(lambda: (attn.attn_fwd(q, k, v, o, lse, window=p.window, scale=p.scale),
-                        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, window=p.window, scale=p.scale)), steps)
+    swa_step = lambda: (attn.attn_fwd(q, k, v, o, lse, window=p.window, scale=p.scale),
+                        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, window=p.window, scale=p.scale))
+    ms = timed(swa_step, steps)
+    kern_ms = per_kernel(swa_step)
     fl = 14 * p.D * pairs_causal(p.S, p.window) * p.B * p.Hq
     fin = all(bool(torch.isfinite(t.float()).all()) for t in (o, dq, dk, dv))
     res["swa_d256_w1024"] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
                              "frac_of_bf16_peak_sustained": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
-                             "all_grads_finite": fin}
+                             "all_grads_finite": fin, "kernel_ms": kern_ms}
     del q, k, v, do, o, lse, dq, dk, dv
 
     # varlen d512
@@ -407,12 +422,14 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
     o = torch.empty_like(q)
     lse = torch.empty((vp.Hq, vp.total_tokens), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ms = timed(lambda: (attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, o, lse, scale=vp.scale),
-                        attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=vp.scale, cu_seqlens=cu,
-                                      max_seqlen=vp.max_seqlen)), steps)
+    vl_step = lambda: (attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, o, lse, scale=vp.scale),
+                       attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=vp.scale, cu_seqlens=cu,
+                                     max_seqlen=vp.max_seqlen))
+    ms = timed(vl_step, steps)
+    kern_ms = per_kernel(vl_step)
     fl = 14 * vp.D * vp.Hq * sum(int(L) * (int(L) + 1) // 2 for L in vp.seqlens)
     res["varlen_d512_causal"] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-                                 "seqlens": [int(x) for x in vp.seqlens]}
+                                 "seqlens": [int(x) for x in vp.seqlens], "kernel_ms": kern_ms}
     del q, k, v, do, o, lse, dq, dk, dv
 
     # paged decode: time the kernel alone, flushing L2 (write > L2) between calls
