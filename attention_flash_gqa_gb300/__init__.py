@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
 * ``attn_bwd(q, k, v, o, lse, dO, ...)``  -> (dQ, dK, dV); dense or packed (cu_seqlens)
 * ``attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, ...)`` -> (o, lse[B,Hq])
 * ``attn_workspace_size``, ``attn_get_device_status``, ``attn_status_string``
+* ``attn_selftest_wait_timeout`` (exercises the bounded-wait failure reporting)
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
     "attn_get_device_status", "attn_status_string", "library_path", "load_library",
     "attn_launch_count", "attn_profile_start", "attn_profile_stop", "attn_decode_paged_noalloc",
+    "attn_selftest_wait_timeout",
     "ATTN_OP_FWD", "ATTN_OP_FWD_VARLEN", "ATTN_OP_BWD", "ATTN_OP_BWD_VARLEN", "ATTN_OP_DECODE_PAGED",
 ]
 
@@ -70,6 +72,7 @@ def load_library():
         lib.attn_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.attn_workspace_size.restype = Z
         lib.attn_get_device_status.argtypes = [P]
+        lib.attn_selftest_wait_timeout.argtypes = [I, P]
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_version.restype = I
@@ -130,6 +133,15 @@ def attn_get_device_status(stream=None) -> int:
     import torch
 
     return int(load_library().attn_get_device_status(_stream_ptr(stream, torch.cuda.current_device())))
+
+
+def attn_selftest_wait_timeout(limit_ms: int = 100, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that nothing completes gives up after
+    limit_ms and records ATTN_ERR_DEVICE_TIMEOUT); read it with attn_get_device_status()."""
+    import torch
+
+    _check(int(load_library().attn_selftest_wait_timeout(int(limit_ms), _stream_ptr(stream, torch.cuda.current_device()))),
+           "attn_selftest_wait_timeout")
 
 
 def _check(status: int, what: str):

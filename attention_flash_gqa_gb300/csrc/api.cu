@@ -24,6 +24,19 @@ namespace {
 // [0]: fault flags; [1]: id of the first pipeline wait that gave up (0 = none).
 __device__ unsigned g_attn_status[2] = {0u, 0u};
 
+// One bounded pipeline wait that nothing completes: the wait gives up after limit_ns, records
+// the timeout in the status word and the kernel returns (see attn_selftest_wait_timeout).
+__global__ void selftest_wait_kernel(unsigned* status, unsigned long long limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        attn::mbar_init(attn::smem_u32(&bar), 1);
+        abort_flag = 0;
+        attn::fence_mbar_init();
+        attn::mbar_wait_for(attn::smem_u32(&bar), 0, &abort_flag, status, 0x7f, limit_ns);
+    }
+}
+
 constexpr int kMaxDevices = 64;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -367,6 +380,17 @@ int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_b
     if (units < grid) grid = (int)units;
     L.grid = grid < 1 ? 1 : grid;
     return attn::launch_decode_paged(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int attn_selftest_wait_timeout(int limit_ms, void* stream) {
+    if (limit_ms < 1 || limit_ms > 10000) return ATTN_ERR_INVALID_ARG;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    const attn::ProfMark m = attn::prof_begin(static_cast<cudaStream_t>(stream), "selftest_wait");
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status,
+                                                                          (unsigned long long)limit_ms * 1000000ull);
+    attn::prof_end(static_cast<cudaStream_t>(stream), m);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_get_device_status(void* stream) {

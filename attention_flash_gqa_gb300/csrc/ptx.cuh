@@ -70,21 +70,25 @@ __device__ __forceinline__ void record_timeout(unsigned* status, unsigned site) 
 // Bounded wait on phase `parity` of an mbarrier. `abort` is a CTA-shared flag: once
 // any thread has given up, the others stop waiting too. Returns false on give-up.
 // `site` identifies the wait in the status record (debugging aid).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
-                                          unsigned site = 0) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
+                                              unsigned site, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0u) {
             if (*abort) return false;
-            if (globaltimer() - t0 > kWaitLimitNs || it > kWaitMaxPolls) {
+            if (globaltimer() - t0 > limit_ns || it > kWaitMaxPolls) {
                 record_timeout(status, site);
                 *abort = 1;
                 return false;
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned* status,
+                                          unsigned site = 0) {
+    return mbar_wait_for(bar, parity, abort, status, site, kWaitLimitNs);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight copies / MMAs).

@@ -189,6 +189,18 @@ ATTN_API size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D
  */
 ATTN_API int attn_get_device_status(void* stream);
 
+/*
+ * attn_selftest_wait_timeout -- exercise the failure-reporting path of the kernels' pipeline
+ * waits (no counterpart on the pages). Enqueues on `stream` one small kernel whose single
+ * thread waits on an mbarrier phase that nothing completes, with the same bounded wait the
+ * attention kernels use but a limit of `limit_ms` milliseconds (1..10000). The wait gives up,
+ * the kernel records ATTN_ERR_DEVICE_TIMEOUT in the device status and returns normally: no
+ * fault, no hang, and the context stays usable. Returns ATTN_OK once enqueued,
+ * ATTN_ERR_INVALID_ARG for a limit out of range; read the outcome with
+ * attn_get_device_status().
+ */
+ATTN_API int attn_selftest_wait_timeout(int limit_ms, void* stream);
+
 /* attn_status_string -- a static, human-readable name for a status code. */
 ATTN_API const char* attn_status_string(int status);
 

@@ -164,3 +164,21 @@ def test_decode_bad_page_id_is_reported_not_read(orc):
     check("o[0]", o[0], ro[0])
     assert np.isfinite(o[1]).all() and np.isfinite(lse[1]).all()
     assert attn.attn_get_device_status() == 0  # cleared by the previous read
+
+
+def test_bounded_wait_gives_up_and_reports(orc):
+    """Failure detection without a fault: a pipeline wait that nothing completes gives up after
+    its limit, the kernel records ATTN_ERR_DEVICE_TIMEOUT and returns; the status is read on the
+    host, cleared, and the context stays usable (a forward afterwards still matches the oracle)."""
+    assert attn.attn_get_device_status() == 0
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    attn.attn_selftest_wait_timeout(50)
+    t1.record()
+    assert attn.attn_get_device_status() == 6  # ATTN_ERR_DEVICE_TIMEOUT
+    assert t0.elapsed_time(t1) >= 45.0  # it really waited out its limit
+    assert attn.attn_get_device_status() == 0  # cleared by the previous read
+    with pytest.raises(attn.AttnError):
+        attn.attn_selftest_wait_timeout(0)  # limit out of range: rejected before anything runs
+    compare_dense(orc, synth.dense(1, 2, 1, 200, 256, 0, seed=31), with_bwd=True)
