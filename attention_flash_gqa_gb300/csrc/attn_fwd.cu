@@ -299,6 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
                     tmem_st32(tO + c * 32 + lane_base, raw);
                 }
+            } else if (j == n - 1 && j > 0) {
+                // last step: P(j-1) V(j-1) completes before this P is released, so the epilogue
+                // waits on exactly one pending phase of pv_done (no parity aliasing)
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done), (j - 1) & 1, abort_flag, a.status, 0x1d));
+                if (!ok) break;
             }
             // P row r -> the first 64 columns of this step's S buffer (S is in registers)
             {
@@ -315,8 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(smem_u32(p_full));
         }
         // ---- epilogue: O / l -> bf16, lse -------------------------------------------------
-        // the last two P V (phases n-2, n-1); earlier ones are complete by s_full(n-1)
-        if (ok && n >= 2) ok = mbar_wait(smem_u32(pv_done), (n - 2) & 1, abort_flag, a.status, 0x17);
+        // the last P V (phase n-1); every earlier one is complete (waited in the last step)
         if (ok) ok = mbar_wait(smem_u32(pv_done), (n - 1) & 1, abort_flag, a.status, 0x17);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
