@@ -69,6 +69,8 @@ class Oracle:
         lib.oracle_attn_dq_rows.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _i, _i, _p, _l, _p, _i]
         lib.oracle_attn_dkv_rows.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _d, _i, _i, _p, _l, _p, _p, _i]
         lib.oracle_attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _d, _i, _p, _p, _i]
+        lib.oracle_attn_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _d, _i, _p, _p,
+                                                  _i]
         lib.oracle_mutant_id.restype = _i
         self.lib = lib
         self.mutant = lib.oracle_mutant_id()
@@ -190,6 +192,24 @@ class Oracle:
         self._check(self.lib.oracle_attn_decode_paged(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(sl), B, Hq, Hkv, D,
                                                       ps, bt.shape[1], num_pages, scale, window, _ptr(o), _ptr(lse),
                                                       nthreads or default_threads()), "decode_paged")
+        return o, lse
+
+
+    def prefill_paged(self, q, k_cache, v_cache, block_table, seq_lens, cu_q, scale, window=0, nthreads=None):
+        """New queries q [T, Hq, D] (request b: rows cu_q[b]..cu_q[b+1]-1, the last n_b of its
+        seq_lens[b] cached tokens) over the paged cache -> o [T, Hq, D], lse [Hq, T]."""
+        q, kc, vc = _u16(q), _u16(k_cache), _u16(v_cache)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        cu = np.ascontiguousarray(cu_q, dtype=np.int32)
+        T, Hq, D = q.shape
+        num_pages, ps, Hkv, _ = kc.shape
+        o = np.zeros((T, Hq, D), np.float64)
+        lse = np.full((Hq, T), -np.inf, np.float64)
+        self._check(self.lib.oracle_attn_prefill_paged(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(sl), _ptr(cu),
+                                                       len(sl), Hq, Hkv, D, ps, bt.shape[1], num_pages, scale, window,
+                                                       _ptr(o), _ptr(lse), nthreads or default_threads()),
+                    "prefill_paged")
         return o, lse
 
 

@@ -65,6 +65,7 @@ typedef struct {
     double scale;
     int causal, window;
     int q_single; /* 1: q holds one row per head (a decode query), whatever i is */
+    int q_first;  /* position of q's first row (the new queries of a paged prefill); 0 otherwise */
 } seq_view;
 
 static inline int kv_head_of(const seq_view* sv, int h) {
@@ -92,6 +93,7 @@ static inline int allowed(const seq_view* sv, int i, int j) {
 
 static inline const uint16_t* qrow(const seq_view* sv, int i, int h) {
     if (sv->q_single) i = 0;
+    else i -= sv->q_first;
     return sv->q + ((size_t)i * sv->Hq + h) * sv->D;
 }
 static inline const uint16_t* dorow(const seq_view* sv, int i, int h) { return sv->dO + ((size_t)i * sv->Hq + h) * sv->D; }
@@ -276,6 +278,7 @@ static seq_view view_of(const problem_t* P, int s) {
     sv.causal = P->causal;
     sv.window = P->window;
     sv.q_single = 0;
+    sv.q_first = 0;
     return sv;
 }
 
@@ -774,6 +777,7 @@ static void decode_item(void* ctx, long b, double* scratch) {
     seq_view sv;
     sv.q = X->q + (size_t)b * X->Hq * D; /* the request's single query row [Hq, D] */
     sv.q_single = 1;
+    sv.q_first = 0;
     sv.k = kk, sv.v = vv, sv.dO = NULL, sv.L = L, sv.Hq = X->Hq, sv.Hkv = Hkv, sv.D = D;
     sv.scale = X->scale, sv.causal = 1, sv.window = X->window;
     for (int h = 0; h < X->Hq; ++h) {
@@ -801,6 +805,88 @@ int oracle_attn_decode_paged(const uint16_t* q, const uint16_t* k_cache, const u
                     scale, o, lse, 0};
     atomic_init(&X.bad, 0);
     int rc = parallel_for(B, nthreads, (size_t)maxL, decode_item, &X);
+    if (rc) return rc;
+    return atomic_load(&X.bad) ? -1 : 0;
+}
+
+/* ---------------------------------------------------------------------------------- */
+/*
+ * Prefill over a paged cache (chunked prefill): request b has L_b = seq_lens[b] cached
+ * tokens (pages as in the decode above) and n_b = cu_q[b+1] - cu_q[b] new query tokens,
+ * rows cu_q[b] .. cu_q[b+1]-1 of q [T, Hq, D], which are the last n_b of its L_b tokens
+ * (their keys and values are already in the cache). New query i sits at position
+ * L_b - n_b + i and sees the cached tokens at positions <= its own (and within the window).
+ * The single-token decode is the case n_b = 1. Implemented literally: gather the request's
+ * keys and values into a contiguous copy, then run the row forward for each new query.
+ * Outputs o [T, Hq, D] and lse [Hq, T]. Returns -1 on a page id outside the pool or
+ * n_b > L_b.
+ */
+typedef struct {
+    const uint16_t *q, *kc, *vc;
+    const int32_t *bt, *lens, *cu_q;
+    int Hq, Hkv, D, ps, max_pages, num_pages, window;
+    int64_t T;
+    double scale;
+    double *o, *lse;
+    atomic_int bad;
+} prefill_paged_ctx;
+
+static void prefill_paged_item(void* ctx, long b, double* scratch) {
+    prefill_paged_ctx* X = (prefill_paged_ctx*)ctx;
+    const int L = X->lens[b], D = X->D, Hkv = X->Hkv;
+    const int q0 = X->cu_q[b], nq = X->cu_q[b + 1] - X->cu_q[b];
+    if (nq < 0 || nq > L) {
+        atomic_store(&X->bad, 1);
+        return;
+    }
+    if (nq == 0) return;
+    size_t row = (size_t)Hkv * D;
+    uint16_t* kk = (uint16_t*)malloc(sizeof(uint16_t) * row * (size_t)L);
+    uint16_t* vv = (uint16_t*)malloc(sizeof(uint16_t) * row * (size_t)L);
+    if (!kk || !vv) {
+        free(kk), free(vv);
+        atomic_store(&X->bad, 2);
+        return;
+    }
+    for (int t = 0; t < L; ++t) {
+        int pidx = t / X->ps;
+        int page = pidx < X->max_pages ? X->bt[(size_t)b * X->max_pages + pidx] : -1;
+        if (page < 0 || page >= X->num_pages) {
+            atomic_store(&X->bad, 1);
+            free(kk), free(vv);
+            return;
+        }
+        size_t src = ((size_t)page * X->ps + (size_t)(t % X->ps)) * row;
+        memcpy(kk + (size_t)t * row, X->kc + src, sizeof(uint16_t) * row);
+        memcpy(vv + (size_t)t * row, X->vc + src, sizeof(uint16_t) * row);
+    }
+    seq_view sv;
+    sv.q = X->q + (size_t)q0 * X->Hq * D; /* the request's new rows [nq, Hq, D] */
+    sv.q_single = 0;
+    sv.q_first = L - nq;
+    sv.k = kk, sv.v = vv, sv.dO = NULL, sv.L = L, sv.Hq = X->Hq, sv.Hkv = Hkv, sv.D = D;
+    sv.scale = X->scale, sv.causal = 1, sv.window = X->window;
+    for (int i = 0; i < nq; ++i)
+        for (int h = 0; h < X->Hq; ++h)
+            row_forward(&sv, h, L - nq + i, scratch, X->o + ((size_t)(q0 + i) * X->Hq + h) * D,
+                        &X->lse[(size_t)h * X->T + q0 + i]);
+    free(kk), free(vv);
+}
+
+int oracle_attn_prefill_paged(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                              const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q, int B, int Hq,
+                              int Hkv, int D, int page_size, int max_pages, int num_pages, double scale, int window,
+                              double* o, double* lse, int nthreads) {
+    if (check_heads(Hq, Hkv, D) || B < 0 || page_size <= 0 || max_pages < 0 || num_pages < 0) return -1;
+    int maxL = 1;
+    for (int b = 0; b < B; ++b) {
+        if (seq_lens[b] < 0) return -1;
+        if (seq_lens[b] > maxL) maxL = seq_lens[b];
+    }
+    prefill_paged_ctx X = {q, k_cache, v_cache, block_table, seq_lens, cu_q, Hq, Hkv, D, page_size, max_pages,
+                           num_pages, window, (int64_t)cu_q[B], scale, o, lse, 0};
+    atomic_init(&X.bad, 0);
+    int rc = parallel_for(B, nthreads, (size_t)maxL, prefill_paged_item, &X);
     if (rc) return rc;
     return atomic_load(&X.bad) ? -1 : 0;
 }

@@ -228,6 +228,58 @@ def paged_from_lengths(seq_lens, Hq, Hkv, D, page_size=16, num_pages=4096, seed=
                  float(scale if scale is not None else D ** -0.5), seq_lens.astype(np.int32), bt, q, kc, vc)
 
 
+@dataclass
+class PagedPrefill:
+    """Chunked prefill over a paged KV cache: request b has seq_lens[b] cached tokens, the last
+    q_lens[b] of which are new queries (packed rows cu_q[b] .. cu_q[b+1]-1 of q)."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    page_size: int
+    num_pages: int
+    max_pages: int
+    window: int
+    scale: float
+    seq_lens: np.ndarray
+    q_lens: np.ndarray
+    cu_q: np.ndarray
+    block_table: np.ndarray = field(repr=False)
+    q: np.ndarray = field(repr=False)
+    k_cache: np.ndarray = field(repr=False)
+    v_cache: np.ndarray = field(repr=False)
+
+    @property
+    def B(self) -> int:
+        return len(self.seq_lens)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.cu_q[-1])
+
+    @property
+    def max_q(self) -> int:
+        return int(self.q_lens.max()) if len(self.q_lens) else 0
+
+
+def prefill_paged_from_lengths(seq_lens, q_lens, Hq, Hkv, D, page_size=16, num_pages=None, window=0, seed=0,
+                               scale=None, max_pages=None, name="prefill_paged") -> PagedPrefill:
+    seq_lens = np.asarray(seq_lens, dtype=np.int64)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    if np.any(q_lens > seq_lens) or np.any(q_lens < 0):
+        raise ValueError("each request needs 0 <= q_len <= seq_len")
+    need = (seq_lens + page_size - 1) // page_size
+    if num_pages is None:
+        num_pages = int(max(1, need.sum()) + 8)
+    base = paged_from_lengths(seq_lens, Hq, Hkv, D, page_size, num_pages, seed, scale, max_pages, name)
+    cu_q = np.zeros(len(q_lens) + 1, dtype=np.int32)
+    cu_q[1:] = np.cumsum(q_lens)
+    q = normal_bf16(seed, STREAM_Q, (int(cu_q[-1]), Hq, D))
+    return PagedPrefill(name, Hq, Hkv, D, page_size, num_pages, base.max_pages, int(window), base.scale,
+                        seq_lens.astype(np.int32), q_lens.astype(np.int32), cu_q, base.block_table, q, base.k_cache,
+                        base.v_cache)
+
+
 def paged(B, lo, hi, Hq, Hkv, D, page_size=16, num_pages=4096, seed=0, max_pages=None, name="paged") -> Paged:
     lens = uniform_int(seed, STREAM_CTX, B, lo, hi)
     if max_pages is None:
@@ -251,6 +303,14 @@ def swa_d256_w1024(seed=0, with_do=True) -> Dense:
 
 def varlen_d512_causal(seed=0, with_do=True) -> Varlen:
     return varlen(8, 512, 4096, 32, 4, 512, 0, seed, name="varlen_d512_causal", with_do=with_do)
+
+
+def prefill_paged_d512(seed=0) -> PagedPrefill:
+    """Chunked prefill of 512 new tokens per request over a paged cache: 8 requests with
+    contexts uniform in [1024, 4096] (the varlen workload's length law), head_dim 512, GQA 8:1."""
+    ctx = uniform_int(seed, STREAM_CTX, 8, 1024, 4096)
+    return prefill_paged_from_lengths(ctx, np.full(8, 512), 32, 4, 512, page_size=16, seed=seed,
+                                      name="prefill_paged_d512")
 
 
 def decode_paged_d128(seed=0) -> Paged:

@@ -10,7 +10,8 @@ oracle disagrees with:
   (pins the backward to the forward, whatever formula either uses),
 * closed forms (scale 0, window 1, identical keys, all-ones values),
 * invariants (wide window = causal, varlen = per-sequence dense, paged =
-  contiguous, decode = last prefill row, GQA = repeat-KV MHA, key shifts),
+  contiguous, decode = last prefill row, paged prefill = gathered keys with a
+  bottom-right mask and one new token = decode, GQA = repeat-KV MHA, key shifts),
 * the hand-worked examples under ``tests/golden``.
 
 The same pins run against deliberately broken builds of the oracle
@@ -289,6 +290,55 @@ def pin_paged(orc):
     assert np.all(o3[0] == 0) and np.all(np.isneginf(l3[0])) and np.all(np.isfinite(o3[1]))
 
 
+def pin_prefill_paged(orc):
+    """Chunked prefill over a paged cache vs torch fp64 SDPA on the gathered contiguous keys
+    with a bottom-right aligned mask (new query i of a request sits at position L - n + i),
+    with and without a window; single new token = decode; page relabelling changes nothing."""
+    for window in (0, 7):
+        pp = synth.prefill_paged_from_lengths([1, 16, 17, 40, 33, 9], [1, 5, 17, 12, 0, 9], 6, 2, 16, page_size=16,
+                                              window=window, seed=21)
+        o, lse = orc.prefill_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.cu_q, pp.scale,
+                                   window)
+        for b in range(pp.B):
+            L, n, r0 = int(pp.seq_lens[b]), int(pp.q_lens[b]), int(pp.cu_q[b])
+            if n == 0:
+                continue
+            tok = np.arange(L)
+            pages = pp.block_table[b, tok // 16]
+            kt = torch.tensor(_f(pp.k_cache[pages, tok % 16])).permute(1, 0, 2)[None]  # 1, Hkv, L, D
+            vt = torch.tensor(_f(pp.v_cache[pages, tok % 16])).permute(1, 0, 2)[None]
+            qt = torch.tensor(_f(pp.q[r0:r0 + n])).permute(1, 0, 2)[None]  # 1, Hq, n, D
+            pos = np.arange(L - n, L)[:, None]
+            j = np.arange(L)[None, :]
+            m = j <= pos
+            if window > 0:
+                m &= (pos - j) < window
+            mask = torch.tensor(m)
+            to = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=pp.scale,
+                                                                  enable_gqa=True)
+            G = pp.Hq // pp.Hkv
+            sc = (qt @ kt.repeat_interleave(G, dim=1).transpose(-1, -2)) * pp.scale
+            tl = torch.logsumexp(sc.masked_fill(~mask, float("-inf")), dim=-1)
+            _close(o[r0:r0 + n], to[0].permute(1, 0, 2).numpy(), 1e-12, f"prefill_paged o vs torch (W={window})")
+            _close(lse[:, r0:r0 + n], tl[0].numpy(), 1e-12, f"prefill_paged lse vs torch (W={window})")
+    # one new token per request is the decode
+    pd = synth.paged_from_lengths([5, 16, 33], 8, 2, 32, page_size=16, num_pages=8, seed=22, max_pages=3)
+    od, ld = orc.decode_paged(pd.q, pd.k_cache, pd.v_cache, pd.block_table, pd.seq_lens, pd.scale)
+    cu = np.arange(pd.B + 1, dtype=np.int32)
+    op, lp = orc.prefill_paged(pd.q, pd.k_cache, pd.v_cache, pd.block_table, pd.seq_lens, cu, pd.scale)
+    _close(op, od, 0, "prefill_paged with one token = decode (o)")
+    _close(lp.T, ld, 0, "prefill_paged with one token = decode (lse)")
+    # relabelling the pool changes nothing
+    pp = synth.prefill_paged_from_lengths([40, 23], [40, 7], 4, 1, 16, page_size=16, seed=23)
+    o, lse = orc.prefill_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.cu_q, pp.scale)
+    perm = np.random.default_rng(6).permutation(pp.num_pages)
+    inv = np.argsort(perm)
+    bt2 = np.where(pp.block_table >= 0, perm[np.maximum(pp.block_table, 0)], -1).astype(np.int32)
+    o2, l2 = orc.prefill_paged(pp.q, pp.k_cache[inv], pp.v_cache[inv], bt2, pp.seq_lens, pp.cu_q, pp.scale)
+    _close(o2, o, 0, "prefill_paged page relabelling (o)")
+    _close(l2, lse, 0, "prefill_paged page relabelling (lse)")
+
+
 def pin_golden(orc):
     for name in ("two_token_causal.json", "three_token_window2.json"):
         g = json.load(open(os.path.join(GOLDEN, name)))
@@ -345,4 +395,4 @@ def pin_sampled_rows(orc):
 
 
 ALL_PINS = [pin_golden, pin_torch_forward, pin_torch_backward, pin_finite_differences, pin_closed_forms,
-            pin_invariants, pin_varlen, pin_paged, pin_sampled_rows]
+            pin_invariants, pin_varlen, pin_paged, pin_prefill_paged, pin_sampled_rows]
