@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
 
 * ``attn_fwd(q, k, v, ...)``          q [B,S,Hq,D], k/v [B,S,Hkv,D] -> (o, lse[B,Hq,S])
 * ``attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, ...)``  packed [T,H,D] -> (o, lse[Hq,T])
+* ``attn_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q_len, ...)``
+  chunked prefill over a paged cache: packed new tokens [T,Hq,D] -> (o, lse[Hq,T])
 * ``attn_bwd(q, k, v, o, lse, dO, ...)``  -> (dQ, dK, dV); dense or packed (cu_seqlens)
 * ``attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, ...)`` -> (o, lse[B,Hq])
 * ``attn_workspace_size``, ``attn_get_device_status``, ``attn_status_string``
@@ -26,7 +28,7 @@ import os
 import threading
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
+    "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
     "attn_get_device_status", "attn_status_string", "library_path", "load_library",
     "attn_launch_count", "attn_profile_start", "attn_profile_stop", "attn_decode_paged_noalloc",
     "attn_selftest_wait_timeout",
@@ -67,6 +69,7 @@ def load_library():
         P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, Z, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
+        lib.attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, I, P]
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P, I, I, P, Z, P]
         lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
         lib.attn_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
@@ -83,7 +86,7 @@ def load_library():
         lib.attn_profile_start.restype = I
         lib.attn_profile_stop.argtypes = [ctypes.c_char_p, Z]
         lib.attn_profile_stop.restype = I
-        for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_bwd, lib.attn_decode_paged, lib.attn_get_device_status):
+        for f in (lib.attn_fwd, lib.attn_fwd_varlen, lib.attn_fwd_paged, lib.attn_bwd, lib.attn_decode_paged, lib.attn_get_device_status):
             f.restype = I
         _lib = lib
         return lib
@@ -212,6 +215,30 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, o=None, lse=None, *, c
                                         _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, D,
                                         scale, int(causal), int(window), None, 0, _stream_ptr(stream, q.device))
     _check(rc, "attn_fwd_varlen")
+    return o, lse
+
+
+def attn_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q_len: int, o=None, lse=None, *,
+                   causal: bool = True, window: int = 0, scale: float | None = None, stream=None):
+    """Chunked prefill: q [T,Hq,D] new tokens packed by cu_q, caches [pages,16,Hkv,D], block_table int32
+    [R,max_pages], seq_lens int32 [R] (cached tokens including the new ones), cu_q int32 [R+1]."""
+    import torch
+
+    T, Hq, D = q.shape
+    num_pages, page_size, Hkv, _ = k_cache.shape
+    scale = float(scale if scale is not None else 1.0 / math.sqrt(D))
+    for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_fwd_paged(
+        _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
+        _ptr(cu_q), _bf16(o, "o"), _ptr(lse), cu_q.numel() - 1, T, int(max_q_len), Hq, Hkv, D, page_size,
+        block_table.shape[1], num_pages, scale, int(causal), int(window), _stream_ptr(stream, q.device))
+    _check(rc, "attn_fwd_paged")
     return o, lse
 
 

@@ -107,6 +107,20 @@ bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int rows, int 
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 5-D map over a paged cache [num_pages, 16, heads, dim] viewed as (64 dims, 8 rows, heads*dim/64
+// chunks of 64 dims, 2 groups of 8 rows, pages); box = 64 x 8 x 2 x 2 x 1: 16 rows x 128 dims of
+// one head of one page (4 KB), the two 64-dim chunks interleaved per 8-row group.
+bool make_cache_map(CUtensorMap* m, const void* base, int D, int H, int num_pages) {
+    const cuuint64_t row = (cuuint64_t)H * D * 2;
+    cuuint64_t dims[5] = {64, 8, (cuuint64_t)H * D / 64, 2, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
+    cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int check_common(int Hq, int Hkv, float scale, int causal, int window) {
@@ -305,6 +319,38 @@ int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
     if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
     return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, 1, Hq, Hkv, D, scale, window,
                       stream);
+}
+
+int attn_fwd_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache, const int32_t* block_table,
+                   const int32_t* seq_lens, const int32_t* cu_q, attn_bf16* o, float* lse, int num_reqs, int total_q,
+                   int max_q_len, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages,
+                   float scale, int causal, int window, void* stream) {
+    if (num_reqs < 0 || total_q < 0 || max_q_len < 0 || max_pages_per_seq < 0 || num_pages < 0 || page_size <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    int st = check_common(Hq, Hkv, scale, causal, window);
+    if (st) return st;
+    if ((st = check_prefill_shape(total_q, Hq, Hkv, D, max_q_len))) return st;
+    if (page_size != 16 || num_reqs > 65535 / (D / 256) || max_pages_per_seq > (1 << 24)) return ATTN_ERR_UNSUPPORTED;
+    if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return ATTN_OK;  // nothing to read or write
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !cu_q || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(cu_q) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    if (num_pages == 0 || max_pages_per_seq == 0) return ATTN_ERR_INVALID_ARG;  // new tokens need cached pages
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    attn::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    if (!make_map(&L.tq, q, D, Hq, total_q, 1) || !make_cache_map(&L.tk, k_cache, D, Hkv, num_pages) ||
+        !make_cache_map(&L.tv, v_cache, D, Hkv, num_pages))
+        return ATTN_ERR_LAUNCH;
+    L.o = o, L.lse = lse, L.cu_seqlens = nullptr, L.status = dev->status;
+    L.nseq = num_reqs, L.Hq = Hq, L.Hkv = Hkv, L.S = max_q_len, L.D = D, L.total_rows = total_q, L.window = window;
+    L.scale = scale;
+    L.block_table = block_table, L.seq_lens = seq_lens, L.cu_q = cu_q;
+    L.max_pages = max_pages_per_seq, L.num_pages = num_pages;
+    return attn::launch_fwd(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const attn_bf16* o, const float* lse,

@@ -17,7 +17,10 @@
 // 5 slots at D = 256, 3 at D = 512.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer (one thread): Q once, then K/V slots in MMA order
+//   warp 0      TMA producer (one thread): Q once, then K/V slots in MMA order. Over a
+//               paged cache the whole warp works: eight lanes fetch one tile's page ids a
+//               tile ahead and each issues its page's box into every slot of the tile, and
+//               the warp zeroes the last tile's V rows past the sequence end before its P V
 //   warp 1      TMEM owner; one thread issues every UMMA and commit
 //   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Masking, fp32 online
 //               softmax in the log2 domain with lazy rescaling (the running max moves
@@ -39,6 +42,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t kSubBytes = 16384;  // 128 rows x 64 bf16
 constexpr float kRescaleLog2 = 8.0f;
+constexpr uint32_t kPagedGroupStride = 2048;  // paged slots: bytes between 8-row groups
 
 template <int DQK>
 struct FwdCfg {
@@ -58,9 +62,23 @@ struct FwdArgs {
     unsigned* status;
     int Hq, Hkv, S, D, window, n_qtiles, nsplit, T;
     float scale_log2;
+    // paged prefill: keys / values through a block table, new queries packed by cu_q
+    const int32_t *block_table, *seq_lens, *cu_q;
+    int max_pages, num_pages;
 };
 
-template <int DQK>
+// PAGED: chunked prefill over a paged cache ("flex_attention + paged KV + CUDA graphs vs
+// vLLM", "Architecture notes": keys and values are read through the block table). A
+// sequence is one request: its n new query rows are the last n of its L cached tokens, so
+// query index i sits at position L - n + i. Key tile t is 8 pages of 16 tokens. A slot is
+// filled by eight 4 KB boxes, one per page: the page's 16 rows x 128 columns of one head,
+// taken by a 5-D tensor map over the cache [num_pages, 16, Hkv, D] viewed as
+// (64 columns, 8 rows, Hkv*D/64 column chunks, 2 row groups, pages). In shared memory the
+// slot then holds 8-row groups of both 64-column chunks interleaved: chunk c of row group G
+// (keys 8G .. 8G+7) at byte G*2048 + c*1024, each a 1 KB 128-byte-swizzle atom. The MMA
+// descriptors differ only in their strides (kPagedGroupStride); one box moves 256 bytes per
+// row, which the TMA engine streams about 1.5x faster than sixteen 16-row boxes of 64 columns.
+template <int DQK, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, FwdArgs a) {
@@ -70,17 +88,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq = blockIdx.y / a.nsplit, split = blockIdx.y % a.nsplit;
     const int q_tile = a.n_qtiles - 1 - (int)blockIdx.z;  // longest tiles first
     int seq_start = 0, L = a.S, bcoord = seq;
-    if (a.cu_seqlens) {
+    int nq = a.S, qoff = 0;  // query rows of the sequence; position of its query row 0
+    if (PAGED) {
+        seq_start = a.cu_q[seq];
+        nq = a.cu_q[seq + 1] - seq_start;
+        L = a.seq_lens[seq];
+        bcoord = 0;
+        if (seq_start < 0 || nq < 0 || seq_start + nq > a.T || nq > L || L > a.max_pages * 16) {
+            // inconsistent request: reported, nothing read or written
+            if (threadIdx.x == 0 && split == 0 && h == 0 && q_tile == a.n_qtiles - 1) atomicOr(a.status, DEVSTAT_BOUNDS);
+            return;
+        }
+        qoff = L - nq;
+    } else if (a.cu_seqlens) {
         seq_start = a.cu_seqlens[seq];
         L = a.cu_seqlens[seq + 1] - seq_start;
+        nq = L;
         bcoord = 0;
     }
     const int q0 = q_tile * kBQ;
-    if (q0 >= L) return;  // uniform: before any barrier or TMEM use
+    if (q0 >= nq) return;  // uniform: before any barrier or TMEM use
+    const int qp0 = qoff + q0;  // position of the tile's first query
     const int g = h / (a.Hq / a.Hkv);
     const int dv0 = split * kDV;
-    const int kv_hi = min(L, q0 + kBQ);
-    const int kv_lo = a.window > 0 ? max(0, q0 - a.window + 1) : 0;
+    const int kv_hi = min(L, qp0 + kBQ);
+    const int kv_lo = a.window > 0 ? max(0, qp0 - a.window + 1) : 0;
     const int t_begin = kv_lo / kBKV, t_end = (kv_hi + kBKV - 1) / kBKV;
     const int n = t_end - t_begin;
 
@@ -96,7 +128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* p_full = s_full + 2;             // 1
     uint64_t* pv_done = p_full + 1;            // 1
     uint64_t* mma_idle = pv_done + 1;          // 1
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
+    uint64_t* vfix = mma_idle + 1;             // 1 (paged): the last tile's V rows past the end are zeroed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vfix + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -112,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(p_full), 128);
         mbar_init(smem_u32(pv_done), 1);
         mbar_init(smem_u32(mma_idle), 1);
+        mbar_init(smem_u32(vfix), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -124,7 +158,116 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tbase = *tmem_slot;
     const uint32_t tO = tbase, tS0 = tbase + 256;
 
-    if (warp == 0) {
+    // keys past the end in the last tile (paged: their cache rows may hold any bits)
+    const bool tail_fix = PAGED && (t_end * kBKV > L);
+    if (warp == 0 && PAGED) {
+        // -------------------- TMA producer, paged keys / values (whole warp) ---------------
+        const int npg = (L + 15) / 16;  // pages of the request
+        const int32_t* bt = a.block_table + (size_t)seq * a.max_pages;
+        auto page_id = [&](int tile) -> int {  // lane i < 8: id of page i of key tile `tile`
+            if (lane >= 8) return 0;
+            const int pi = tile * 8 + lane;
+            int id = bt[pi < npg ? pi : 0];  // pages past the request: its first page (masked anyway)
+            if (id < 0 || id >= a.num_pages) {
+                atomicOr(a.status, DEVSTAT_BOUNDS);
+                id = 0;
+            }
+            return id;
+        };
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            mbar_expect_tx(smem_u32(q_full), C::kQBytes);
+            for (int c = 0; c < DQK / 64; ++c)
+                tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, seq_start + q0, 0);
+        }
+        int slot = 0, round = 0;
+        bool ok = true;
+        // one slot = 128 keys x 128 columns: lane i < 8 loads page i's 4 KB box
+        const int chunk0 = g * (DQK / 64);  // first 64-column chunk of KV head g
+        auto load_slot = [&](const CUtensorMap* map, int col0, int ids, int& used_slot, int& used_round) -> bool {
+            if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag,
+                                                                 a.status, 0x11)))
+                return false;
+            const uint32_t fb = smem_u32(&full[slot]);
+            if (lane == 0) mbar_expect_tx(fb, kSlotBytes);
+            const uint32_t dst = sSlots + slot * kSlotBytes;
+            if (lane < 8) tma_load_5d(dst + lane * 4096, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
+            used_slot = slot, used_round = round;
+            if (++slot == C::kStages) slot = 0, ++round;
+            return true;
+        };
+        // page ids one tile ahead, separately for the K and the V sequence
+        int k_cur = page_id(t_begin), k_nxt = n > 1 ? page_id(t_begin + 1) : 0;
+        int v_cur = k_cur, v_nxt = k_nxt;
+        int vs[C::kVChunks], vr[C::kVChunks];
+        auto load_k = [&]() -> bool {
+            int us, ur;
+            for (int c = 0; c < C::kQChunks; ++c)
+                if (!load_slot(&tk, c * 128, k_cur, us, ur)) return false;
+            return true;
+        };
+        auto load_v = [&]() -> bool {
+            for (int c = 0; c < C::kVChunks; ++c)
+                if (!load_slot(&tv, dv0 + c * 128, v_cur, vs[c], vr[c])) return false;
+            return true;
+        };
+        int kt = 0, vt = 0;  // next K / V tile to load
+        auto next_k = [&]() {
+            ++kt;
+            k_cur = k_nxt;
+            k_nxt = kt + 1 < n ? page_id(t_begin + kt + 1) : 0;
+        };
+        auto next_v = [&]() {
+            ++vt;
+            v_cur = v_nxt;
+            v_nxt = vt + 1 < n ? page_id(t_begin + vt + 1) : 0;
+        };
+        ok = load_k();
+        next_k();
+        if (ok && n > 1) {
+            ok = load_k();
+            next_k();
+        }
+        for (int j = 0; ok && j < n; ++j) {
+            ok = load_v();
+            next_v();
+            if (ok && j + 2 < n) {
+                ok = load_k();
+                next_k();
+            }
+        }
+        if (ok && tail_fix) {
+            // zero the rows of keys >= L in the last tile's V slots before their P V (P is 0 there,
+            // but 0 * NaN is not 0)
+            const int r_valid = L - (t_end - 1) * kBKV;  // 1 .. 127
+            for (int c = 0; ok && c < C::kVChunks; ++c)
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[vs[c]]), vr[c] & 1, abort_flag, a.status, 0x1e));
+            if (ok) {
+                const int units = (kBQ - r_valid) * 16;  // 16-byte pieces of the rows past the end (2 chunks)
+                for (int c = 0; c < C::kVChunks; ++c) {
+                    const uint32_t base = sSlots + vs[c] * kSlotBytes;
+                    for (int e = lane; e < units; e += 32) {
+                        const int row = r_valid + (e >> 4), chunk = (e >> 3) & 1, piece = e & 7;
+                        st_shared_v4(base + (row >> 3) * kPagedGroupStride + chunk * 1024 + (row & 7) * 128 + piece * 16,
+                                     0u, 0u, 0u, 0u);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(vfix));
+            }
+        }
+        if (lane == 0) {
+            const int issued = round * C::kStages + slot;
+            for (int s = 0; s < C::kStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x18);
+            }
+            mbar_drain(smem_u32(q_full), 0, a.status, 0x19);
+        }
+    } else if (warp == 0) {
         // ------------------------------- TMA producer ----------------------------------
         if (lane == 0) {
             prefetch_tmap(&tq);
@@ -195,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int sub = 0; sub < 2; ++sub)
                         for (int kk = 0; kk < 4; ++kk) {
                             const uint64_t ad = sdesc_sw128(sQ + (2 * c + sub) * kSubBytes + kk * 32, 16, 1024);
-                            const uint64_t bd = sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
+                            const uint64_t bd = PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, kPagedGroupStride)
+                                                      : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
                             umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
                         }
                     release_slot();
@@ -206,10 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_pv = [&](int j) -> bool {
                 for (int c = 0; c < C::kVChunks; ++c) {
                     if (!next_slot()) return false;
+                    if (tail_fix && j == n - 1 && c == 0) {  // the producer zeroed the rows past the end
+                        if (!mbar_wait(smem_u32(vfix), 0, abort_flag, a.status, 0x1f)) return false;
+                        tc_fence_after();
+                    }
                     const uint32_t vslot = sSlots + slot * kSlotBytes;
                     const uint32_t tP = tS0 + (j & 1) * 128;  // P of step j, packed bf16 pairs
                     for (int kk = 0; kk < 8; ++kk) {          // 16 keys per step
-                        const uint64_t bd = sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
+                        const uint64_t bd = PAGED ? sdesc_sw128(vslot + kk * 2 * kPagedGroupStride, 1024, kPagedGroupStride)
+                                                  : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
                         umma_bf16_ts(tO + c * 128, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     release_slot();
@@ -234,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------- softmax --------------------------------------
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // query row within the tile == TMEM lane
-        const int qi = q0 + r;           // query index within the sequence
+        const int qi = qp0 + r;          // position of the query in its sequence
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
@@ -253,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[e]);
             }
             const int key0 = (t_begin + j) * kBKV;
-            const bool edge = (key0 + kBKV - 1 > q0) || (a.window > 0 && q0 + kBQ - 1 - key0 >= a.window) ||
+            const bool edge = (key0 + kBKV - 1 > qp0) || (a.window > 0 && qp0 + kBQ - 1 - key0 >= a.window) ||
                               (key0 + kBKV > L);
             if (edge) {
 #pragma unroll
@@ -325,9 +474,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         if (ok) {
-            const bool row_ok = qi < L;
+            const int qrow = q0 + r;  // query row index within the sequence's rows
+            const bool row_ok = qrow < nq;
+            const bool packed = PAGED || a.cu_seqlens;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint16_t* orow = a.o + ((size_t)(a.cu_seqlens ? seq_start + qi : seq * a.S + qi) * a.Hq + h) * a.D + dv0;
+            uint16_t* orow = a.o + ((size_t)(packed ? seq_start + qrow : seq * a.S + qrow) * a.Hq + h) * a.D + dv0;
 #pragma unroll 1
             for (int c = 0; c < kDV / 32; ++c) {
                 uint32_t raw[32];
@@ -347,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (row_ok && split == 0) {
                 const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
-                const size_t li = a.cu_seqlens ? (size_t)h * a.T + seq_start + qi : ((size_t)seq * a.Hq + h) * a.S + qi;
+                const size_t li = packed ? (size_t)h * a.T + seq_start + qrow : ((size_t)seq * a.Hq + h) * a.S + qrow;
                 a.lse[li] = lse;
             }
         }
@@ -360,21 +511,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int DQK>
+template <int DQK, bool PAGED>
 cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     using C = FwdCfg<DQK>;
     FwdArgs a;
     a.o = L.o, a.lse = L.lse, a.cu_seqlens = L.cu_seqlens, a.status = L.status;
+    a.block_table = L.block_table, a.seq_lens = L.seq_lens, a.cu_q = L.cu_q;
+    a.max_pages = L.max_pages, a.num_pages = L.num_pages;
     a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.D = L.D, a.window = L.window;
     a.n_qtiles = (L.S + kBQ - 1) / kBQ;
     a.nsplit = DQK / kDV;
     a.T = L.total_rows;
     a.scale_log2 = L.scale * 1.4426950408889634f;
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<DQK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel<DQK, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.Hq, L.nseq * a.nsplit, a.n_qtiles);
-    const ProfMark m = prof_begin(stream, DQK == 256 ? "fwd_d256" : "fwd_d512");
-    fwd_kernel<DQK><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
+    const char* name = PAGED ? (DQK == 256 ? "fwd_paged_d256" : "fwd_paged_d512") : (DQK == 256 ? "fwd_d256" : "fwd_d512");
+    const ProfMark m = prof_begin(stream, name);
+    fwd_kernel<DQK, PAGED><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
     prof_end(stream, m);
     return cudaGetLastError();
 }
@@ -383,8 +538,9 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     if (L.nseq == 0 || L.S == 0) return cudaSuccess;
-    if (L.D == 256) return launch_fwd_t<256>(L, stream);
-    if (L.D == 512) return launch_fwd_t<512>(L, stream);
+    const bool paged = L.block_table != nullptr;
+    if (L.D == 256) return paged ? launch_fwd_t<256, true>(L, stream) : launch_fwd_t<256, false>(L, stream);
+    if (L.D == 512) return paged ? launch_fwd_t<512, true>(L, stream) : launch_fwd_t<512, false>(L, stream);
     return cudaErrorInvalidValue;
 }
 

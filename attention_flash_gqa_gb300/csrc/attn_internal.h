@@ -36,18 +36,26 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream);
 
 // ---- prefill forward ---------------------------------------------------------------------
 // q/k/v tensor maps are 4-D over [D, H, S, B] (varlen: B = 1, S = total tokens) with a
-// 64 x 1 x 128 x 1 box and 128-byte swizzle.
+// 64 x 1 x 128 x 1 box and 128-byte swizzle. Paged prefill: q as varlen over the packed new
+// tokens; k/v over the caches as 5-D (64, 8, Hkv*D/64, 2, num_pages) with a 64 x 8 x 2 x 2 x 1
+// box (16 rows x 128 dims of one head of one page).
 struct FwdLaunch {
     CUtensorMap tq, tk, tv;
     uint16_t* o;
     float* lse;
-    const int32_t* cu_seqlens;  // null: dense
+    const int32_t* cu_seqlens;  // null: dense (or paged)
     unsigned* status;
-    int nseq;                   // B (dense) or num_seqs (varlen)
-    int Hq, Hkv, S, D;          // S: dense sequence length or max_seqlen (varlen)
-    int total_rows;             // B*S (dense) or total tokens (varlen)
+    int nseq;                   // B (dense), num_seqs (varlen) or num_reqs (paged)
+    int Hq, Hkv, S, D;          // S: dense sequence length, max_seqlen (varlen) or max new tokens (paged)
+    int total_rows;             // B*S (dense), total tokens (varlen) or total new tokens (paged)
     int window;
     float scale;
+    // paged prefill (block_table non-null): request b's n_b = cu_q[b+1] - cu_q[b] new tokens
+    // are the last n_b of its seq_lens[b] cached tokens
+    const int32_t* block_table = nullptr;  // [num_reqs, max_pages]
+    const int32_t* seq_lens = nullptr;
+    const int32_t* cu_q = nullptr;
+    int max_pages = 0, num_pages = 0;
 };
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream);
 

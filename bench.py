@@ -369,7 +369,8 @@ def finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launch
 
 
 def bench_extra(args, attn, synth, peaks, peak_src, clocks):
-    """Sliding-window d256 fwd+bwd, varlen d512 fwd+bwd, paged decode (GB/s)."""
+    """Sliding-window d256 fwd+bwd, varlen d512 fwd+bwd, paged-cache chunked prefill d512 (forward),
+    paged decode (GB/s)."""
     import numpy as np
     import torch
 
@@ -431,6 +432,28 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
     res["varlen_d512_causal"] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
                                  "seqlens": [int(x) for x in vp.seqlens], "kernel_ms": kern_ms}
     del q, k, v, do, o, lse, dq, dk, dv
+
+    # chunked prefill over a paged cache, d512 (forward only: the new tokens' attention)
+    pf = synth.prefill_paged_d512(seed=7)
+    qp, kcp, vcp = to_dev(pf.q), to_dev(pf.k_cache), to_dev(pf.v_cache)
+    btp = torch.from_numpy(pf.block_table).cuda()
+    slp = torch.from_numpy(pf.seq_lens).cuda()
+    cuq = torch.from_numpy(pf.cu_q).cuda()
+    op = torch.empty_like(qp)
+    lp = torch.empty((pf.Hq, pf.total_q), dtype=torch.float32, device="cuda")
+    pf_step = lambda: attn.attn_fwd_paged(qp, kcp, vcp, btp, slp, cuq, pf.max_q, op, lp, scale=pf.scale)
+    ms = timed(pf_step, max(10, steps))
+    kern_ms = per_kernel(pf_step)
+    # query i of a request with L cached and n new tokens sees L - n + i + 1 keys
+    pairs = sum(int(n) * (int(L) - int(n)) + int(n) * (int(n) + 1) // 2 for L, n in zip(pf.seq_lens, pf.q_lens))
+    fl = 4 * pf.D * pf.Hq * pairs
+    res["prefill_paged_d512"] = {
+        "value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_call": ms,
+        "frac_of_bf16_peak_sustained": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "seq_lens": [int(x) for x in pf.seq_lens], "new_tokens": [int(x) for x in pf.q_lens],
+        "all_finite": bool(torch.isfinite(op.float()).all()), "kernel_ms": kern_ms,
+        "l2": "inputs larger than L2 (q 134 MB, caches 2 x 84 MB)"}
+    del qp, kcp, vcp, op, lp
 
     # paged decode: time the kernel alone, flushing L2 (write > L2) between calls
     pp = synth.decode_paged_d128(seed=7)

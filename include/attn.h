@@ -105,6 +105,36 @@ ATTN_API int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_
                     float scale, int causal, int window, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * attn_fwd_paged -- chunked prefill over a paged KV cache: each request appends n_b new
+ * tokens whose keys and values are already written into its pages, and those n_b queries
+ * attend causally to the request's whole cache ("flex_attention + paged KV ..." page,
+ * "Architecture notes": keys and values are gathered through the block table).
+ *   q [total_q, Hq, D] bf16: the new tokens of all requests, packed; request b owns rows
+ *   cu_q[b] .. cu_q[b+1]-1. cu_q: DEVICE int32 [num_reqs + 1], non-decreasing, cu_q[0] = 0,
+ *   cu_q[num_reqs] = total_q.
+ *   k_cache, v_cache [num_pages, page_size, Hkv, D] bf16; block_table DEVICE int32
+ *   [num_reqs, max_pages_per_seq]: page ids of request b in order; seq_lens DEVICE int32
+ *   [num_reqs]: L_b, its cached tokens INCLUDING the n_b new ones. New query i of request b
+ *   is token L_b - n_b + i and sees keys 0 .. L_b - n_b + i (with window > 0 only the last
+ *   `window` of them). n_b = 1 is single-token decode; n_b = L_b is a first prefill.
+ *   o [total_q, Hq, D] bf16 out; lse [Hq, total_q] fp32 out (natural log).
+ *   max_q_len: an upper bound on every n_b (sizes the grid without reading cu_q on the
+ *   host); query rows past it are not computed. A request with n_b > L_b or
+ *   L_b > max_pages_per_seq * page_size, or a page id outside [0, num_pages), is reported
+ *   as ATTN_ERR_DEVICE_BOUNDS by attn_get_device_status() (the bad request's rows are left
+ *   unwritten; a bad page id is replaced by page 0). Cache slots past L_b in a request's
+ *   last page are never used, whatever they hold.
+ *   Supported: D in {256, 512}, page_size = 16, num_reqs <= 65535 / (D / 256). No workspace.
+ *   With num_reqs, total_q or max_q_len zero there is nothing to compute: the call checks
+ *   its scalar arguments and returns ATTN_OK, and the pointers may then be NULL.
+ */
+ATTN_API int attn_fwd_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
+                            const int32_t* block_table, const int32_t* seq_lens, const int32_t* cu_q, attn_bf16* o,
+                            float* lse, int num_reqs, int total_q, int max_q_len, int Hq, int Hkv, int D,
+                            int page_size, int max_pages_per_seq, int num_pages, float scale, int causal, int window,
+                            void* stream);
+
+/*
  * attn_bwd -- gradient of the forward above with respect to q, k and v, given dO.
  *   Inputs q, k, v, o (the forward's output), lse (the forward's log-sum-exp) and dO in
  *   the forward's layouts; outputs dQ [.., Hq, D], dK, dV [.., Hkv, D] bf16 (dK/dV sum

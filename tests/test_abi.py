@@ -29,7 +29,7 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = set(declared_functions())
-    assert {"attn_fwd", "attn_bwd", "attn_fwd_varlen", "attn_decode_paged"} <= names
+    assert {"attn_fwd", "attn_bwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_decode_paged"} <= names
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -132,6 +132,29 @@ def test_decode_argument_checks(lib):
     assert call(ws=None) == WORKSPACE
     assert call(wsb=100) == WORKSPACE
     assert call(B=0) == OK
+
+
+def test_prefill_paged_argument_checks(lib):
+    def call(q=P(A), bt=P(A), cu=P(A), R=3, T=600, maxq=512, Hq=32, Hkv=4, D=512, ps=16, maxp=256, npages=4096,
+             scale=0.044, causal=1, window=0):
+        return lib.attn_fwd_paged(q, P(A), P(A), bt, P(A), cu, P(A), P(A), R, T, maxq, Hq, Hkv, D, ps, maxp, npages,
+                                  scale, causal, window, None)
+    assert call(bt=None) == INVALID
+    assert call(cu=None) == INVALID
+    assert call(R=-1) == INVALID
+    assert call(T=-1) == INVALID
+    assert call(Hq=30) == INVALID
+    assert call(scale=float("nan")) == INVALID
+    assert call(window=-2) == INVALID
+    assert call(npages=0) == INVALID  # new tokens but no cache
+    assert call(causal=0) == UNSUPPORTED
+    assert call(D=128) == UNSUPPORTED
+    assert call(ps=32) == UNSUPPORTED
+    assert call(R=40000) == UNSUPPORTED  # 2 CTAs per (request, head) at D = 512
+    assert call(q=P(A + 8)) == MISALIGNED
+    assert call(cu=P(A + 2)) == MISALIGNED
+    assert call(T=0) == OK
+    assert call(R=0, q=None, bt=None, cu=None) == OK  # nothing to do: pointers may be NULL
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
