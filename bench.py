@@ -553,6 +553,43 @@ def bench_reference(args, rank, world):
     }
 
 
+def profile_case(args):
+    """Run one workload's kernel W + K times and print its device time, for profiler captures
+    on a reduced case (no bench line). prefill_paged_d512: the first `--requests` requests of
+    the chunked-prefill workload."""
+    import numpy as np
+    import torch
+
+    import attention_flash_gqa_gb300 as attn
+    import synth
+
+    attn.load_library()
+    torch.cuda.set_device(0)
+    if args.profile_case != "prefill_paged_d512":
+        raise SystemExit(f"unknown profile case {args.profile_case}")
+    full = synth.prefill_paged_d512(seed=7)
+    n = max(1, min(args.requests, full.B))
+    pf = synth.prefill_paged_from_lengths(full.seq_lens[:n], full.q_lens[:n], full.Hq, full.Hkv, full.D, seed=7)
+    qp, kc, vc = to_dev(pf.q), to_dev(pf.k_cache), to_dev(pf.v_cache)
+    bt, sl, cu = (torch.from_numpy(x).cuda() for x in (pf.block_table, pf.seq_lens, pf.cu_q))
+    o = torch.empty_like(qp)
+    lse = torch.empty((pf.Hq, pf.total_q), dtype=torch.float32, device="cuda")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        attn.attn_fwd_paged(qp, kc, vc, bt, sl, cu, pf.max_q, o, lse, scale=pf.scale)
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(args.steps):
+        attn.attn_fwd_paged(qp, kc, vc, bt, sl, cu, pf.max_q, o, lse, scale=pf.scale)
+    ev1.record()
+    torch.cuda.synchronize()
+    ok = bool(torch.isfinite(o.float()).all()) and attn.attn_get_device_status() == 0
+    print(json.dumps({"profile_case": args.profile_case, "requests": n, "seq_lens": [int(x) for x in pf.seq_lens],
+                      "ms_per_call": ev0.elapsed_time(ev1) / args.steps, "ok": ok}), flush=True)
+    if not ok:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -565,9 +602,14 @@ def main():
     ap.add_argument("--batch", type=int, default=2, help="batch of the dense workload (2 = the workload; 1 for "
                                                           "smaller profiler captures)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) leg")
+    ap.add_argument("--profile-case", default=None, help="run only this workload's kernel (for profiler captures)")
+    ap.add_argument("--requests", type=int, default=8, help="requests of the --profile-case workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
         world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
