@@ -71,6 +71,7 @@ class Oracle:
         lib.oracle_attn_decode_paged.argtypes = [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _d, _i, _p, _p, _i]
         lib.oracle_attn_prefill_paged.argtypes = [_p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _d, _i, _p, _p,
                                                   _i]
+        lib.oracle_merge_lse.argtypes = [_p, _p, _i, _i, _i, _i, _i, _p, _p]
         lib.oracle_mutant_id.restype = _i
         self.lib = lib
         self.mutant = lib.oracle_mutant_id()
@@ -211,6 +212,29 @@ class Oracle:
                                                        _ptr(o), _ptr(lse), nthreads or default_threads()),
                     "prefill_paged")
         return o, lse
+
+
+    def merge_lse(self, o_parts, lse_parts):
+        """Combine attention results over disjoint key sets. o_parts [P, B, S, H, D] (or
+        [P, T, H, D]) as bf16 bit patterns (uint16/int16) or floats; lse_parts [P, B, H, S]
+        (or [P, H, T]). Returns o [B, S, H, D] (or [T, H, D]) and lse [B, H, S] (or [H, T])."""
+        o_parts = np.asarray(o_parts)
+        if o_parts.dtype in (np.uint16, np.int16):
+            o_parts = (o_parts.astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        packed = o_parts.ndim == 4
+        if packed:
+            o_parts = o_parts[:, None]
+            lse_parts = np.asarray(lse_parts)[:, None]
+        o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+        lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+        P, B, S, H, D = o_parts.shape
+        if lse_parts.shape != (P, B, H, S):
+            raise ValueError("lse_parts shape does not match o_parts")
+        o = np.empty((B, S, H, D), np.float64)
+        lse = np.empty((B, H, S), np.float64)
+        self._check(self.lib.oracle_merge_lse(_ptr(o_parts), _ptr(lse_parts), P, B, S, H, D, _ptr(o), _ptr(lse)),
+                    "merge_lse")
+        return (o[0], lse[0]) if packed else (o, lse)
 
 
 _default = None

@@ -891,4 +891,69 @@ int oracle_attn_prefill_paged(const uint16_t* q, const uint16_t* k_cache, const 
     return atomic_load(&X.bad) ? -1 : 0;
 }
 
+/*
+ * Merge of attention results over disjoint key sets (the combining step of context-parallel
+ * ring attention). "Gemma4 FFPA attention backend support ...", "Integration": under
+ * context parallelism every ring chunk of keys is attended separately by the fused kernel
+ * (dense or varlen per chunk) and the chunks' results make up the attention over all keys.
+ * The pages do not write the combination out; it is the softmax over the union of the key
+ * sets. Part p holds o_p, normalised over its own keys, and lse_p = ln sum_{j in p} exp(s_j):
+ *
+ *   lse = ln sum_p exp(lse_p),    o = sum_p exp(lse_p - lse) o_p
+ *
+ * evaluated with the largest lse_p factored out of the sum (exact algebra, no overflow).
+ * A part with lse_p = -inf had no allowed key and contributes nothing; a row where every
+ * part has lse_p = -inf gets o = 0 and lse = -inf.
+ * Inputs o_parts [P, B, S, H, D] and lse_parts [P, B, H, S] in fp64; outputs o [B, S, H, D]
+ * and lse [B, H, S].
+ */
+int oracle_merge_lse(const double* o_parts, const double* lse_parts, int P, int B, int S, int H, int D, double* o,
+                     double* lse) {
+    if (P < 1 || B < 0 || S < 0 || H < 1 || D < 1) return -1;
+    const size_t rows = (size_t)B * S * H;
+    for (int b = 0; b < B; ++b)
+        for (int s = 0; s < S; ++s)
+            for (int h = 0; h < H; ++h) {
+                const size_t orow = (((size_t)b * S + s) * H + h) * D;
+                const size_t li = ((size_t)b * H + h) * S + s;
+                double m = -INFINITY;
+                for (int p = 0; p < P; ++p) {
+                    const double x = lse_parts[(size_t)p * B * H * S + li];
+                    if (x > m) m = x;
+                }
+                double* out = o + orow;
+                for (int d = 0; d < D; ++d) out[d] = 0.0;
+                if (m == -INFINITY) {
+                    lse[li] = -INFINITY;
+                    continue;
+                }
+                double sum = 0.0;
+                for (int p = 0; p < P; ++p) {
+#if ORACLE_MUTANT == 10
+                    sum += exp(lse_parts[(size_t)p * B * H * S + li]); /* planted: no max factored out */
+#else
+                    sum += exp(lse_parts[(size_t)p * B * H * S + li] - m);
+#endif
+                }
+#if ORACLE_MUTANT == 10
+                const double L = log(sum);
+#else
+                const double L = m + log(sum);
+#endif
+                lse[li] = L;
+                for (int p = 0; p < P; ++p) {
+                    const double lp = lse_parts[(size_t)p * B * H * S + li];
+                    if (lp == -INFINITY) continue;
+#if ORACLE_MUTANT == 9
+                    const double w = exp(L - lp); /* planted: weight with the sign flipped */
+#else
+                    const double w = exp(lp - L);
+#endif
+                    const double* src = o_parts + (size_t)p * rows * D + orow;
+                    for (int d = 0; d < D; ++d) out[d] += w * src[d];
+                }
+            }
+    return 0;
+}
+
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }

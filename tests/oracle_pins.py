@@ -339,6 +339,64 @@ def pin_prefill_paged(orc):
     _close(l2, lse, 0, "prefill_paged page relabelling (lse)")
 
 
+def _sdpa_part(q, k, v, scale, mask):
+    """torch fp64 attention of q [1,H,S,D] over the keys k, v [1,H,n,D] that `mask` [S,n] allows:
+    (o [S,H,D], lse [H,S]); rows with no allowed key give o = 0, lse = -inf."""
+    sc = (q @ k.transpose(-1, -2)) * scale
+    sc = sc.masked_fill(~mask, float("-inf"))
+    lse = torch.logsumexp(sc, dim=-1)  # 1, H, S
+    p = torch.exp(sc - torch.where(torch.isfinite(lse), lse, torch.zeros_like(lse))[..., None])
+    o = p @ v
+    return o[0].permute(1, 0, 2).numpy(), lse[0].numpy()
+
+
+def pin_merge_lse(orc):
+    """Merging attention results over disjoint key chunks reproduces torch fp64 attention over
+    all keys (non-causal and causal, so some chunks have rows with no allowed key); closed forms:
+    one part is the identity, two equal parts keep o and add ln 2 to lse, lse of order 1e4 does
+    not overflow, all-empty rows give o = 0 / lse = -inf; the order of the parts does not matter."""
+    rng = np.random.default_rng(31)
+    S, H, D = 23, 3, 16
+    q = torch.tensor(_f(synth.normal_bf16(31, 1, (S, H, D)))).permute(1, 0, 2)[None]
+    k = torch.tensor(_f(synth.normal_bf16(31, 2, (S, H, D)))).permute(1, 0, 2)[None]
+    v = torch.tensor(_f(synth.normal_bf16(31, 3, (S, H, D)))).permute(1, 0, 2)[None]
+    cuts = [0, 5, 6, 6, 17, 23]  # chunks of 5, 1, 0, 11, 6 keys
+    for causal in (False, True):
+        i = np.arange(S)[:, None]
+        full = (np.arange(S)[None, :] <= i) if causal else np.ones((S, S), bool)
+        ref_o, ref_l = _sdpa_part(q, k, v, 0.37, torch.tensor(full))
+        parts_o, parts_l = [], []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            po, pl = _sdpa_part(q, k[:, :, a:b], v[:, :, a:b], 0.37, torch.tensor(full[:, a:b]))
+            parts_o.append(po)
+            parts_l.append(pl)
+        po, pl = np.stack(parts_o), np.stack(parts_l)
+        o, lse = orc.merge_lse(po, pl)
+        _close(o, ref_o, 1e-12, f"merge of key chunks = attention over all keys (o, causal={causal})")
+        _close(lse, ref_l, 1e-12, f"merge of key chunks = attention over all keys (lse, causal={causal})")
+        perm = rng.permutation(len(parts_o))
+        o2, l2 = orc.merge_lse(po[perm], pl[perm])
+        _close(o2, o, 1e-13, "merge is independent of the order of the parts (o)")
+        _close(l2, lse, 1e-13, "merge is independent of the order of the parts (lse)")
+    x = rng.standard_normal((1, 4, 2, 8))
+    lx = rng.standard_normal((1, 2, 4)) * 3
+    o, lse = orc.merge_lse(x, lx)
+    _close(o, x[0], 0, "one part is the identity (o)")
+    _close(lse, lx[0], 0, "one part is the identity (lse)")
+    o, lse = orc.merge_lse(np.stack([x[0], x[0]]), np.stack([lx[0], lx[0]]))
+    _close(o, x[0], 1e-15, "two equal parts keep o")
+    _close(lse, lx[0] + np.log(2.0), 1e-14, "two equal parts add ln 2 to lse")
+    big = np.stack([np.full((2, 4), 1.0e4), np.full((2, 4), 1.0e4 - 1.0)])
+    y = rng.standard_normal((2, 4, 2, 8))
+    o, lse = orc.merge_lse(y, big)
+    w1 = 1.0 / (1.0 + np.exp(-1.0))
+    _close(lse, np.full((2, 4), 1.0e4 + np.log1p(np.exp(-1.0))), 1e-11, "lse of order 1e4 merges without overflow")
+    _close(o, w1 * y[0] + (1 - w1) * y[1], 1e-11, "lse of order 1e4 (one ulp of lse is 2e-12): weights 1/(1+e^-1) and e^-1/(1+e^-1)")
+    empty = np.full((3, 2, 4), -np.inf)
+    o, lse = orc.merge_lse(rng.standard_normal((3, 4, 2, 8)), empty)
+    assert np.all(o == 0) and np.all(np.isneginf(lse)), "rows with no key in any part: o = 0, lse = -inf"
+
+
 def pin_golden(orc):
     for name in ("two_token_causal.json", "three_token_window2.json"):
         g = json.load(open(os.path.join(GOLDEN, name)))
@@ -395,4 +453,4 @@ def pin_sampled_rows(orc):
 
 
 ALL_PINS = [pin_golden, pin_torch_forward, pin_torch_backward, pin_finite_differences, pin_closed_forms,
-            pin_invariants, pin_varlen, pin_paged, pin_prefill_paged, pin_sampled_rows]
+            pin_invariants, pin_varlen, pin_paged, pin_prefill_paged, pin_merge_lse, pin_sampled_rows]

@@ -20,6 +20,8 @@ MUTANTS = {
     6: "ds used in place of p for dV",
     7: "causal diagonal excluded",
     8: "V used in place of K for dQ",
+    9: "merge weights with the sign of the exponent flipped",
+    10: "merge without the largest lse factored out",
 }
 
 
