@@ -284,6 +284,25 @@ def pin_paged(orc):
     o2, l2 = orc.decode_paged(pp.q, kc2, vc2, bt2, pp.seq_lens, pp.scale)
     _close(o2, o, 0, "page relabelling (o)")
     _close(l2, lse, 0, "page relabelling (lse)")
+    # a sliding window: the query at position L-1 sees keys max(0, L-W) .. L-1 (torch fp64 attention
+    # over exactly those keys); windows of 1, inside a page, a whole page, across pages, beyond L
+    for D in (32, 256):
+        pw = synth.paged_from_lengths([1, 16, 17, 40, 33, 100], 4, 2, D, page_size=16, num_pages=64, seed=16 + D,
+                                      max_pages=7)
+        for W in (1, 7, 16, 17, 50):
+            ow, lw = orc.decode_paged(pw.q, pw.k_cache, pw.v_cache, pw.block_table, pw.seq_lens, pw.scale, W)
+            for b in range(pw.B):
+                L = int(pw.seq_lens[b])
+                tok = np.arange(max(0, L - W), L)
+                pages = pw.block_table[b, tok // 16]
+                kt = torch.tensor(_f(pw.k_cache[pages, tok % 16])).permute(1, 0, 2)[None]  # 1, Hkv, n, D
+                vt = torch.tensor(_f(pw.v_cache[pages, tok % 16])).permute(1, 0, 2)[None]
+                qt = torch.tensor(_f(pw.q[b]))[None, :, None, :]  # 1, Hq, 1, D
+                to = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=pw.scale, enable_gqa=True)
+                G = pw.Hq // pw.Hkv
+                tl = torch.logsumexp((qt @ kt.repeat_interleave(G, dim=1).transpose(-1, -2)) * pw.scale, dim=-1)
+                _close(ow[b], to[0, :, 0].numpy(), 1e-12, f"windowed decode o vs torch (W={W}, D={D})")
+                _close(lw[b], tl[0, :, 0].numpy(), 1e-12, f"windowed decode lse vs torch (W={W}, D={D})")
     # an empty request gives o = 0 and lse = -inf, never NaN
     pe = synth.paged_from_lengths([0, 3], 4, 1, 16, page_size=16, num_pages=4, seed=15, max_pages=1)
     o3, l3 = orc.decode_paged(pe.q, pe.k_cache, pe.v_cache, pe.block_table, pe.seq_lens, pe.scale)
