@@ -16,6 +16,7 @@ Entry points (same names as the C ABI):
 * ``attn_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q_len, ...)``
   chunked prefill over a paged cache: packed new tokens [T,Hq,D] -> (o, lse[Hq,T])
 * ``attn_bwd(q, k, v, o, lse, dO, ...)``  -> (dQ, dK, dV); dense or packed (cu_seqlens)
+* ``attn_merge_lse(o_parts, lse_parts, ...)`` attention results over disjoint key sets -> (o, lse)
 * ``attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, ...)`` -> (o, lse[B,Hq])
 * ``attn_workspace_size``, ``attn_get_device_status``, ``attn_status_string``
 * ``attn_selftest_wait_timeout`` (exercises the bounded-wait failure reporting)
@@ -31,7 +32,7 @@ __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_varlen", "attn_fwd_paged", "attn_bwd", "attn_decode_paged", "attn_workspace_size",
     "attn_get_device_status", "attn_status_string", "library_path", "load_library",
     "attn_launch_count", "attn_profile_start", "attn_profile_stop", "attn_decode_paged_noalloc",
-    "attn_selftest_wait_timeout",
+    "attn_selftest_wait_timeout", "attn_merge_lse",
     "ATTN_OP_FWD", "ATTN_OP_FWD_VARLEN", "ATTN_OP_BWD", "ATTN_OP_BWD_VARLEN", "ATTN_OP_DECODE_PAGED",
 ]
 
@@ -70,8 +71,10 @@ def load_library():
         lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P, Z, P]
         lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, I, P, Z, P]
         lib.attn_fwd_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, I, I, P]
+        lib.attn_merge_lse.argtypes = [P, P, P, P, I, I, I, I, I, P]
+        lib.attn_merge_lse.restype = I
         lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, I, I, P, I, I, P, Z, P]
-        lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, Z, P]
+        lib.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P, Z, P]
         lib.attn_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
         lib.attn_workspace_size.restype = Z
         lib.attn_get_device_status.argtypes = [P]
@@ -79,7 +82,7 @@ def load_library():
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_version.restype = I
-        lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.attn_decode_paged_noalloc.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
         lib.attn_decode_paged_noalloc.restype = I
         lib.attn_decode_paged_noalloc_max_bytes.restype = Z
         lib.attn_launch_count.restype = ctypes.c_ulonglong
@@ -165,6 +168,7 @@ def _ptr(t):
 
 
 _ws_cache: dict = {}
+_decode_layout: dict = {}  # device -> shape of the last decode call on the cached workspace
 
 
 def _workspace(nbytes: int, device, zero: bool, key: str):
@@ -242,6 +246,32 @@ def attn_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q_len: 
     return o, lse
 
 
+def attn_merge_lse(o_parts, lse_parts, o=None, lse=None, *, stream=None):
+    """Combine results over disjoint key sets: o_parts [P,B,S,H,D] (or [P,T,H,D]) bf16, lse_parts
+    [P,B,H,S] (or [P,H,T]) fp32 -> (o, lse) in the forward's layouts. o / lse may be o_parts[0] /
+    lse_parts[0] (in-place running merge)."""
+    import torch
+
+    packed = o_parts.dim() == 4
+    if packed:
+        P, S, H, D = o_parts.shape
+        B = 1
+    else:
+        P, B, S, H, D = o_parts.shape
+    if lse_parts.dtype != torch.float32 or not lse_parts.is_cuda or not lse_parts.is_contiguous():
+        raise ValueError("lse_parts must be a contiguous float32 CUDA tensor")
+    if tuple(lse_parts.shape) != ((P, H, S) if packed else (P, B, H, S)):
+        raise ValueError("lse_parts shape does not match o_parts")
+    if o is None:
+        o = torch.empty(o_parts.shape[1:], dtype=torch.bfloat16, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    rc = load_library().attn_merge_lse(_bf16(o_parts, "o_parts"), _ptr(lse_parts), _bf16(o, "o"), _ptr(lse), P, B,
+                                       S, H, D, _stream_ptr(stream, o_parts.device))
+    _check(rc, "attn_merge_lse")
+    return o, lse
+
+
 def attn_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, causal: bool = True, window: int = 0,
              scale: float | None = None, cu_seqlens=None, max_seqlen: int = 0, workspace=None, stream=None):
     """Gradients (dQ, dK, dV). Dense [B,S,H,D] when cu_seqlens is None, else packed [T,H,D]."""
@@ -272,8 +302,9 @@ def attn_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, causal: bool = T
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=None, *, scale: float | None = None,
-                      workspace=None, stream=None):
-    """Single-token decode: q [B,Hq,D], caches [pages,16,Hkv,D], block_table int32 [B,max_pages], seq_lens int32 [B]."""
+                      window: int = 0, workspace=None, stream=None):
+    """Single-token decode: q [B,Hq,D], caches [pages,16,Hkv,D], block_table int32 [B,max_pages], seq_lens int32 [B];
+    window > 0: the query sees only the last `window` keys."""
     import torch
 
     B, Hq, D = q.shape
@@ -289,16 +320,23 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=No
     need = attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D)
     if workspace is None:
         workspace = _workspace(need, q.device, True, "decode")
+        # the arrival counters sit at the start and their extent depends on the shape: when the
+        # shape changes, the region may hold the previous call's partials, so clear it
+        key = (str(q.device), B, Hq, Hkv, D)
+        if _decode_layout.get(str(q.device)) != key:
+            workspace[:min(workspace.numel(), 4 * B * Hkv + 256)].zero_()
+            _decode_layout[str(q.device)] = key
     rc = load_library().attn_decode_paged(_bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
                                           _ptr(block_table), _ptr(seq_lens), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D,
-                                          page_size, block_table.shape[1], num_pages, scale, _ptr(workspace),
+                                          page_size, block_table.shape[1], num_pages, scale, int(window),
+                                          _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device))
     _check(rc, "attn_decode_paged")
     return o, lse
 
 
 def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse, *, scale: float | None = None,
-                              stream=None):
+                              window: int = 0, stream=None):
     """attn_decode_paged without a workspace: the library's built-in scratch buffer is used.
 
     For callers that cannot allocate device memory on their decode path, so the outputs
@@ -315,7 +353,7 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse
             raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
     rc = load_library().attn_decode_paged_noalloc(
         _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
-        _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, scale,
+        _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, scale, int(window),
         _stream_ptr(stream, q.device))
     _check(rc, "attn_decode_paged_noalloc")
     return o, lse

@@ -143,9 +143,27 @@ size_t bwd_ws(long long rows, int Hq, int D) {
     return align256((size_t)rows * Hq * D * 4) + align256((size_t)rows * Hq * 4);
 }
 
-size_t decode_ws(int B, int Hq, int D) {
-    return align256((size_t)B * 4) +
-           align256((size_t)(B + attn::decode_max_grid()) * 2 * Hq * attn::decode_row_floats() * 4);
+// CTAs per KV-head block of a decode launch at most: the blocks share decode_max_grid() CTAs.
+int decode_grid_cap(int nhb) { return attn::decode_max_grid() / nhb > 1 ? attn::decode_max_grid() / nhb : 1; }
+
+// Decode workspace: per-(request, head block) arrival counters, then the split partials (slot
+// (b + k) * 2 + half for CTA k of a head block, every head block writing only its own heads).
+size_t decode_ws(int B, int Hq, int Hkv, int D) {
+    const int nhb = Hkv > 0 && D > 0 && Hq > 0 ? Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv) : 1;
+    return align256((size_t)B * nhb * 4) +
+           align256((size_t)(B + decode_grid_cap(nhb)) * 2 * Hq * attn::decode_row_floats(D > 0 ? D : 0) * 4);
+}
+
+// 3-D map over a paged cache [num_pages * 16 tokens, heads, dim]: box = dim x hb heads x 16 tokens,
+// no swizzle, so one box lands as the [16][hb][dim] block the decode kernel reads.
+bool make_decode_map(CUtensorMap* m, const void* base, int D, int H, int num_pages, int hb) {
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)num_pages * 16};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)hb, 16};
+    cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 int fwd_common(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
@@ -285,7 +303,7 @@ size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D, int num
         case ATTN_OP_FWD_VARLEN: return 0;
         case ATTN_OP_BWD:
         case ATTN_OP_BWD_VARLEN: return bwd_ws((long long)B * S, Hq, D);
-        case ATTN_OP_DECODE_PAGED: return decode_ws(B, Hq, D);
+        case ATTN_OP_DECODE_PAGED: return decode_ws(B, Hq, Hkv, D);
         default: return 0;
     }
 }
@@ -396,36 +414,62 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
 
 int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                       const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
-                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale, int window,
                       void* workspace, size_t workspace_bytes, void* stream) {
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse) return ATTN_ERR_INVALID_ARG;
-    if (B < 0 || max_pages_per_seq < 0 || num_pages < 0 || page_size <= 0) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || max_pages_per_seq < 0 || num_pages < 0 || page_size <= 0 || window < 0) return ATTN_ERR_INVALID_ARG;
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (D != 128 || page_size != 16 || Hkv > 8 || (G != 1 && G != 2 && G != 4 && G != 8) || B > 4096 ||
-        num_pages > (1 << 26))
+    const bool groups_ok = D == 128 ? (G == 1 || G == 2 || G == 4 || G == 8) : (G == 1 || G == 2 || G == 4);
+    if ((D != 128 && D != 256) || !groups_ok || page_size != 16 || Hkv > 256 || B > 4096 || num_pages > (1 << 26))
         return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
         (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return ATTN_ERR_MISALIGNED;
     if (B == 0) return ATTN_OK;
-    if (!workspace || workspace_bytes < decode_ws(B, Hq, D)) return ATTN_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < decode_ws(B, Hq, Hkv, D)) return ATTN_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return ATTN_ERR_MISALIGNED;
     const DeviceInfo* dev = device_info();
     if (!dev) return ATTN_ERR_NO_DEVICE;
     attn::DecodeLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const int hb = attn::decode_heads_per_unit(Hkv, D, G), nhb = Hkv / hb;
+    if (nhb > 1 && (!make_decode_map(&L.tk, k_cache, D, Hkv, num_pages, hb) ||
+                    !make_decode_map(&L.tv, v_cache, D, Hkv, num_pages, hb)))
+        return ATTN_ERR_LAUNCH;
     L.q = q, L.k_cache = k_cache, L.v_cache = v_cache, L.block_table = block_table, L.seq_lens = seq_lens;
     L.o = o, L.lse = lse, L.status = dev->status;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     L.counters = reinterpret_cast<int32_t*>(ws);
-    L.part = reinterpret_cast<float*>(ws + align256((size_t)B * 4));
-    L.B = B, L.Hq = Hq, L.Hkv = Hkv, L.max_pages = max_pages_per_seq, L.num_pages = num_pages, L.scale = scale;
+    L.part = reinterpret_cast<float*>(ws + align256((size_t)B * nhb * 4));
+    L.B = B, L.Hq = Hq, L.Hkv = Hkv, L.D = D, L.max_pages = max_pages_per_seq, L.num_pages = num_pages;
+    L.scale = scale, L.window = window;
+    // the head blocks share the SMs: each block's pages are split over sms / nhb CTAs
     long long units = (long long)B * (max_pages_per_seq > 0 ? max_pages_per_seq : 1);
-    int grid = dev->sms < attn::decode_max_grid() ? dev->sms : attn::decode_max_grid();
+    int grid = dev->sms / nhb;
+    if (grid > decode_grid_cap(nhb)) grid = decode_grid_cap(nhb);
     if (units < grid) grid = (int)units;
     L.grid = grid < 1 ? 1 : grid;
     return attn::launch_decode_paged(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
+}
+
+int attn_merge_lse(const attn_bf16* o_parts, const float* lse_parts, attn_bf16* o, float* lse, int num_parts, int B,
+                   int S, int H, int D, void* stream) {
+    if (num_parts < 1 || B < 0 || S < 0 || H < 1) return ATTN_ERR_INVALID_ARG;
+    if ((D != 64 && D != 128 && D != 256 && D != 512) || num_parts > 64) return ATTN_ERR_UNSUPPORTED;
+    const long long rows = (long long)B * S * H;
+    if (rows == 0) return ATTN_OK;
+    if (!o_parts || !lse_parts || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (!aligned16(o_parts) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse_parts) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return ATTN_ERR_MISALIGNED;
+    const DeviceInfo* dev = device_info();
+    if (!dev) return ATTN_ERR_NO_DEVICE;
+    attn::MergeLaunch L;
+    L.o_parts = o_parts, L.lse_parts = lse_parts, L.o = o, L.lse = lse;
+    L.P = num_parts, L.B = B, L.S = S, L.H = H, L.D = D, L.sms = dev->sms;
+    return attn::launch_merge_lse(L, static_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK : ATTN_ERR_LAUNCH;
 }
 
 int attn_selftest_wait_timeout(int limit_ms, void* stream) {

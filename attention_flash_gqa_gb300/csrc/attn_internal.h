@@ -18,20 +18,24 @@ ProfMark prof_begin(cudaStream_t stream, const char* kernel);
 void prof_end(cudaStream_t stream, ProfMark m);
 
 // ---- paged decode -----------------------------------------------------------------------
+// tk / tv: 3-D maps over the caches (D, Hkv, num_pages * 16) with a D x hb x 16 box, no swizzle;
+// used only when the KV heads are split into several blocks (hb < Hkv).
 struct DecodeLaunch {
+    CUtensorMap tk, tv;
     const uint16_t *q, *k_cache, *v_cache;
     const int32_t *block_table, *seq_lens;
     uint16_t* o;
     float* lse;
     float* part;
-    int32_t* counters;
+    int32_t* counters;  // [B][Hkv / hb]
     unsigned* status;
-    int B, Hq, Hkv, max_pages, num_pages, grid;
+    int B, Hq, Hkv, D, max_pages, num_pages, grid, window;
     float scale;
 };
-size_t decode_smem_bytes(int Hkv);
+size_t decode_smem_bytes(int hb, int D);
 int decode_max_grid();
-int decode_row_floats();  // floats per (slot, head) partial row
+int decode_row_floats(int D);              // floats per (slot, head) partial row
+int decode_heads_per_unit(int Hkv, int D, int G);  // hb: KV heads per unit (divides Hkv)
 cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream);
 
 // ---- prefill forward ---------------------------------------------------------------------
@@ -75,5 +79,16 @@ struct BwdLaunch {
     float scale;
 };
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+
+// ---- merge of attention results over disjoint key sets -----------------------------------
+struct MergeLaunch {
+    const uint16_t* o_parts;  // [P, B, S, H, D] bf16
+    const float* lse_parts;   // [P, B, H, S]
+    uint16_t* o;              // [B, S, H, D]
+    float* lse;               // [B, H, S]
+    int P, B, S, H, D;        // D in {64, 128, 256, 512}
+    int sms;
+};
+cudaError_t launch_merge_lse(const MergeLaunch& L, cudaStream_t stream);
 
 }  // namespace attn

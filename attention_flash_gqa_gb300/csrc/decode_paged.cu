@@ -1,22 +1,32 @@
-// Single-token decode over a paged KV cache (D = 128, page = 16 tokens).
+// Single-token decode over a paged KV cache (D = 128 or 256, page = 16 tokens), optionally
+// restricted to a sliding window.
 //
 // Source: "flex_attention + paged KV + CUDA graphs vs vLLM", sections "What each
 // option did" (page-table indirection per block, contiguous blocks, more warps) and
 // "Architecture notes" (PagedKVCache + PageTable); "What broke correctness" (a row
-// whose mask has no allowed key must not produce NaN).
+// whose mask has no allowed key must not produce NaN). The window: the head_dim 256
+// sliding-window layers of "Gemma4 FFPA attention backend support ..." (opening summary)
+// at inference, the query at position L-1 seeing keys max(0, L-W) .. L-1.
 //
-// Design (memory bound: every cached K/V byte is read exactly once):
-//  * A page holds 16 tokens x Hkv heads x 128 dims, contiguous, so one page of K and
-//    one of V are fetched with two untiled TMA bulk copies into a 3-stage ring.
+// Design (memory bound: every cached K/V byte in the window is read exactly once):
+//  * A unit is one page (16 tokens) of a block of hb KV heads, 32 KB of K and 32 KB of V
+//    at most (hb = 8 heads at D = 128, 4 at D = 256). When the block is every head the
+//    page is contiguous and K and V are fetched with two untiled TMA bulk copies; otherwise
+//    with two 3-D tensor copies (16 tokens x hb heads x D) into a 3-stage ring. KV-head
+//    blocks are the grid's y dimension; each block runs the scheme below on its heads.
+//  * With a window only the pages that hold keys of the window are units; tokens of the
+//    window's first page below L-W are masked like the slots past L in the last page.
 //  * Work is balanced by pages, not by requests: the pages of all requests are laid
 //    end to end and CTA k takes the k-th equal share. A CTA may cover the tail of one
 //    request and the head of the next.
-//  * 16 consumer warps, two per KV head: each serves all query heads of the head's GQA
-//    group (one K/V row read feeds all of them) on one half of the page's 16 tokens, with
-//    its own running softmax state. For GQA groups up to 4 each half-warp takes 4 of the
-//    warp's tokens with 8 dims per lane and paired fp32 FMAs; for a group of 8, lane l owns
-//    dims 4l..4l+3 of all 8. Per-token dot products are finished by a butterfly
-//    reduce-scatter across the lanes that split a token.
+//  * Consumer warps serve one KV head each (two per head on the two halves of the page's
+//    tokens when a warp's registers cannot hold the whole head): each serves all query heads
+//    of the head's GQA group (one K/V row read feeds all of them) with its own running
+//    softmax state. D = 128 with GQA groups up to 4: one warp per head, each half-warp takes
+//    8 of the page's tokens with 8 dims per lane and paired fp32 FMAs. D = 128 with a group
+//    of 8: two warps per head, lane l owns dims 4l..4l+3 of the warp's 8 tokens. D = 256:
+//    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
+//    a butterfly reduce-scatter across the lanes that split a token.
 //  * fp32 online softmax in the log2 domain. Every (CTA, token half) touching a request
 //    leaves unnormalised partials (o, m, l) in the workspace; the last CTA to finish that
 //    request (arrival counter) merges them and resets the counter to zero.
@@ -28,24 +38,32 @@
 namespace attn {
 namespace {
 
-constexpr int kD = 128;
 constexpr int kPage = 16;
 constexpr int kStages = 3;
 constexpr int kMaxConsumerWarps = 16;
-// GQA groups up to 4 use one consumer warp per KV head (8 warps: fewer warps per scheduler,
-// so each thread can hold its 8 query dims and 8 output dims per head in registers); a group
-// of 8 uses two warps per head.
-template <int G>
+constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tokens x hb heads x D
+// D = 128 with GQA groups up to 4 uses one consumer warp per KV head (8 warps: fewer warps per
+// scheduler, so each thread can hold its 8 query dims and 8 output dims per head in
+// registers); a group of 8, and D = 256, use two warps per head. Every configuration runs 8
+// consumer warps.
+template <int G, int D>
 struct DecCfg {
-    static constexpr bool PACKED = G <= 4;
-    static constexpr int CW = PACKED ? 8 : 16;     // consumer warps
-    static constexpr int WPH = PACKED ? 1 : 2;     // consumer warps per KV head
-    static constexpr int TPW = 16 / WPH;           // page tokens per warp
-    static constexpr int kThreads = (CW + 1) * 32;  // + one producer warp
+    static constexpr bool PACKED = D == 128 && G <= 4;
+    static constexpr int QD = D == 128 && !PACKED ? 4 : 8;  // dims per lane
+    static constexpr int NL = PACKED ? 16 : 32;            // lanes that split one token's dims
+    static constexpr int WPH = PACKED ? 1 : 2;             // consumer warps per KV head
+    // KV heads per unit at most: 32 KB of K per stage, and for a group of 8 at D = 128 half of
+    // that, so 8 consumer warps (168 registers each) cover the unit without spilling
+    static constexpr int HB = (D == 128 && G == 8) ? 4 : kUnitBytes / (kPage * D * 2);
+    static constexpr int CW = WPH * HB;                    // consumer warps
+    static constexpr int TPW = 16 / WPH;                   // page tokens per warp
+    static constexpr int kThreads = (CW + 1) * 32;         // + one producer warp
+    static constexpr int kRowF = D + 4;  // partial row: o[D], m, l, 2 pad floats (float4 alignment)
+    static_assert(QD * NL == D, "lanes x dims per lane must cover the head");
+    static_assert(CW <= kMaxConsumerWarps, "consumer warps");
 };
 constexpr int kMaxB = 4096;
-constexpr int kRowF = kD + 4;
-constexpr int kMaxUnits = 2048;  // page-table entries of a CTA's range staged in shared memory  // partial row: o[kD], m, l, 2 pad floats (keeps float4 alignment)
+constexpr int kMaxUnits = 2048;  // page-table entries of a CTA's range staged in shared memory
 
 struct DecodeArgs {
     const uint16_t* q;
@@ -55,17 +73,19 @@ struct DecodeArgs {
     const int32_t* seq_lens;
     uint16_t* o;
     float* lse;
-    float* part;       // [(B + grid) * 2 slots][Hq][kRowF]
-    int32_t* counters; // [B]
+    float* part;       // [(B + grid) * 2 slots][Hq][D + 4]
+    int32_t* counters; // [B][nhb]
     unsigned* status;
     int B, Hq, Hkv, max_pages, num_pages;
+    int window;        // <= 0: none
+    int hb, nhb;       // KV heads per unit, head blocks (hb * nhb = Hkv)
     float scale_log2;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Clamped page count of request b (records a bounds fault for lengths beyond the table).
+// Clamped length of request b (records a bounds fault for lengths beyond the table).
 __device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
     int L = a.seq_lens[b];
     int cap = a.max_pages * kPage;
@@ -76,20 +96,35 @@ __device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
     return L;
 }
 
+// First token the query of a request of length L sees (the window's start).
+__device__ __forceinline__ int first_token(const DecodeArgs& a, int L) {
+    return a.window > 0 && L > a.window ? L - a.window : 0;
+}
+
+// Units (pages holding keys the query sees) of a request of length L.
+__device__ __forceinline__ int req_units(const DecodeArgs& a, int L) {
+    return L > 0 ? (L - 1) / kPage - first_token(a, L) / kPage + 1 : 0;
+}
+
 // CTA that owns global page unit u when P units are split evenly over G CTAs
 // (CTA k owns [floor(kP/G), floor((k+1)P/G))).
 __device__ __forceinline__ int owner_of(long long u, long long P, int G) {
     return (int)(((u + 1) * (long long)G - 1) / P);
 }
 
-template <int G>
-__global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(DecodeArgs a) {
-    using DC = DecCfg<G>;
+template <int G, int D>
+__global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
+    decode_paged_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, DecodeArgs a) {
+    using DC = DecCfg<G, D>;
     constexpr int kThreads = DC::kThreads;
     constexpr int kConsumerWarps = DC::CW;
+    constexpr int kRowF = DC::kRowF;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int page_bytes = kPage * a.Hkv * kD * 2;
+    const int hbk = blockIdx.y;         // head block
+    const int g0 = hbk * a.hb;          // its first KV head
+    const int h0 = g0 * G, h1 = (g0 + a.hb) * G;  // its query heads
+    const int page_bytes = kPage * a.hb * D * 2;
     uint8_t* stage_base = smem;  // kStages x (K page, V page)
     int32_t* start = reinterpret_cast<int32_t*>(smem + kStages * 2 * page_bytes);  // [B + 1]
     float* scratch = reinterpret_cast<float*>(start + kMaxB + 8);                  // per warp: sc[8G], sp[8G]
@@ -120,7 +155,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
         if (tid < 256) {
             for (int i = 0; i < per; ++i) {
                 int b = tid * per + i;
-                if (b < B) local += (req_len(a, b) + kPage - 1) / kPage;
+                if (b < B) local += req_units(a, req_len(a, b));
             }
         }
         // inclusive scan of `local` over threads 0..255
@@ -141,7 +176,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                 int b = tid * per + i;
                 if (b < B) {
                     start[b] = acc;
-                    acc += (req_len(a, b) + kPage - 1) / kPage;
+                    acc += req_units(a, req_len(a, b));
                 }
             }
             if (tid == 255) start[B] = acc;
@@ -154,14 +189,15 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
     const int Gc = (int)(P < (long long)gridDim.x ? P : (long long)gridDim.x);
     const int k = blockIdx.x;
 
-    // Requests with no cached token: o = 0, lse = -inf (CTA 0 writes them).
+    // Requests with no cached token: o = 0, lse = -inf (CTA 0 of each head block writes its heads).
     if (k == 0) {
-        for (int idx = tid; idx < B * a.Hq; idx += kThreads) {
-            int b = idx / a.Hq;
+        const int nh = h1 - h0;
+        for (int idx = tid; idx < B * nh; idx += kThreads) {
+            const int b = idx / nh, h = h0 + idx % nh;
             if (start[b + 1] == start[b]) {
-                a.lse[idx] = -INFINITY;
-                uint16_t* orow = a.o + (size_t)idx * kD;
-                for (int d = 0; d < kD; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
+                a.lse[(size_t)b * a.Hq + h] = -INFINITY;
+                uint16_t* orow = a.o + ((size_t)b * a.Hq + h) * D;
+                for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
             }
         }
     }
@@ -194,13 +230,14 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
             if (start[mid] <= u) lo = mid;
             else hi = mid - 1;
         }
-        const int p = (int)(u - start[lo]);
+        const int L = req_len(a, lo);
+        const int p = (int)(u - start[lo]) + first_token(a, L) / kPage;  // page index in the request
         const int page = a.block_table[(size_t)lo * a.max_pages + p];
         if (page < 0 || page >= a.num_pages) {
             atomicOr(a.status, DEVSTAT_BOUNDS);
             return -1;
         }
-        const int nt = min(kPage, req_len(a, lo) - p * kPage);
+        const int nt = min(kPage, L - p * kPage);
         return (page << 5) | nt;
     };
     // The producer warp stages the first units itself and issues their pages at once, so
@@ -211,9 +248,15 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
         const uint32_t fb = smem_u32(&full[s]);
         if (entry >= 0) {
             mbar_expect_tx(fb, 2u * page_bytes);
-            const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * kD;
-            bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes), a.kc + off, page_bytes, fb);
-            bulk_load(smem_u32(stage_base + (size_t)s * 2 * page_bytes + page_bytes), a.vc + off, page_bytes, fb);
+            const uint32_t dk = smem_u32(stage_base + (size_t)s * 2 * page_bytes), dv = dk + page_bytes;
+            if (a.nhb == 1) {  // every head: the page is contiguous
+                const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * D;
+                bulk_load(dk, a.kc + off, page_bytes, fb);
+                bulk_load(dv, a.vc + off, page_bytes, fb);
+            } else {  // 16 tokens x hb heads x D of the page
+                tma_load_3d(dk, &tk, fb, 0, g0, (entry >> 5) * kPage);
+                tma_load_3d(dv, &tv, fb, 0, g0, (entry >> 5) * kPage);
+            }
         } else {
             mbar_arrive(fb);
         }
@@ -260,13 +303,14 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
     //    warp's 8 tokens (32-lane butterfly).
     constexpr bool PACKED = DC::PACKED;
     constexpr int TPW = DC::TPW;
-    const int g = warp / DC::WPH, half = warp % DC::WPH;
-    const bool active = g < a.Hkv;
+    const int gl = warp / DC::WPH, half = warp % DC::WPH;  // KV head within the block, token half
+    const int g = g0 + gl;                                  // KV head
+    const bool active = gl < a.hb;
     float* sc = scratch + warp * 2 * TPW * G;  // [TPW * G] scores (log2 domain), index token * G + head
     float* sp = sc + TPW * G;                  // [TPW * G] probabilities
-    constexpr int QD = PACKED ? 8 : 4;    // dims per lane
+    constexpr int QD = DC::QD;            // dims per lane
     constexpr int NT = 8;                 // tokens per lane group (half-warp when packed)
-    constexpr int NL = PACKED ? 16 : 32;  // lanes that split one token's dims
+    constexpr int NL = DC::NL;            // lanes that split one token's dims
     constexpr int NV = TPW * G;           // (token, head) values of the warp's tokens
     constexpr int NVL = NT * G;           // partial values per lane
     constexpr int NF = NVL >= NL ? NVL / NL : 1;  // finished values per lane after the butterfly
@@ -289,15 +333,17 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
     int i = 0;
     bool ok = true;
     int cur_b = -1;
+    int lo_tok = 0;  // first visible token within the request's first unit (window)
     for (long long u = u0; u < u1 && ok; ++u, ++i) {
         while (start[b + 1] <= u) ++b;
         if (b != cur_b) {
             cur_b = b;
+            lo_tok = first_token(a, req_len(a, b)) % kPage;
             if (active) {
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
-                    const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + hh) * kD + dim0;
-                    if constexpr (PACKED) {
+                    const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + hh) * D + dim0;
+                    if constexpr (QD == 8) {
                         const uint4 w = *reinterpret_cast<const uint4*>(qrow);
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -313,16 +359,17 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
         ok = mbar_wait(smem_u32(&full[s]), r & 1, abort_flag, a.status, 0x32);
         if (!ok) break;
         const int32_t entry = unit_entry(i);
-        const int nt = (entry >= 0 ? (entry & 31) : 0) - TPW * half;  // valid tokens of this warp's (may be <= 0)
-        if (active && nt > 0) {
+        const int nt = (entry >= 0 ? (entry & 31) : 0) - TPW * half;  // end of this warp's valid tokens (may be <= 0)
+        const int tlo = (u == start[b] ? lo_tok : 0) - TPW * half;     // first of them (may be < 0)
+        if (active && nt > 0 && tlo < TPW) {
             const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes;
             const uint8_t* vp = kp + page_bytes;
             // partial scores over this lane's dims: v[t * G + hh] for its NT tokens
             float v[NVL];
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
-                const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.Hkv + g) * kD + dim0) * 2;
-                if constexpr (PACKED) {
+                const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2;
+                if constexpr (QD == 8) {
                     const uint4 w = *reinterpret_cast<const uint4*>(krow);
                     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                     float2 k2[4];
@@ -371,7 +418,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                 for (int j = 0; j < NF; ++j) {
                     const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
                     const int tw = NT * sub + idx / G;               // token within the warp's 8
-                    sc[tw * G + idx % G] = tw < nt ? v[j] * a.scale_log2 : -INFINITY;
+                    sc[tw * G + idx % G] = tw < nt && tw >= tlo ? v[j] * a.scale_log2 : -INFINITY;
                 }
             }
             __syncwarp();
@@ -413,9 +460,9 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     const int tw = NT * sub + t;
-                    const uint4 w = *reinterpret_cast<const uint4*>(vp + ((size_t)((tok0 + t) * a.Hkv + g) * kD + dim0) * 2);
+                    const uint4 w = *reinterpret_cast<const uint4*>(vp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2);
                     // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
-                    const bool valid = tw < nt;
+                    const bool valid = tw < nt && tw >= tlo;
                     const uint32_t ws[4] = {valid ? w.x : 0u, valid ? w.y : 0u, valid ? w.z : 0u, valid ? w.w : 0u};
                     float2 v2[4];
 #pragma unroll
@@ -440,13 +487,23 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                 }
             } else {
                 const int tmax = nt < 8 ? nt : 8;
-                for (int t = 0; t < tmax; ++t) {
-                    const uint2 w = *reinterpret_cast<const uint2*>(vp + ((size_t)((TPW * half + t) * a.Hkv + g) * kD + dim0) * 2);
-                    const float v0 = bf16_lo(w.x), v1 = bf16_hi(w.x), v2 = bf16_lo(w.y), v3 = bf16_hi(w.y);
+                for (int t = tlo > 0 ? tlo : 0; t < tmax; ++t) {  // only the warp's visible tokens
+                    const uint8_t* vrow = vp + ((size_t)((TPW * half + t) * a.hb + gl) * D + dim0) * 2;
+                    float vv[QD];
+                    if constexpr (QD == 8) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(vrow);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) vv[2 * e] = bf16_lo(ws[e]), vv[2 * e + 1] = bf16_hi(ws[e]);
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2*>(vrow);
+                        vv[0] = bf16_lo(w.x), vv[1] = bf16_hi(w.x), vv[2] = bf16_lo(w.y), vv[3] = bf16_hi(w.y);
+                    }
 #pragma unroll
                     for (int hh = 0; hh < G; ++hh) {
                         const float pt = sp[t * G + hh];
-                        acc_o[hh][0] += pt * v0, acc_o[hh][1] += pt * v1, acc_o[hh][2] += pt * v2, acc_o[hh][3] += pt * v3;
+#pragma unroll
+                        for (int e = 0; e < QD; ++e) acc_o[hh][e] = fmaf(pt, vv[e], acc_o[hh][e]);
                     }
                 }
             }
@@ -478,15 +535,15 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                                 make_float4(acc_o[hh][e], acc_o[hh][e + 1], acc_o[hh][e + 2], acc_o[hh][e + 3]);
                     }
                     if (lane == hh) {
-                        row[kD] = m_run;
-                        row[kD + 1] = l_run;
+                        row[D] = m_run;
+                        row[D + 1] = l_run;
                     }
                 }
             }
             __threadfence();
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             if (tid == 0) {
-                const int prev = atomicAdd(&a.counters[b], 1);
+                const int prev = atomicAdd(&a.counters[(size_t)b * a.nhb + hbk], 1);
                 *last_flag = prev == kl - kf;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
@@ -501,9 +558,9 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                 auto slot_row = [&](int q, int h) -> const float* {
                     return a.part + ((size_t)(b + kf + q / DC::WPH) * 2 + q % DC::WPH) * a.Hq * kRowF + (size_t)h * kRowF;
                 };
-                float* mM = scratch;          // [Hq] max over the slots
-                float* mI = scratch + a.Hq;   // [Hq] 1 / sum
-                for (int h = tid; h < a.Hq; h += kConsumerWarps * 32) {
+                float* mM = scratch;               // [h1 - h0] max over the slots
+                float* mI = scratch + (h1 - h0);   // [h1 - h0] 1 / sum
+                for (int h = h0 + tid; h < h1; h += kConsumerWarps * 32) {
                     float M = -INFINITY, Ls = 0.f;
                     for (int q0 = 0; q0 < nslots; q0 += 8) {  // 8 slots' loads in flight at once
                         float mk[8], lk[8];
@@ -512,7 +569,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                             mk[j] = -INFINITY, lk[j] = 0.f;
                             if (q0 + j < nslots) {
                                 const float* row = slot_row(q0 + j, h);
-                                mk[j] = __ldcg(row + kD), lk[j] = __ldcg(row + kD + 1);
+                                mk[j] = __ldcg(row + D), lk[j] = __ldcg(row + D + 1);
                             }
                         }
                         float Mc = M;
@@ -524,20 +581,20 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                         for (int j = 0; j < 8; ++j) Ls += mk[j] == -INFINITY ? 0.f : lk[j] * fast_exp2(mk[j] - Mc);
                         M = Mc;
                     }
-                    mM[h] = M;
-                    mI[h] = Ls > 0.f ? 1.f / Ls : 0.f;
+                    mM[h - h0] = M;
+                    mI[h - h0] = Ls > 0.f ? 1.f / Ls : 0.f;
                     a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
                 }
                 asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
                 constexpr int IPT = 4;
-                const int nitems = a.Hq * (kD / 4);
+                const int nitems = (h1 - h0) * (D / 4);
                 for (int base = tid; base < nitems; base += kConsumerWarps * 32 * IPT) {
                     float4 O[IPT];
                     int hI[IPT], dI[IPT];
 #pragma unroll
                     for (int k2 = 0; k2 < IPT; ++k2) {
                         const int idx = min(base + k2 * kConsumerWarps * 32, nitems - 1);
-                        hI[k2] = idx / (kD / 4), dI[k2] = idx % (kD / 4);
+                        hI[k2] = h0 + idx / (D / 4), dI[k2] = idx % (D / 4);
                         O[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                     for (int q0 = 0; q0 < nslots; q0 += 2) {  // loads of 2 slots x IPT items in flight
@@ -551,7 +608,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                                 ov[j][k2] = make_float4(0.f, 0.f, 0.f, 0.f);
                                 if (q0 + j < nslots) {
                                     const float* row = slot_row(q0 + j, hI[k2]);
-                                    mk[j][k2] = __ldcg(row + kD);
+                                    mk[j][k2] = __ldcg(row + D);
                                     ov[j][k2] = __ldcg(reinterpret_cast<const float4*>(row) + dI[k2]);
                                 }
                             }
@@ -559,7 +616,7 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
                         for (int j = 0; j < 2; ++j)
 #pragma unroll
                             for (int k2 = 0; k2 < IPT; ++k2) {
-                                const float wgt = mk[j][k2] == -INFINITY ? 0.f : fast_exp2(mk[j][k2] - mM[hI[k2]]);
+                                const float wgt = mk[j][k2] == -INFINITY ? 0.f : fast_exp2(mk[j][k2] - mM[hI[k2] - h0]);
                                 O[k2].x += wgt * ov[j][k2].x, O[k2].y += wgt * ov[j][k2].y;
                                 O[k2].z += wgt * ov[j][k2].z, O[k2].w += wgt * ov[j][k2].w;
                             }
@@ -567,14 +624,14 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
 #pragma unroll
                     for (int k2 = 0; k2 < IPT; ++k2) {
                         if (base + k2 * kConsumerWarps * 32 >= nitems) break;
-                        const float inv = mI[hI[k2]];
+                        const float inv = mI[hI[k2] - h0];
                         uint2 w;
                         w.x = pack_bf16x2(O[k2].x * inv, O[k2].y * inv);
                         w.y = pack_bf16x2(O[k2].z * inv, O[k2].w * inv);
-                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + hI[k2]) * kD + 4 * dI[k2]) = w;
+                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + hI[k2]) * D + 4 * dI[k2]) = w;
                     }
                 }
-                if (tid == 0) a.counters[b] = 0;
+                if (tid == 0) a.counters[(size_t)b * a.nhb + hbk] = 0;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             // reset the running state for the next request
@@ -589,37 +646,58 @@ __global__ void __launch_bounds__(DecCfg<G>::kThreads, 1) decode_paged_kernel(De
 
 }  // namespace
 
-size_t decode_smem_bytes(int Hkv) {
-    return 1024 + (size_t)kStages * 2 * kPage * Hkv * kD * 2 + (kMaxB + 8) * 4 + (size_t)kMaxConsumerWarps * 16 * 8 * 4 +
+size_t decode_smem_bytes(int hb, int D) {
+    return 1024 + (size_t)kStages * 2 * kPage * hb * D * 2 + (kMaxB + 8) * 4 + (size_t)kMaxConsumerWarps * 16 * 8 * 4 +
            256 + kMaxUnits * 4;
 }
 
 int decode_max_grid() { return 256; }
-int decode_row_floats() { return kRowF; }
+int decode_row_floats(int D) { return D + 4; }
+
+int decode_heads_per_unit(int Hkv, int D, int G) {
+    const int cap = (D == 128 && G == 8) ? 4 : kUnitBytes / (kPage * D * 2);
+    int hb = Hkv < cap ? Hkv : cap;
+    while (hb > 1 && Hkv % hb) --hb;
+    return hb;
+}
 
 cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     DecodeArgs a;
     a.q = L.q, a.kc = L.k_cache, a.vc = L.v_cache, a.block_table = L.block_table, a.seq_lens = L.seq_lens;
     a.o = L.o, a.lse = L.lse, a.part = L.part, a.counters = L.counters, a.status = L.status;
     a.B = L.B, a.Hq = L.Hq, a.Hkv = L.Hkv, a.max_pages = L.max_pages, a.num_pages = L.num_pages;
-    a.scale_log2 = L.scale * 1.4426950408889634f;
+    a.window = L.window;
     const int G = L.Hq / L.Hkv;
-    const size_t smem = decode_smem_bytes(L.Hkv);
+    a.hb = decode_heads_per_unit(L.Hkv, L.D, G);
+    a.nhb = L.Hkv / a.hb;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    const size_t smem = decode_smem_bytes(a.hb, L.D);
     auto go = [&](auto kern, int threads) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const ProfMark m = prof_begin(stream, "decode_paged");
-        kern<<<L.grid, threads, smem, stream>>>(a);
+        const ProfMark m = prof_begin(stream, L.D == 128 ? "decode_paged" : "decode_paged_d256");
+        kern<<<dim3(L.grid, a.nhb), threads, smem, stream>>>(L.tk, L.tv, a);
         prof_end(stream, m);
         return cudaGetLastError();
     };
-    switch (G) {
-        case 1: return go(decode_paged_kernel<1>, DecCfg<1>::kThreads);
-        case 2: return go(decode_paged_kernel<2>, DecCfg<2>::kThreads);
-        case 4: return go(decode_paged_kernel<4>, DecCfg<4>::kThreads);
-        case 8: return go(decode_paged_kernel<8>, DecCfg<8>::kThreads);
-        default: return cudaErrorInvalidValue;
+    if (L.D == 128) {
+        switch (G) {
+            case 1: return go(decode_paged_kernel<1, 128>, DecCfg<1, 128>::kThreads);
+            case 2: return go(decode_paged_kernel<2, 128>, DecCfg<2, 128>::kThreads);
+            case 4: return go(decode_paged_kernel<4, 128>, DecCfg<4, 128>::kThreads);
+            case 8: return go(decode_paged_kernel<8, 128>, DecCfg<8, 128>::kThreads);
+            default: return cudaErrorInvalidValue;
+        }
     }
+    if (L.D == 256) {
+        switch (G) {
+            case 1: return go(decode_paged_kernel<1, 256>, DecCfg<1, 256>::kThreads);
+            case 2: return go(decode_paged_kernel<2, 256>, DecCfg<2, 256>::kThreads);
+            case 4: return go(decode_paged_kernel<4, 256>, DecCfg<4, 256>::kThreads);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

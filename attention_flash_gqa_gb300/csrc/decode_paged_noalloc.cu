@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "attn_internal.h"
 
 namespace {
 
@@ -53,20 +54,22 @@ ATTN_API size_t attn_decode_paged_noalloc_max_bytes(void) { return kScratchBytes
 ATTN_API int attn_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                                        const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse,
                                        int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
-                                       int num_pages, float scale, void* stream) {
-    if (B < 0 || Hq <= 0) return ATTN_ERR_INVALID_ARG;
+                                       int num_pages, float scale, int window, void* stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     const size_t need = attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, 0, max_pages_per_seq);
     if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;  // beyond the built-in buffer
     if (B == 0) return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, D, page_size,
-                                         max_pages_per_seq, num_pages, scale, nullptr, 0, stream);
+                                         max_pages_per_seq, num_pages, scale, window, nullptr, 0, stream);
     void* scratch = scratch_for_current_device();
     if (!scratch) return ATTN_ERR_NO_DEVICE;
-    // The arrival counters at the start of the scratch must be zero when the kernel starts.
-    // The buffer keeps whatever the previous call left, so clear them on this stream.
-    if (cudaMemsetAsync(scratch, 0, align256((size_t)B * 4), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    // The arrival counters (one per request and KV-head block) at the start of the scratch must
+    // be zero when the kernel starts. The buffer keeps whatever the previous call left, so clear
+    // them on this stream.
+    const int nhb = Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv);
+    if (cudaMemsetAsync(scratch, 0, align256((size_t)B * nhb * 4), static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_LAUNCH;
     return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, D, page_size,
-                             max_pages_per_seq, num_pages, scale, scratch, kScratchBytes, stream);
+                             max_pages_per_seq, num_pages, scale, window, scratch, kScratchBytes, stream);
 }
 
 }  // extern "C"

@@ -51,7 +51,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # bwd_main_d512: captured at B=1 (half the workload, same per-cluster work) and doubled.
 KERNEL_SOURCES = {"bwd_main_d512": ["attn_bwd.cu", "ptx.cuh", "attn_internal.h"],
                   "fwd_d512": ["attn_fwd.cu", "ptx.cuh", "attn_internal.h"]}
-TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (2.443940e9 + 1.310306e9), "src": "d86f41fffc1bbd60"}}
+TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (3.059751e9 + 1.640225e9), "src": "eceadd8d728cb67e"}}
 
 
 def pairs_causal(S: int, W: int = 0) -> int:
@@ -370,7 +370,7 @@ def finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launch
 
 def bench_extra(args, attn, synth, peaks, peak_src, clocks):
     """Sliding-window d256 fwd+bwd, varlen d512 fwd+bwd, paged-cache chunked prefill d512 (forward),
-    paged decode (GB/s)."""
+    merge of results over disjoint key sets (GB/s), paged decode d128 and sliding-window d256 (GB/s)."""
     import numpy as np
     import torch
 
@@ -391,6 +391,23 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
         torch.cuda.synchronize()
         clocks.mark(t0, time.time())
         return ev0.elapsed_time(ev1) / n
+
+    def per_call_ms(fn, n, before=None):
+        """Device time of each of n calls, every call bracketed by its own event pair. All calls are
+        queued before the first is waited on, so the host's launch overhead overlaps the GPU's
+        work and never sits inside a bracket. `before` (e.g. an L2 flush) runs ahead of each
+        bracket."""
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        t0 = time.time()
+        for e0, e1 in pairs:
+            if before is not None:
+                before()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        clocks.mark(t0, time.time())
+        return [e0.elapsed_time(e1) for e0, e1 in pairs]
 
     def per_kernel(fn, n=3):  # a separate, profiled pass: average ms per launch of each kernel
         attn.attn_profile_start()
@@ -455,6 +472,24 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
         "l2": "inputs larger than L2 (q 134 MB, caches 2 x 84 MB)"}
     del qp, kcp, vcp, op, lp
 
+    # merge of results over disjoint key sets: one rank's combining step of an 8-way ring
+    mg = synth.merge_cp8_d512(seed=7)
+    mo = to_dev(mg.o_parts)
+    ml = torch.from_numpy(mg.lse_parts).cuda()
+    om = torch.empty(mo.shape[1:], dtype=torch.bfloat16, device="cuda")
+    lm = torch.empty(ml.shape[1:], dtype=torch.float32, device="cuda")
+    rows_m = mg.B * mg.S * mg.H
+    m_bytes = mg.P * rows_m * (mg.D * 2 + 4) + rows_m * (mg.D * 2 + 4)
+    mtimes = per_call_ms(lambda: attn.attn_merge_lse(mo, ml, om, lm), max(20, args.steps) + 3)[3:]
+    mmed = statistics.median(mtimes)
+    mgbs = m_bytes / (mmed * 1e-3) / 1e9
+    res["merge_lse_cp8_d512"] = {"value": mgbs, "unit": "GB/s", "us_per_call_median": mmed * 1e3,
+                                 "us_per_call_min": min(mtimes) * 1e3, "bytes_per_call": m_bytes,
+                                 "frac_of_hbm_peak": mgbs / peaks["hbm_gbs"], "peak_source": peak_src,
+                                 "parts": mg.P, "rows": rows_m, "D": mg.D,
+                                 "l2": "inputs larger than L2 (537 MB of parts)"}
+    del mo, ml, om, lm
+
     # paged decode: time the kernel alone, flushing L2 (write > L2) between calls
     pp = synth.decode_paged_d128(seed=7)
     qd, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
@@ -467,21 +502,38 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
     kv_bytes = int(sum(int(L) for L in pp.seq_lens)) * pp.Hkv * pp.D * 2 * 2
     io_bytes = pp.B * pp.Hq * pp.D * 2 * 2 + pp.B * pp.Hq * 4
-    times = []
-    for i in range(max(20, args.steps) + 3):
-        flush.fill_(i & 0xff)
-        ev0.record(stream)
-        attn.attn_decode_paged(qd, kc, vc, bt, sl, od, ld, scale=pp.scale, workspace=wsd)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        if i >= 3:
-            times.append(ev0.elapsed_time(ev1))
+    flush_l2 = lambda: flush.fill_(1)
+    times = per_call_ms(lambda: attn.attn_decode_paged(qd, kc, vc, bt, sl, od, ld, scale=pp.scale, workspace=wsd),
+                        max(20, args.steps) + 3, flush_l2)[3:]
     med = statistics.median(times)
     gbs = (kv_bytes + io_bytes) / (med * 1e-3) / 1e9
     res["decode_paged_d128"] = {"value": gbs, "unit": "GB/s", "us_per_call_median": med * 1e3,
                                 "us_per_call_min": min(times) * 1e3, "bytes_per_call": kv_bytes + io_bytes,
                                 "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
-                                "l2": "flushed (512 MB write) before every call"}
+                                "l2": "flushed (512 MB write) before every call",
+                                "timing": "per-call event pairs, all calls queued ahead (no host gap inside a bracket)"}
+    del qd, kc, vc, od, ld, wsd
+
+    # sliding-window decode at head_dim 256 (W = 1024): only the window's keys are read
+    ps = synth.decode_paged_swa_d256(seed=7)
+    qs, kcs, vcs = to_dev(ps.q), to_dev(ps.k_cache), to_dev(ps.v_cache)
+    bts = torch.from_numpy(ps.block_table).cuda()
+    sls = torch.from_numpy(ps.seq_lens).cuda()
+    os_ = torch.empty_like(qs)
+    ls = torch.empty((ps.B, ps.Hq), dtype=torch.float32, device="cuda")
+    wss = torch.zeros(attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, ps.B, ps.Hq, ps.Hkv, 0, ps.D),
+                      dtype=torch.uint8, device="cuda")
+    kv_s = int(sum(min(int(L), ps.window) for L in ps.seq_lens)) * ps.Hkv * ps.D * 2 * 2
+    io_s = ps.B * ps.Hq * ps.D * 2 * 2 + ps.B * ps.Hq * 4
+    times = per_call_ms(lambda: attn.attn_decode_paged(qs, kcs, vcs, bts, sls, os_, ls, scale=ps.scale,
+                                                       window=ps.window, workspace=wss),
+                        max(20, args.steps) + 3, flush_l2)[3:]
+    med = statistics.median(times)
+    gbs = (kv_s + io_s) / (med * 1e-3) / 1e9
+    res["decode_paged_swa_d256"] = {"value": gbs, "unit": "GB/s", "us_per_call_median": med * 1e3,
+                                    "us_per_call_min": min(times) * 1e3, "bytes_per_call": kv_s + io_s,
+                                    "frac_of_hbm_peak": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
+                                    "window": ps.window, "l2": "flushed (512 MB write) before every call"}
     return res
 
 

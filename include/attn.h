@@ -155,23 +155,29 @@ ATTN_API int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v
 
 /*
  * attn_decode_paged -- one new query token per request over a paged KV cache
- * ("flex_attention + paged KV ..." page, "Architecture notes").
+ * ("flex_attention + paged KV ..." page, "Architecture notes"), optionally over a sliding
+ * window (the head_dim 256 sliding-window layers of the Gemma4 FFPA page at inference).
  *   q [B, Hq, D] bf16; k_cache, v_cache [num_pages, page_size, Hkv, D] bf16;
  *   block_table DEVICE int32 [B, max_pages_per_seq]: page ids of request b in order;
- *   seq_lens DEVICE int32 [B]: cached tokens of request b (the query is token L-1 and
- *   sees all L of them). o [B, Hq, D] bf16 out, lse [B, Hq] fp32 out.
+ *   seq_lens DEVICE int32 [B]: cached tokens of request b (the query is token L-1).
+ *   window: 0 = the query sees all L cached keys; W > 0 = only keys max(0, L-W) .. L-1 (pages
+ *   wholly before the window are not read); W < 0 is rejected.
+ *   o [B, Hq, D] bf16 out, lse [B, Hq] fp32 out.
  *   A request with L = 0 gets o = 0 and lse = -inf. Page ids outside [0, num_pages) or
  *   lengths beyond max_pages_per_seq * page_size are not read: the affected tokens are
  *   skipped and ATTN_ERR_DEVICE_BOUNDS is recorded for attn_get_device_status().
- *   Supported: D = 128, page_size = 16, Hkv <= 8, Hq / Hkv in {1, 2, 4, 8}, B <= 4096.
- *   workspace: at least attn_workspace_size(ATTN_OP_DECODE_PAGED, ...) bytes; it holds
- *   split partials and per-request arrival counters. The counters must be zero before
- *   the FIRST call on a workspace (e.g. cudaMemset); every call leaves them zero again.
- *   Calls that share a workspace must not overlap on the GPU.
+ *   Supported: D = 128 with Hq / Hkv in {1, 2, 4, 8}, D = 256 with Hq / Hkv in {1, 2, 4};
+ *   page_size = 16, Hkv <= 256, B <= 4096.
+ *   workspace: at least attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, ...) bytes;
+ *   it holds split partials and arrival counters (one per request and block of KV heads) at its
+ *   start. The counters must be zero before the first call on a workspace, and again when a
+ *   call's (B, Hq, Hkv, D) differs from the previous call's on it: clear the first 4 * B * Hkv
+ *   bytes (e.g. cudaMemsetAsync), since the previous call's partials may lie there. Every call
+ *   leaves its own counters zero. Calls that share a workspace must not overlap on the GPU.
  */
 ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                       const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
-                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale,
+                      int Hkv, int D, int page_size, int max_pages_per_seq, int num_pages, float scale, int window,
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
@@ -198,15 +204,35 @@ ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, con
 ATTN_API int attn_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                                        const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse,
                                        int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
-                                       int num_pages, float scale, void* stream);
+                                       int num_pages, float scale, int window, void* stream);
 
 /* attn_decode_paged_noalloc_max_bytes -- size of the built-in decode scratch buffer (bytes). */
 ATTN_API size_t attn_decode_paged_noalloc_max_bytes(void);
 
 /*
+ * attn_merge_lse -- combine attention results computed over disjoint sets of keys into the
+ * attention over all of them: the combining step of context-parallel ring attention, where each
+ * ring chunk of keys is attended separately ("Gemma4 FFPA attention backend support ..." page,
+ * "Integration"). Part p holds o_p, normalised over its own keys, and lse_p (natural log of the
+ * sum of exp(scale * q.k) over them), as every forward of this library returns them. Per row:
+ *   lse = ln sum_p exp(lse_p),   o = sum_p exp(lse_p - lse) * o_p   (fp32, o rounded to bf16)
+ * A part with lse_p = -inf (no allowed key) contributes nothing, whatever its o_p holds; a row
+ * with no key in any part gets o = 0, lse = -inf. lse values must be finite or -inf.
+ *   o_parts [num_parts, B, S, H, D] bf16 and lse_parts [num_parts, B, H, S] fp32: the parts
+ *   stacked in the forward's layouts (packed [T, H, D] / [H, T] results: B = 1, S = T).
+ *   o [B, S, H, D] bf16 out, lse [B, H, S] fp32 out. The outputs may be part 0's own buffers
+ *   (o == o_parts and lse == lse_parts: a running merge in place); any other overlap between
+ *   inputs and outputs is not allowed.
+ *   Supported: D in {64, 128, 256, 512}, 1 <= num_parts <= 64. o_parts and o 16-byte aligned.
+ *   With B, S or H zero there is nothing to do and the pointers may be NULL. No workspace.
+ */
+ATTN_API int attn_merge_lse(const attn_bf16* o_parts, const float* lse_parts, attn_bf16* o, float* lse, int num_parts,
+                            int B, int S, int H, int D, void* stream);
+
+/*
  * attn_workspace_size -- bytes of workspace an operation needs (0 if none).
  *   For ATTN_OP_BWD: B, Hq, S, D; for ATTN_OP_BWD_VARLEN pass B = 1 and S = total tokens.
- *   For ATTN_OP_DECODE_PAGED: B, Hq, D. Unused arguments are ignored. Returns 0 for an
+ *   For ATTN_OP_DECODE_PAGED: B, Hq, Hkv, D. Unused arguments are ignored. Returns 0 for an
  *   unknown op. Pure host arithmetic; needs no GPU.
  */
 ATTN_API size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D, int num_seqs, int max_pages_per_seq);

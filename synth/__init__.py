@@ -16,6 +16,13 @@ Recipe (all draws counter based, see ``synth.c``):
   a Fisher-Yates permutation of the 4096 pool pages (stream 12) is dealt in
   order to the requests, ``ceil(L / 16)`` pages each; unused block-table entries
   are -1. The whole pool and q are N(0, 1) bf16 (streams 13, 14, 1).
+* sliding-window decode, head_dim 256: contexts uniform integers in [1024, 4096] (stream 11),
+  the pool sized to the requests' pages plus 64 and dealt as for paged decode.
+* chunked prefill over a paged cache: as paged decode, with each request's last
+  q_len tokens new (q packed by ``cu_q``, stream 1).
+* merge of results over disjoint key sets: part outputs N(0, 1) bf16 (stream 15);
+  part lse = 8 + 2 * (a bf16 N(0, 1) draw, stream 16), exact in fp32; optionally a
+  percentage of (part, row) entries empty (lse = -inf) by uniform draws (stream 17).
 """
 from __future__ import annotations
 
@@ -35,6 +42,7 @@ _lib = None
 
 STREAM_Q, STREAM_K, STREAM_V, STREAM_DO = 1, 2, 3, 4
 STREAM_SEQLENS, STREAM_CTX, STREAM_PERM, STREAM_KCACHE, STREAM_VCACHE = 10, 11, 12, 13, 14
+STREAM_OPARTS, STREAM_LSEPARTS, STREAM_EMPTY = 15, 16, 17
 
 
 def build(force: bool = False) -> str:
@@ -176,6 +184,7 @@ class Paged:
     q: np.ndarray = field(repr=False)
     k_cache: np.ndarray = field(repr=False)
     v_cache: np.ndarray = field(repr=False)
+    window: int = 0  # > 0: the query sees only the last `window` keys
 
 
 def dense(B, Hq, Hkv, S, D, window=0, seed=0, outlier_frac=0.0, outlier_scale=1.0, scale=None,
@@ -206,7 +215,7 @@ def varlen(num_seqs, lo, hi, Hq, Hkv, D, window=0, seed=0, name="varlen", with_d
 
 
 def paged_from_lengths(seq_lens, Hq, Hkv, D, page_size=16, num_pages=4096, seed=0, scale=None,
-                       max_pages=None, name="paged") -> Paged:
+                       max_pages=None, name="paged", window=0) -> Paged:
     seq_lens = np.asarray(seq_lens, dtype=np.int64)
     B = len(seq_lens)
     need = (seq_lens + page_size - 1) // page_size
@@ -225,7 +234,8 @@ def paged_from_lengths(seq_lens, Hq, Hkv, D, page_size=16, num_pages=4096, seed=
     kc = normal_bf16(seed, STREAM_KCACHE, (num_pages, page_size, Hkv, D))
     vc = normal_bf16(seed, STREAM_VCACHE, (num_pages, page_size, Hkv, D))
     return Paged(name, B, Hq, Hkv, D, page_size, num_pages, max_pages,
-                 float(scale if scale is not None else D ** -0.5), seq_lens.astype(np.int32), bt, q, kc, vc)
+                 float(scale if scale is not None else D ** -0.5), seq_lens.astype(np.int32), bt, q, kc, vc,
+                 int(window))
 
 
 @dataclass
@@ -287,6 +297,30 @@ def paged(B, lo, hi, Hq, Hkv, D, page_size=16, num_pages=4096, seed=0, max_pages
     return paged_from_lengths(lens, Hq, Hkv, D, page_size, num_pages, seed, max_pages=max_pages, name=name)
 
 
+@dataclass
+class MergeParts:
+    """Results over P disjoint key sets in the forward's layouts: o_parts [P, B, S, H, D] bf16
+    bits, lse_parts [P, B, H, S] fp32 (-inf = no key in that part for that row)."""
+    name: str
+    P: int
+    B: int
+    S: int
+    H: int
+    D: int
+    o_parts: np.ndarray = field(repr=False)
+    lse_parts: np.ndarray = field(repr=False)
+
+
+def merge_parts(P, B, S, H, D, seed=0, empty_pct=0, name="merge_parts") -> MergeParts:
+    o = normal_bf16(seed, STREAM_OPARTS, (P, B, S, H, D))
+    lb = normal_bf16(seed, STREAM_LSEPARTS, (P, B, H, S))
+    lse = (lb.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0) + np.float32(8.0)
+    if empty_pct:
+        draw = uniform_int(seed, STREAM_EMPTY, P * B * H * S, 0, 99).reshape(P, B, H, S)
+        lse[draw < empty_pct] = -np.inf
+    return MergeParts(name, P, B, S, H, D, o, lse.astype(np.float32))
+
+
 # The five workloads, named by what they are.
 def tiny_d512_causal(seed=0) -> Dense:
     return dense(1, 2, 1, 128, 512, 0, seed, name="tiny_d512_causal")
@@ -311,6 +345,21 @@ def prefill_paged_d512(seed=0) -> PagedPrefill:
     ctx = uniform_int(seed, STREAM_CTX, 8, 1024, 4096)
     return prefill_paged_from_lengths(ctx, np.full(8, 512), 32, 4, 512, page_size=16, seed=seed,
                                       name="prefill_paged_d512")
+
+
+def merge_cp8_d512(seed=0) -> MergeParts:
+    """The combining step of an 8-way context-parallel ring over a 16k-token sequence, seen from
+    one rank: its 2048 query tokens' results from 8 key chunks, 32 heads of dim 512."""
+    return merge_parts(8, 1, 2048, 32, 512, seed, name="merge_cp8_d512")
+
+
+def decode_paged_swa_d256(seed=0) -> Paged:
+    """Sliding-window decode at head_dim 256 (the window workload's heads and window: Hq 32,
+    Hkv 16, W 1024) for 64 requests with contexts uniform in [1024, 4096], so the window binds."""
+    lens = uniform_int(seed, STREAM_CTX, 64, 1024, 4096)
+    need = int(((lens + 15) // 16).sum())
+    return paged_from_lengths(lens, 32, 16, 256, 16, need + 64, seed, max_pages=256, name="decode_paged_swa_d256",
+                              window=1024)
 
 
 def decode_paged_d128(seed=0) -> Paged:

@@ -53,6 +53,9 @@ def test_workspace_sizes(lib):
     assert attn.attn_workspace_size(attn.ATTN_OP_BWD_VARLEN, 1, 32, 4, 18000, 512) >= 18000 * 32 * 513 * 4
     d = attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, 64, 32, 8, 0, 128)
     assert d >= 64 * 4 + 64 * 32 * 130 * 4
+    # head_dim 256 with 16 KV heads: four blocks of 4 heads, a counter per (request, block)
+    d2 = attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, 64, 32, 16, 0, 256)
+    assert d2 >= 64 * 4 * 4 + 64 * 32 * 260 * 4
     assert attn.attn_workspace_size(99, 1, 1, 1, 1, 256) == 0
 
 
@@ -114,17 +117,20 @@ def test_bwd_argument_checks(lib):
 
 
 def test_decode_argument_checks(lib):
-    def call(B=4, Hq=32, Hkv=8, D=128, ps=16, maxp=8, npages=64, scale=0.088, ws=P(256 * 4096), wsb=1 << 30,
-             bt=P(A), q=P(A)):
+    def call(B=4, Hq=32, Hkv=8, D=128, ps=16, maxp=8, npages=64, scale=0.088, window=0, ws=P(256 * 4096),
+             wsb=1 << 30, bt=P(A), q=P(A)):
         return lib.attn_decode_paged(q, P(A), P(A), bt, P(A), P(A), P(A), B, Hq, Hkv, D, ps, maxp, npages, scale,
-                                     ws, wsb, None)
+                                     window, ws, wsb, None)
     assert call(bt=None) == INVALID
     assert call(Hq=30) == INVALID
     assert call(scale=0.0) == INVALID
     assert call(B=-1) == INVALID
-    assert call(D=256) == UNSUPPORTED
+    assert call(window=-1) == INVALID
+    assert call(D=64) == UNSUPPORTED
+    assert call(D=512) == UNSUPPORTED
+    assert call(D=256, Hq=64, Hkv=8) == UNSUPPORTED  # group of 8 at head_dim 256
     assert call(ps=32) == UNSUPPORTED
-    assert call(Hkv=16, Hq=32) == UNSUPPORTED
+    assert call(Hkv=512, Hq=512) == UNSUPPORTED
     assert call(Hq=8 * 16, Hkv=8) == UNSUPPORTED  # group of 16
     assert call(B=5000) == UNSUPPORTED
     assert call(q=P(A + 8)) == MISALIGNED
@@ -155,6 +161,20 @@ def test_prefill_paged_argument_checks(lib):
     assert call(cu=P(A + 2)) == MISALIGNED
     assert call(T=0) == OK
     assert call(R=0, q=None, bt=None, cu=None) == OK  # nothing to do: pointers may be NULL
+
+
+def test_merge_lse_argument_checks(lib):
+    def call(op=P(A), lp=P(A), o=P(A), l=P(A), n=4, B=1, S=100, H=8, D=512):
+        return lib.attn_merge_lse(op, lp, o, l, n, B, S, H, D, None)
+    assert call(n=0) == INVALID
+    assert call(B=-1) == INVALID
+    assert call(H=0) == INVALID
+    assert call(op=None) == INVALID
+    assert call(D=96) == UNSUPPORTED
+    assert call(n=65) == UNSUPPORTED
+    assert call(op=P(A + 8)) == MISALIGNED
+    assert call(l=P(A + 2)) == MISALIGNED
+    assert call(S=0, op=None, lp=None, o=None, l=None) == OK
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

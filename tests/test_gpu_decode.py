@@ -1,0 +1,106 @@
+"""Paged decode beyond the head_dim 128 workload: sliding windows, head_dim 256, KV heads split
+into blocks, against the fp64 oracle; and the sliding-window head_dim 256 workload at full size."""
+import numpy as np
+import pytest
+import torch
+
+import attention_flash_gqa_gb300 as attn
+import synth
+from gpu_util import check, check_lse, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+LENS = [1, 15, 16, 17, 33, 256, 1024, 0, 700, 5, 2049]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from attention_flash_gqa_gb300 import _build
+
+    _build.build()
+    attn.load_library()
+    torch.cuda.set_device(0)
+
+
+def run(pp, window=None):
+    q, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
+    bt = torch.from_numpy(pp.block_table).cuda()
+    sl = torch.from_numpy(pp.seq_lens).cuda()
+    o, lse = attn.attn_decode_paged(q, kc, vc, bt, sl, scale=pp.scale, window=pp.window if window is None else window)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    return to_np(o), to_np(lse)
+
+
+def compare(orc, pp, window):
+    o, lse = run(pp, window)
+    ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, window)
+    check("o", o, ro)
+    check_lse("lse", lse, rl)
+    empty = [i for i, L in enumerate(pp.seq_lens) if L == 0]
+    for i in empty:
+        assert np.all(o[i] == 0) and np.all(np.isneginf(lse[i]))
+
+
+@pytest.mark.parametrize("window", [1, 15, 16, 17, 100, 1024, 5000])
+def test_decode_window_d128(orc, window):
+    pp = synth.paged_from_lengths(LENS, 32, 8, 128, page_size=16, num_pages=512, seed=window, max_pages=160)
+    compare(orc, pp, window)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 16), (16, 4), (4, 4), (8, 2), (2, 2), (24, 6)])
+@pytest.mark.parametrize("window", [0, 1, 40, 1024])
+def test_decode_d256(orc, Hq, Hkv, window):
+    pp = synth.paged_from_lengths(LENS, Hq, Hkv, 256, page_size=16, num_pages=512, seed=Hq * 7 + Hkv + window,
+                                  max_pages=160)
+    compare(orc, pp, window)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(64, 8), (128, 16), (16, 16)])
+def test_decode_d128_head_blocks(orc, Hq, Hkv):
+    """More KV heads than one unit holds: the heads are served in blocks by the grid's y."""
+    pp = synth.paged_from_lengths(LENS, Hq, Hkv, 128, page_size=16, num_pages=512, seed=Hq + Hkv, max_pages=160)
+    compare(orc, pp, 0)
+    compare(orc, pp, 300)
+
+
+def test_decode_window_unused_tokens_are_never_read(orc):
+    """Tokens before the window and slots past the end hold NaN: neither reaches the result."""
+    pp = synth.paged_from_lengths([40, 100, 17], 8, 4, 256, page_size=16, num_pages=16, seed=5, max_pages=7)
+    W = 37
+    kc, vc = pp.k_cache.copy(), pp.v_cache.copy()
+    for b, L in enumerate(pp.seq_lens):
+        for t in list(range(0, max(0, L - W))) + list(range(L, ((L + 15) // 16) * 16)):
+            page = pp.block_table[b, t // 16]
+            kc[page, t % 16] = 0x7FC0
+            vc[page, t % 16] = 0x7FC0
+    bad = synth.Paged(**{**pp.__dict__, "k_cache": kc, "v_cache": vc})
+    o, lse = run(bad, W)
+    ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, W)
+    check("o", o, ro)
+    check_lse("lse", lse, rl)
+
+
+def test_decode_noalloc_window_d256(orc):
+    pp = synth.paged_from_lengths([300, 17, 1024], 32, 16, 256, page_size=16, num_pages=128, seed=8, max_pages=64)
+    q, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
+    bt = torch.from_numpy(pp.block_table).cuda()
+    sl = torch.from_numpy(pp.seq_lens).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((pp.B, pp.Hq), dtype=torch.float32, device="cuda")
+    attn.attn_decode_paged_noalloc(q, kc, vc, bt, sl, o, lse, scale=pp.scale, window=100)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, 100)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
+
+
+def test_decode_swa_d256_full_workload(orc):
+    """The benchmarked sliding-window workload (64 requests, contexts U[1024, 4096], Hq 32, Hkv 16,
+    D 256, W 1024) in the benchmark's launch, every output against the oracle."""
+    pp = synth.decode_paged_swa_d256(seed=0)
+    o, lse = run(pp)
+    ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, pp.window)
+    check("o", o, ro)
+    check_lse("lse", lse, rl)

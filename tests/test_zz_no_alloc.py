@@ -62,7 +62,7 @@ def test_noalloc_rejects_problems_beyond_the_buffer(lib):
     args = [fake] * 7
 
     def call(B, Hq):
-        return lib.attn_decode_paged_noalloc(*args, B, Hq, 8, 128, 16, 64, 4096, 0.088, None)
+        return lib.attn_decode_paged_noalloc(*args, B, Hq, 8, 128, 16, 64, 4096, 0.088, 0, None)
 
     assert attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, 481, 32, 8, 0, 128) > cap
     assert call(481, 32) == 4  # ATTN_ERR_WORKSPACE
