@@ -109,12 +109,13 @@ bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int rows, int 
 
 // 5-D map over a paged cache [num_pages, 16, heads, dim] viewed as (64 dims, 8 rows, heads*dim/64
 // chunks of 64 dims, 2 groups of 8 rows, pages); box = 64 x 8 x 2 x 2 x 1: 16 rows x 128 dims of
-// one head of one page (4 KB), the two 64-dim chunks interleaved per 8-row group.
+// one head of one page (4 KB), the two 64-dim chunks interleaved per 8-row group (D = 64: one
+// chunk, 2 KB).
 bool make_cache_map(CUtensorMap* m, const void* base, int D, int H, int num_pages) {
     const cuuint64_t row = (cuuint64_t)H * D * 2;
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)H * D / 64, 2, (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
-    cuuint32_t box[5] = {64, 8, 2, 2, 1};
+    cuuint32_t box[5] = {64, 8, D >= 128 ? 2u : 1u, 2, 1};  // the forward's slot width: 128 (or 64) dims
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -132,12 +133,15 @@ int check_common(int Hq, int Hkv, float scale, int causal, int window) {
 }
 
 int check_prefill_shape(long long rows, int Hq, int Hkv, int D, int S) {
-    if (D != 256 && D != 512) return ATTN_ERR_UNSUPPORTED;
+    if (D != 64 && D != 128 && D != 256 && D != 512) return ATTN_ERR_UNSUPPORTED;
     if (S > 65535LL * 128) return ATTN_ERR_UNSUPPORTED;
     if (rows > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;  // TMA row coordinates are int32
     (void)Hq, (void)Hkv;
     return ATTN_OK;
 }
+
+// CTAs per query tile and head in the forward: one per 256 output columns.
+int fwd_splits(int D) { return D > 256 ? D / 256 : 1; }
 
 size_t bwd_ws(long long rows, int Hq, int D) {
     return align256((size_t)rows * Hq * D * 4) + align256((size_t)rows * Hq * 4);
@@ -317,7 +321,7 @@ int attn_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf
     if (st) return st;
     const long long rows = (long long)B * S;
     if ((st = check_prefill_shape(rows, Hq, Hkv, D, S))) return st;
-    if (B > 65535 / (D / 256)) return ATTN_ERR_UNSUPPORTED;
+    if (B > 65535 / fwd_splits(D)) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
     if (rows == 0) return ATTN_OK;
     return fwd_common(q, k, v, o, lse, nullptr, B, S, rows, B, Hq, Hkv, D, scale, window, stream);
@@ -332,7 +336,7 @@ int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, 
     int st = check_common(Hq, Hkv, scale, causal, window);
     if (st) return st;
     if ((st = check_prefill_shape(total_tokens, Hq, Hkv, D, max_seqlen))) return st;
-    if (num_seqs > 65535 / (D / 256)) return ATTN_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 / fwd_splits(D)) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse)) return ATTN_ERR_MISALIGNED;
     if (num_seqs == 0 || total_tokens == 0 || max_seqlen == 0) return ATTN_OK;
     return fwd_common(q, k, v, o, lse, cu_seqlens, num_seqs, max_seqlen, total_tokens, 1, Hq, Hkv, D, scale, window,
@@ -348,7 +352,7 @@ int attn_fwd_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16
     int st = check_common(Hq, Hkv, scale, causal, window);
     if (st) return st;
     if ((st = check_prefill_shape(total_q, Hq, Hkv, D, max_q_len))) return st;
-    if (page_size != 16 || num_reqs > 65535 / (D / 256) || max_pages_per_seq > (1 << 24)) return ATTN_ERR_UNSUPPORTED;
+    if (page_size != 16 || num_reqs > 65535 / fwd_splits(D) || max_pages_per_seq > (1 << 24)) return ATTN_ERR_UNSUPPORTED;
     if (num_reqs == 0 || total_q == 0 || max_q_len == 0) return ATTN_OK;  // nothing to read or write
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !cu_q || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
@@ -383,6 +387,7 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
     const long long rows = (long long)B * S;
     const int grid_len = varlen ? max_seqlen : S;
     if ((st = check_prefill_shape(rows, Hq, Hkv, D, grid_len))) return st;
+    if (D < 256) return ATTN_ERR_UNSUPPORTED;  // head_dim 64 / 128: forward only so far
     if ((varlen ? num_seqs : B) > 65535) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
         !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))

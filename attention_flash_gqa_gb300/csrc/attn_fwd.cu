@@ -37,22 +37,28 @@
 namespace attn {
 namespace {
 
-constexpr int kBQ = 128, kBKV = 128, kDV = 256;
+constexpr int kBQ = 128, kBKV = 128;
 constexpr int kThreads = 192;
-constexpr uint32_t kSlotBytes = 32768;
 constexpr uint32_t kSubBytes = 16384;  // 128 rows x 64 bf16
 constexpr float kRescaleLog2 = 8.0f;
-constexpr uint32_t kPagedGroupStride = 2048;  // paged slots: bytes between 8-row groups
 
 template <int DQK>
 struct FwdCfg {
-    static constexpr int kQChunks = DQK / 128;  // 32 KB slots per K tile
-    static constexpr int kVChunks = kDV / 128;  // 32 KB slots per V half-tile
-    static constexpr int kStages = DQK == 256 ? 5 : 3;
+    static constexpr int kDV = DQK < 256 ? DQK : 256;      // O columns per CTA
+    static constexpr int kSubs = DQK >= 128 ? 2 : 1;        // 64-column sub-tiles per slot
+    static constexpr int kSlotCols = 64 * kSubs;
+    static constexpr uint32_t kSlotBytes = kSubs * kSubBytes;
+    static constexpr int kQChunks = DQK / kSlotCols;        // slots per K tile
+    static constexpr int kVChunks = kDV / kSlotCols;        // slots per V tile (this CTA's columns)
+    // ring depth: what shared memory leaves next to the resident Q tile
+    static constexpr int kStages = DQK == 512 ? 3 : DQK == 256 ? 5 : DQK == 128 ? 6 : 12;
     static constexpr uint32_t kQBytes = DQK * 256;  // 128 rows x DQK bf16
     static constexpr uint32_t kOffSlots = kQBytes;
     static constexpr uint32_t kOffBar = kOffSlots + kStages * kSlotBytes;
-    static constexpr uint32_t kSmem = kOffBar + 256 + 1024;  // + alignment slack
+    static constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
+    // paged slots: the slot's sub-tiles interleaved per 8-row group
+    static constexpr uint32_t kPagedGroupStride = 1024 * kSubs;
+    static_assert(kSmem <= 232448, "shared memory");
 };
 
 struct FwdArgs {
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (q0 >= nq) return;  // uniform: before any barrier or TMEM use
     const int qp0 = qoff + q0;  // position of the tile's first query
     const int g = h / (a.Hq / a.Hkv);
-    const int dv0 = split * kDV;
+    const int dv0 = split * C::kDV;
     const int kv_hi = min(L, qp0 + kBQ);
     const int kv_lo = a.window > 0 ? max(0, qp0 - a.window + 1) : 0;
     const int t_begin = kv_lo / kBKV, t_end = (kv_hi + kBKV - 1) / kBKV;
@@ -184,16 +190,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int slot = 0, round = 0;
         bool ok = true;
-        // one slot = 128 keys x 128 columns: lane i < 8 loads page i's 4 KB box
+        // one slot = 128 keys x kSlotCols columns: lane i < 8 loads page i's box (16 rows x kSlotCols)
         const int chunk0 = g * (DQK / 64);  // first 64-column chunk of KV head g
         auto load_slot = [&](const CUtensorMap* map, int col0, int ids, int& used_slot, int& used_round) -> bool {
             if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag,
                                                                  a.status, 0x11)))
                 return false;
             const uint32_t fb = smem_u32(&full[slot]);
-            if (lane == 0) mbar_expect_tx(fb, kSlotBytes);
-            const uint32_t dst = sSlots + slot * kSlotBytes;
-            if (lane < 8) tma_load_5d(dst + lane * 4096, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
+            if (lane == 0) mbar_expect_tx(fb, C::kSlotBytes);
+            const uint32_t dst = sSlots + slot * C::kSlotBytes;
+            if (lane < 8) tma_load_5d(dst + lane * 2 * C::kPagedGroupStride, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
             used_slot = slot, used_round = round;
             if (++slot == C::kStages) slot = 0, ++round;
             return true;
@@ -205,12 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_k = [&]() -> bool {
             int us, ur;
             for (int c = 0; c < C::kQChunks; ++c)
-                if (!load_slot(&tk, c * 128, k_cur, us, ur)) return false;
+                if (!load_slot(&tk, c * C::kSlotCols, k_cur, us, ur)) return false;
             return true;
         };
         auto load_v = [&]() -> bool {
             for (int c = 0; c < C::kVChunks; ++c)
-                if (!load_slot(&tv, dv0 + c * 128, v_cur, vs[c], vr[c])) return false;
+                if (!load_slot(&tv, dv0 + c * C::kSlotCols, v_cur, vs[c], vr[c])) return false;
             return true;
         };
         int kt = 0, vt = 0;  // next K / V tile to load
@@ -245,12 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; ok && c < C::kVChunks; ++c)
                 ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[vs[c]]), vr[c] & 1, abort_flag, a.status, 0x1e));
             if (ok) {
-                const int units = (kBQ - r_valid) * 16;  // 16-byte pieces of the rows past the end (2 chunks)
+                const int units = (kBQ - r_valid) * 8 * C::kSubs;  // 16-byte pieces of the rows past the end
                 for (int c = 0; c < C::kVChunks; ++c) {
-                    const uint32_t base = sSlots + vs[c] * kSlotBytes;
+                    const uint32_t base = sSlots + vs[c] * C::kSlotBytes;
                     for (int e = lane; e < units; e += 32) {
-                        const int row = r_valid + (e >> 4), chunk = (e >> 3) & 1, piece = e & 7;
-                        st_shared_v4(base + (row >> 3) * kPagedGroupStride + chunk * 1024 + (row & 7) * 128 + piece * 16,
+                        const int row = r_valid + e / (8 * C::kSubs), chunk = (e >> 3) % C::kSubs, piece = e & 7;
+                        st_shared_v4(base + (row >> 3) * C::kPagedGroupStride + chunk * 1024 + (row & 7) * 128 + piece * 16,
                                      0u, 0u, 0u, 0u);
                     }
                 }
@@ -282,21 +288,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_chunk = [&](const CUtensorMap* map, int col0, int row0) -> bool {
                 if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x11)) return false;
                 const uint32_t fb = smem_u32(&full[slot]);
-                mbar_expect_tx(fb, kSlotBytes);
-                const uint32_t dst = sSlots + slot * kSlotBytes;
-                tma_load_4d(dst, map, fb, col0, g, row0, bcoord);
-                tma_load_4d(dst + kSubBytes, map, fb, col0 + 64, g, row0, bcoord);
+                mbar_expect_tx(fb, C::kSlotBytes);
+                const uint32_t dst = sSlots + slot * C::kSlotBytes;
+                for (int sub = 0; sub < C::kSubs; ++sub)
+                    tma_load_4d(dst + sub * kSubBytes, map, fb, col0 + sub * 64, g, row0, bcoord);
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
             auto load_k = [&](int t) -> bool {
                 for (int c = 0; c < C::kQChunks; ++c)
-                    if (!load_chunk(&tk, c * 128, seq_start + (t_begin + t) * kBKV)) return false;
+                    if (!load_chunk(&tk, c * C::kSlotCols, seq_start + (t_begin + t) * kBKV)) return false;
                 return true;
             };
             auto load_v = [&](int t) -> bool {
                 for (int c = 0; c < C::kVChunks; ++c)
-                    if (!load_chunk(&tv, dv0 + c * 128, seq_start + (t_begin + t) * kBKV)) return false;
+                    if (!load_chunk(&tv, dv0 + c * C::kSlotCols, seq_start + (t_begin + t) * kBKV)) return false;
                 return true;
             };
             ok = load_k(0);
@@ -317,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------- UMMA issuer -----------------------------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // Q K^T: both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(128, 128, false, true);   // P (TMEM) V: V is N-major
+            constexpr uint32_t idO = idesc_bf16_f32(128, C::kSlotCols, false, true);  // P (TMEM) V: V is N-major
             int slot = 0, round = 0;
             bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.status, 0x12);
             tc_fence_after();
@@ -334,12 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = tS0 + buf * 128;
                 for (int c = 0; c < C::kQChunks; ++c) {
                     if (!next_slot()) return false;
-                    const uint32_t kslot = sSlots + slot * kSlotBytes;
-                    for (int sub = 0; sub < 2; ++sub)
+                    const uint32_t kslot = sSlots + slot * C::kSlotBytes;
+                    for (int sub = 0; sub < C::kSubs; ++sub)
                         for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sdesc_sw128(sQ + (2 * c + sub) * kSubBytes + kk * 32, 16, 1024);
-                            const uint64_t bd = PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, kPagedGroupStride)
-                                                      : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
+                            const uint64_t ad =
+                                sdesc_sw128(sQ + (C::kSubs * c + sub) * kSubBytes + kk * 32, 16, 1024);
+                            const uint64_t bd =
+                                PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, C::kPagedGroupStride)
+                                      : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
                             umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
                         }
                     release_slot();
@@ -354,12 +362,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!mbar_wait(smem_u32(vfix), 0, abort_flag, a.status, 0x1f)) return false;
                         tc_fence_after();
                     }
-                    const uint32_t vslot = sSlots + slot * kSlotBytes;
+                    const uint32_t vslot = sSlots + slot * C::kSlotBytes;
                     const uint32_t tP = tS0 + (j & 1) * 128;  // P of step j, packed bf16 pairs
                     for (int kk = 0; kk < 8; ++kk) {          // 16 keys per step
-                        const uint64_t bd = PAGED ? sdesc_sw128(vslot + kk * 2 * kPagedGroupStride, 1024, kPagedGroupStride)
-                                                  : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
-                        umma_bf16_ts(tO + c * 128, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                        const uint64_t bd =
+                            PAGED ? sdesc_sw128(vslot + kk * 2 * C::kPagedGroupStride, 1024, C::kPagedGroupStride)
+                                  : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
+                        umma_bf16_ts(tO + c * C::kSlotCols, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     release_slot();
                 }
@@ -440,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const float f = moved ? alpha : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < kDV / 32; ++c) {
+                for (int c = 0; c < C::kDV / 32; ++c) {
                     uint32_t raw[32];
                     tmem_ld32(tO + c * 32 + lane_base, raw);
                     tmem_ld_wait();
@@ -480,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint16_t* orow = a.o + ((size_t)(packed ? seq_start + qrow : seq * a.S + qrow) * a.Hq + h) * a.D + dv0;
 #pragma unroll 1
-            for (int c = 0; c < kDV / 32; ++c) {
+            for (int c = 0; c < C::kDV / 32; ++c) {
                 uint32_t raw[32];
                 tmem_ld32(tO + c * 32 + lane_base, raw);
                 tmem_ld_wait();
@@ -520,14 +529,16 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     a.max_pages = L.max_pages, a.num_pages = L.num_pages;
     a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.D = L.D, a.window = L.window;
     a.n_qtiles = (L.S + kBQ - 1) / kBQ;
-    a.nsplit = DQK / kDV;
+    a.nsplit = DQK / C::kDV;
     a.T = L.total_rows;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     cudaError_t e =
         cudaFuncSetAttribute(fwd_kernel<DQK, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.Hq, L.nseq * a.nsplit, a.n_qtiles);
-    const char* name = PAGED ? (DQK == 256 ? "fwd_paged_d256" : "fwd_paged_d512") : (DQK == 256 ? "fwd_d256" : "fwd_d512");
+    static const char* const kNames[2][4] = {{"fwd_d64", "fwd_d128", "fwd_d256", "fwd_d512"},
+                                             {"fwd_paged_d64", "fwd_paged_d128", "fwd_paged_d256", "fwd_paged_d512"}};
+    const char* name = kNames[PAGED ? 1 : 0][DQK == 64 ? 0 : DQK == 128 ? 1 : DQK == 256 ? 2 : 3];
     const ProfMark m = prof_begin(stream, name);
     fwd_kernel<DQK, PAGED><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
     prof_end(stream, m);
@@ -539,6 +550,8 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     if (L.nseq == 0 || L.S == 0) return cudaSuccess;
     const bool paged = L.block_table != nullptr;
+    if (L.D == 64) return paged ? launch_fwd_t<64, true>(L, stream) : launch_fwd_t<64, false>(L, stream);
+    if (L.D == 128) return paged ? launch_fwd_t<128, true>(L, stream) : launch_fwd_t<128, false>(L, stream);
     if (L.D == 256) return paged ? launch_fwd_t<256, true>(L, stream) : launch_fwd_t<256, false>(L, stream);
     if (L.D == 512) return paged ? launch_fwd_t<512, true>(L, stream) : launch_fwd_t<512, false>(L, stream);
     return cudaErrorInvalidValue;

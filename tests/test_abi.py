@@ -75,7 +75,7 @@ def fwd(lib, **kw):
     (dict(Hq=0), INVALID), (dict(Hkv=0), INVALID), (dict(Hq=6, Hkv=4), INVALID),
     (dict(scale=0.0), INVALID), (dict(scale=-1.0), INVALID), (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID), (dict(window=-1), INVALID),
-    (dict(causal=0), UNSUPPORTED), (dict(D=128), UNSUPPORTED), (dict(D=64), UNSUPPORTED),
+    (dict(causal=0), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(D=1024), UNSUPPORTED),
     (dict(q=A + 8), MISALIGNED), (dict(o=A + 2), MISALIGNED), (dict(lse=A + 4), MISALIGNED),
     (dict(B=0), OK), (dict(S=0), OK),
 ])
@@ -154,7 +154,7 @@ def test_prefill_paged_argument_checks(lib):
     assert call(window=-2) == INVALID
     assert call(npages=0) == INVALID  # new tokens but no cache
     assert call(causal=0) == UNSUPPORTED
-    assert call(D=128) == UNSUPPORTED
+    assert call(D=96) == UNSUPPORTED
     assert call(ps=32) == UNSUPPORTED
     assert call(R=40000) == UNSUPPORTED  # 2 CTAs per (request, head) at D = 512
     assert call(q=P(A + 8)) == MISALIGNED

@@ -179,7 +179,7 @@ def test_prefill_paged_rejects_bad_arguments():
     with pytest.raises(attn.AttnError) as e:  # page_size 8 is not supported
         attn.attn_fwd_paged(q, kc.view(-1, 8, 2, 256), vc.view(-1, 8, 2, 256), bt, sl, cu, 8)
     assert e.value.status == 2
-    with pytest.raises(attn.AttnError) as e:  # D = 128 is the decode kernel's, not this one's
-        attn.attn_fwd_paged(q[..., :128].contiguous(), kc[..., :128].contiguous(), vc[..., :128].contiguous(), bt,
+    with pytest.raises(attn.AttnError) as e:  # D = 96 is not a supported head size
+        attn.attn_fwd_paged(q[..., :96].contiguous(), kc[..., :96].contiguous(), vc[..., :96].contiguous(), bt,
                             sl, cu, 8)
     assert e.value.status == 2

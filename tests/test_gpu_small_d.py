@@ -1,0 +1,62 @@
+"""head_dim 128 and 64 (Qwen3-class heads): the forward in its dense, windowed, varlen and paged
+forms against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import attention_flash_gqa_gb300 as attn
+import synth
+from gpu_util import check, check_lse, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from attention_flash_gqa_gb300 import _build
+
+    _build.build()
+    attn.load_library()
+    torch.cuda.set_device(0)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B,Hq,Hkv,S,W", [(2, 4, 2, 300, 0), (1, 8, 1, 385, 0), (1, 6, 2, 129, 0), (2, 4, 4, 700, 129),
+                                          (1, 2, 1, 1, 0), (1, 4, 1, 513, 1), (1, 4, 2, 640, 300)])
+def test_forward_small_d(orc, D, B, Hq, Hkv, S, W):
+    p = synth.dense(B, Hq, Hkv, S, D, W, seed=S + D + W, with_do=False)
+    q, k, v = to_dev(p.q), to_dev(p.k), to_dev(p.v)
+    o, lse = attn.attn_fwd(q, k, v, window=W, scale=p.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.fwd(p.q, p.k, p.v, p.scale, 1, W)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_small_d_varlen(orc, D):
+    vp = synth.varlen_from_lengths([1, 127, 128, 129, 300, 0, 513], 8, 2, D, seed=D, with_do=False)
+    q, k, v = to_dev(vp.q), to_dev(vp.k), to_dev(vp.v)
+    cu = torch.from_numpy(vp.cu_seqlens).cuda()
+    o, lse = attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, scale=vp.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.fwd_varlen(vp.q, vp.k, vp.v, vp.cu_seqlens, vp.scale)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
+
+
+@pytest.mark.parametrize("D,window", [(64, 0), (128, 0), (128, 100), (64, 37)])
+def test_prefill_paged_small_d(orc, D, window):
+    seq = [1, 16, 17, 300, 1000, 129, 700, 2049]
+    nq = [1, 16, 5, 300, 128, 0, 257, 131]
+    pp = synth.prefill_paged_from_lengths(seq, nq, 8, 2, D, window=window, seed=D + window)
+    q, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
+    bt, sl, cu = (torch.from_numpy(x).cuda() for x in (pp.block_table, pp.seq_lens, pp.cu_q))
+    o, lse = attn.attn_fwd_paged(q, kc, vc, bt, sl, cu, pp.max_q, window=window, scale=pp.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.prefill_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.cu_q, pp.scale, window)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
