@@ -14,7 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libattn_gb300.so")
 BUILD_DIR = os.path.join(HERE, "_build_tmp")
-SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "decode_paged.cu", "decode_paged_noalloc.cu", "merge_lse.cu"]
+SOURCES = ["api.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd_small.cu", "decode_paged.cu", "decode_paged_noalloc.cu",
+           "merge_lse.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

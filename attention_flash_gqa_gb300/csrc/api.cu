@@ -387,7 +387,6 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
     const long long rows = (long long)B * S;
     const int grid_len = varlen ? max_seqlen : S;
     if ((st = check_prefill_shape(rows, Hq, Hkv, D, grid_len))) return st;
-    if (D < 256) return ATTN_ERR_UNSUPPORTED;  // head_dim 64 / 128: forward only so far
     if ((varlen ? num_seqs : B) > 65535) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(dO) ||
         !aligned16(dQ) || !aligned16(dK) || !aligned16(dV))
@@ -402,9 +401,11 @@ int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, const a
     std::memset(&L, 0, sizeof(L));
     const int map_rows = varlen ? (int)rows : S, batch = varlen ? 1 : B;
     if (!make_map(&L.tq, q, D, Hq, map_rows, batch) || !make_map(&L.tk, k, D, Hkv, map_rows, batch) ||
-        !make_map(&L.tv, v, D, Hkv, map_rows, batch) || !make_map(&L.tdo, dO, D, Hq, map_rows, batch) ||
-        !make_map(&L.tqh, q, D, Hq, map_rows, batch, 256 * 128 / D) ||
-        !make_map(&L.tdoh, dO, D, Hq, map_rows, batch, 256 * 128 / D))
+        !make_map(&L.tv, v, D, Hkv, map_rows, batch) || !make_map(&L.tdo, dO, D, Hq, map_rows, batch))
+        return ATTN_ERR_LAUNCH;
+    // query-share maps of the cluster kernel (D >= 256 only)
+    if (D >= 256 && (!make_map(&L.tqh, q, D, Hq, map_rows, batch, 256 * 128 / D) ||
+                     !make_map(&L.tdoh, dO, D, Hq, map_rows, batch, 256 * 128 / D)))
         return ATTN_ERR_LAUNCH;
     L.q = q, L.k = k, L.v = v, L.o = o, L.dO = dO, L.lse = lse, L.dQ = dQ, L.dK = dK, L.dV = dV;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -585,26 +585,37 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const uint16_t* __restric
     if (w >= rows_times_heads) return;
     const long long row = w / Hq;
     const int h = (int)(w % Hq);
-    constexpr int E = D / 32;  // 8 or 16 elements per lane
+    constexpr int E = D / 32;  // 2, 4, 8 or 16 elements per lane
     const uint16_t* orow = o + w * D + lane * E;
     const uint16_t* drow = dO + w * D + lane * E;
     float acc = 0.f;
+    auto dot2 = [](uint32_t x, uint32_t y) {
+        return __uint_as_float(x << 16) * __uint_as_float(y << 16) +
+               __uint_as_float(x & 0xffff0000u) * __uint_as_float(y & 0xffff0000u);
+    };
+    if constexpr (E >= 8) {
 #pragma unroll
-    for (int e = 0; e < E; e += 8) {
-        const uint4 a = *reinterpret_cast<const uint4*>(orow + e);
-        const uint4 b = *reinterpret_cast<const uint4*>(drow + e);
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            acc += __uint_as_float(av[j] << 16) * __uint_as_float(bv[j] << 16);
-            acc += __uint_as_float(av[j] & 0xffff0000u) * __uint_as_float(bv[j] & 0xffff0000u);
+        for (int e = 0; e < E; e += 8) {
+            const uint4 a = *reinterpret_cast<const uint4*>(orow + e);
+            const uint4 b = *reinterpret_cast<const uint4*>(drow + e);
+            acc += dot2(a.x, b.x) + dot2(a.y, b.y) + dot2(a.z, b.z) + dot2(a.w, b.w);
         }
+    } else if constexpr (E == 4) {
+        const uint2 a = *reinterpret_cast<const uint2*>(orow);
+        const uint2 b = *reinterpret_cast<const uint2*>(drow);
+        acc = dot2(a.x, b.x) + dot2(a.y, b.y);
+    } else {
+        acc = dot2(*reinterpret_cast<const uint32_t*>(orow), *reinterpret_cast<const uint32_t*>(drow));
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float4* dq = reinterpret_cast<float4*>(dq_acc + w * D + lane * E);
+    float* dq = dq_acc + w * D + lane * E;
+    if constexpr (E >= 4) {
 #pragma unroll
-    for (int e = 0; e < E / 4; ++e) dq[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int e = 0; e < E; e += 4) *reinterpret_cast<float4*>(dq + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+        *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+    }
     if (lane == 0) {
         size_t li;
         if (cu_seqlens) {
@@ -645,7 +656,10 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    {
+    if constexpr (D < 256) {
+        cudaError_t e = launch_bwd_small_main<D>(L, stream);
+        if (e != cudaSuccess) return e;
+    } else {
         BwdArgs a;
         a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV;
         a.cu_seqlens = L.cu_seqlens, a.status = L.status;
@@ -690,6 +704,8 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
 
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream) {
     if (L.nseq == 0 || L.S == 0 || L.total_rows == 0) return cudaSuccess;
+    if (L.D == 64) return launch_bwd_t<64>(L, stream);
+    if (L.D == 128) return launch_bwd_t<128>(L, stream);
     if (L.D == 256) return launch_bwd_t<256>(L, stream);
     if (L.D == 512) return launch_bwd_t<512>(L, stream);
     return cudaErrorInvalidValue;

@@ -1,0 +1,482 @@
+// Attention backward main kernel for head_dim 128 and 64 (Qwen3-class heads), for the forward in
+// attn_fwd.cu. The same gradient as the D = 256 / 512 kernel in attn_bwd.cu:
+//   P  = exp(scale * Q K^T - lse),   dP = dO V^T,   dS = P * (dP - Delta)
+//   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K
+// but at D <= 128 one CTA's tensor memory holds everything a key tile needs, so there is no
+// cluster and no exchange of P^T / dS^T between CTAs.
+//
+// Source: the head_dim 128 attention of "flex_attention + paged KV + CUDA graphs vs vLLM"
+// ("Setup": Qwen3-4B heads) trained with the backward the FFPA page describes for its fused
+// kernel ("Gemma4 FFPA attention backend support ...": the fused path recomputes P from the
+// saved lse instead of materialising S x S).
+//
+// One CTA = one 128-key tile x one KV head. It keeps K and V resident in shared memory and
+// loops over every query head of the GQA group and every query tile that can see its keys
+// (causal / window tile skipping), accumulating dV and dK in tensor memory (summed over the
+// group without atomics). Per step (head h, query tile i):
+//   S^T  = K Q_i^T         (keys on TMEM lanes)       -> region R0
+//   dP^T = V dO_i^T                                    -> region R1
+//   elementwise warps: P^T = exp2(S^T * scale * log2 e - lse2) written back over R0 as bf16
+//   (the A operand of dV straight from tensor memory), then dS^T = P^T (dP^T - Delta) into
+//   shared memory (A operand of dK, and, read MN-major, of dQ)
+//   dV += P^T dO_i,   dK += dS^T Q_i,   dQ_i = dS K   (queries on lanes; R1 at D = 128)
+//   dQ_i leaves tensor memory at once: scaled, staged 32 columns at a time, and added into
+//   the fp32 accumulator with TMA bulk reduce-adds.
+// Tensor memory (512 columns): D = 128: [0,128) dV, [128,256) dK, [256,384) R0, [384,512) R1
+// (dQ reuses R1 once dP^T has been read); D = 64: dV, dK 64 each, R0 and R1 128 each, dQ 64.
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 UMMA issuer and TMEM owner, warps 2..5
+// elementwise work and dQ readout (thread j owns key row j, or query row j for dQ).
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kB = 128;  // query tile = key tile = 128 rows
+constexpr int kThreads = 192;
+constexpr uint32_t kSub = 16384;  // 128 rows x 64 bf16, 128-byte swizzle
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct SmallCfg {
+    static constexpr int NSUB = D / 64;                   // 64-column sub-tiles of a [128 x D] tile
+    static constexpr uint32_t kTile = NSUB * kSub;        // one Q or dO tile = one ring slot
+    static constexpr int kStages = D == 128 ? 3 : 8;
+    static constexpr bool ALIAS = D == 128;               // dQ reuses R1
+    static constexpr uint32_t kOffK = 0;                  // K tile, resident
+    static constexpr uint32_t kOffV = kOffK + kTile;      // V tile, resident
+    static constexpr uint32_t kOffDS = kOffV + kTile;     // dS^T [128 keys x 128 queries] bf16
+    static constexpr uint32_t kOffStage = kOffDS + 2 * kSub;  // dQ staging, 2 x (128 rows x 32 fp32)
+    static constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
+    static constexpr uint32_t kOffBar = kOffRing + kStages * kTile;
+    static constexpr uint32_t kSmem = kOffBar + 512 + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct SmallArgs {
+    const float* lse;
+    const float* delta;
+    uint16_t *dK, *dV;
+    const int32_t* cu_seqlens;
+    unsigned* status;
+    int Hq, Hkv, S, window, T;
+    float scale, scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_small_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                     const __grid_constant__ CUtensorMap tdq, SmallArgs a) {
+    using C = SmallCfg<D>;
+    const int g = blockIdx.x;  // KV head
+    const int seq = blockIdx.y;
+    const int kv_tile = blockIdx.z;  // tile 0 sees the most queries: launched first
+    int seq_start = 0, L = a.S, bcoord = seq;
+    if (a.cu_seqlens) {
+        seq_start = a.cu_seqlens[seq];
+        L = a.cu_seqlens[seq + 1] - seq_start;
+        bcoord = 0;
+    }
+    const int k0 = kv_tile * kB;
+    if (k0 >= L) return;  // uniform: before any barrier or TMEM use
+    const int G = a.Hq / a.Hkv;
+    const int q_last = a.window > 0 ? min(L, k0 + kB - 1 + a.window) : L;  // exclusive bound on queries
+    const int i_begin = k0 / kB, i_end = (q_last + kB - 1) / kB;
+    const int n_qt = i_end - i_begin;
+    const int n = G * n_qt;  // steps: (head, query tile)
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sK = sbase + C::kOffK, sV = sbase + C::kOffV, sDS = sbase + C::kOffDS;
+    const uint32_t sStage = sbase + C::kOffStage, sRing = sbase + C::kOffRing;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint64_t* full = bars;                      // [kStages]
+    uint64_t* empty = bars + C::kStages;        // [kStages]
+    uint64_t* kv_full = bars + 2 * C::kStages;  // K and V resident
+    uint64_t* s_full = kv_full + 1;             // S^T(t) in R0
+    uint64_t* dp_full = s_full + 1;             // dP^T(t) in R1
+    uint64_t* p_full = dp_full + 1;             // P^T(t) written over R0 (128 threads)
+    uint64_t* ds_full = p_full + 1;             // dS^T(t) in shared memory, dP^T(t) read (128 threads)
+    uint64_t* ds_free = ds_full + 1;            // dK(t) and dQ(t) have read dS^T(t)
+    uint64_t* dq_full = ds_free + 1;            // dQ(t) in tensor memory
+    uint64_t* dq_free = dq_full + 1;            // dQ(t) read out (128 threads)
+    uint64_t* mma_idle = dq_free + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(kv_full), 1);
+        mbar_init(smem_u32(s_full), 1);
+        mbar_init(smem_u32(dp_full), 1);
+        mbar_init(smem_u32(p_full), 128);
+        mbar_init(smem_u32(ds_full), 128);
+        mbar_init(smem_u32(ds_free), 1);
+        mbar_init(smem_u32(dq_full), 1);
+        mbar_init(smem_u32(dq_free), 128);
+        mbar_init(smem_u32(mma_idle), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+    const uint32_t tDV = tbase, tDK = tbase + D, tR0 = tbase + 2 * D, tR1 = tR0 + 128;
+    const uint32_t tDQ = C::ALIAS ? tR1 : tR1 + 128;
+    const int krow = seq_start + k0;
+
+    if (warp == 0) {
+        // ---------------------------------- producer -------------------------------------
+        if (lane == 0) {
+            prefetch_tmap(&tq);
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            prefetch_tmap(&tdo);
+            mbar_expect_tx(smem_u32(kv_full), 2 * C::kTile);
+            for (int u = 0; u < C::NSUB; ++u) {
+                tma_load_4d(sK + u * kSub, &tk, smem_u32(kv_full), 64 * u, g, krow, bcoord);
+                tma_load_4d(sV + u * kSub, &tv, smem_u32(kv_full), 64 * u, g, krow, bcoord);
+            }
+            int slot = 0, round = 0;
+            bool ok = true;
+            auto load_tile = [&](const CUtensorMap* map, int h, int qrow) -> bool {
+                if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x41))
+                    return false;
+                const uint32_t fb = smem_u32(&full[slot]);
+                mbar_expect_tx(fb, C::kTile);
+                const uint32_t dst = sRing + slot * C::kTile;
+                for (int u = 0; u < C::NSUB; ++u) tma_load_4d(dst + u * kSub, map, fb, 64 * u, h, qrow, bcoord);
+                if (++slot == C::kStages) slot = 0, ++round;
+                return true;
+            };
+            // consumption order of the UMMA issuer: Q(0) dO(0) Q(1) dO(1) ...
+            for (int t = 0; ok && t < n; ++t) {
+                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
+                ok = load_tile(&tq, h, qrow) && load_tile(&tdo, h, qrow);
+            }
+            const int issued = round * C::kStages + slot;
+            for (int s = 0; s < C::kStages && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x47);
+            }
+            mbar_drain(smem_u32(kv_full), 0, a.status, 0x4e);
+        }
+    } else if (warp == 1) {
+        // --------------------------------- UMMA issuer -----------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // K x Q^T: both K-major
+            constexpr uint32_t idG = idesc_bf16_f32(128, D, false, true);     // P^T / dS^T x (dO | Q) N-major
+            constexpr uint32_t idQ = idesc_bf16_f32(128, D, true, true);      // dS (MN-major) x K (N-major)
+            int slot = 0, round = 0;
+            auto acquire = [&](int& s) -> bool {
+                if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x42)) return false;
+                tc_fence_after();
+                s = slot;
+                if (++slot == C::kStages) slot = 0, ++round;
+                return true;
+            };
+            // acc(128 x 128) = X (resident [keys x D], K-major) x Y^T (ring tile [queries x D], K-major)
+            auto rows_x_tile = [&](uint32_t dacc, uint32_t x, int ys) {
+                const uint32_t y = sRing + ys * C::kTile;
+                for (int u = 0; u < C::NSUB; ++u)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ss(dacc, sdesc_sw128(x + u * kSub + kk * 32, 16, 1024),
+                                     sdesc_sw128(y + u * kSub + kk * 32, 16, 1024), idS, (u | kk) ? 1u : 0u);
+            };
+            bool ok = mbar_wait(smem_u32(kv_full), 0, abort_flag, a.status, 0x43);
+            tc_fence_after();
+            int qs = 0, ds = 0;  // ring slots of this step's Q and dO tiles
+            if (ok) ok = acquire(qs);
+            if (ok) {
+                rows_x_tile(tR0, sK, qs);  // S^T(0)
+                umma_commit(smem_u32(s_full));
+            }
+            if (ok) ok = acquire(ds);
+            if (ok) {
+                rows_x_tile(tR1, sV, ds);  // dP^T(0)
+                umma_commit(smem_u32(dp_full));
+            }
+            for (int t = 0; ok && t < n; ++t) {
+                // dV += P^T dO: A = P^T (bf16, packed over R0's first 64 columns), B = dO (N-major)
+                ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x44);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t dob = sRing + ds * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ts(tDV, tR0 + kk * 8, sdesc_sw128(dob + kk * 2048, kSub, 1024), idG,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&empty[ds]));
+                const int qs_t = qs;
+                // S^T(t+1) over R0: issued after the P V read of R0 (the MMA pipe runs in order)
+                if (t + 1 < n) {
+                    ok = acquire(qs);
+                    if (!ok) break;
+                    rows_x_tile(tR0, sK, qs);
+                    umma_commit(smem_u32(s_full));
+                }
+                // dK += dS^T Q: A = dS^T (K-major, shared memory), B = Q (N-major)
+                ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x45);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t qb = sRing + qs_t * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(qb + kk * 2048, kSub, 1024), idG, (t > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&empty[qs_t]));
+                // dQ(t) = dS K: A = dS^T read MN-major (queries contiguous), B = K (N-major)
+                if (!C::ALIAS && t > 0) {  // its own columns: the previous dQ has been read out
+                    ok = mbar_wait(smem_u32(dq_free), (t - 1) & 1, abort_flag, a.status, 0x46);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024), sdesc_sw128(sK + kk * 2048, kSub, 1024),
+                                 idQ, kk > 0 ? 1u : 0u);
+                umma_commit(smem_u32(dq_full));
+                umma_commit(smem_u32(ds_free));
+                // dP^T(t+1) over R1 (at D = 128 once dQ(t) has left it)
+                if (t + 1 < n) {
+                    if (C::ALIAS) {
+                        ok = mbar_wait(smem_u32(dq_free), t & 1, abort_flag, a.status, 0x48);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    ok = acquire(ds);
+                    if (!ok) break;
+                    rows_x_tile(tR1, sV, ds);
+                    umma_commit(smem_u32(dp_full));
+                }
+            }
+            // every issued UMMA has finished before TMEM may be released
+            umma_commit(smem_u32(mma_idle));
+            mbar_drain(smem_u32(mma_idle), 0, a.status, 0x49);
+        }
+    } else {
+        // ------------------------- elementwise / dQ readout warps ----------------------------
+        const int quad = warp & 3;
+        const int j = quad * 32 + lane;  // TMEM lane: key row (S, dP, dV, dK) or query row (dQ)
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int kabs = k0 + j;
+        const bool key_ok = kabs < L;
+        bool ok = true;
+
+        // dQ(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory and add
+        // into the fp32 accumulator with TMA bulk reduce-adds
+        auto drain_dq = [&](int t) -> bool {
+            bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x4a));
+            tc_fence_after();
+            const int h = g * G + t / n_qt;
+            const int q0 = (i_begin + t % n_qt) * kB;
+            const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
+#pragma unroll 1
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                const uint32_t buf = sStage + (c4 & 1) * kSub;
+                if (tid == 64) bulk_wait_group_read1();  // the reduce that last read `buf` is done
+                named_bar_sync(2, 128);
+                if (w) {
+                    uint32_t rq[32];
+                    tmem_ld32(tDQ + c4 * 32 + lane_base, rq);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(buf + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 1]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 2]) * f),
+                                     __float_as_uint(__uint_as_float(rq[4 * ch + 3]) * f));
+                }
+                fence_proxy_async_smem();
+                w = named_bar_and(2, 128, w);
+                if (w && tid == 64) {
+                    tma_reduce_add_4d(&tdq, buf, 32 * c4, h, seq_start + q0, bcoord);
+                    bulk_commit_group();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(dq_free));
+            return w;
+        };
+
+        for (int t = 0; t < n; ++t) {
+            const int h = g * G + t / n_qt;
+            const int q0 = (i_begin + t % n_qt) * kB;
+            // lse (log2 units; +inf past the end -> P = 0) and Delta of the tile's queries: lane l
+            // holds queries q0 + 32 i + l; columns are broadcast with shuffles
+            float lreg[4], dreg[4];
+            {
+                const size_t lbase = a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int qa = q0 + 32 * i + lane;
+                    lreg[i] = qa < L ? a.lse[lbase + qa] * kLog2e : INFINITY;
+                    dreg[i] = qa < L ? a.delta[lbase + qa] : 0.f;
+                }
+            }
+            // ---- P^T = exp2(S^T * scale * log2 e - lse2), written back over R0 as bf16 ----
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full), t & 1, abort_flag, a.status, 0x4b));
+            uint32_t pk[64];
+            if (ok) {
+                tc_fence_after();
+                uint32_t rr[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t tmp[32];
+                    tmem_ld32(tR0 + c * 32 + lane_base, tmp);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
+                }
+                tmem_ld_wait();
+                const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) &&
+                                    q0 + kB <= L && k0 + kB <= L);
+                // on edge tiles key j sees the queries qa with 0 <= qa - kabs < span
+                int qhi = key_ok ? L : kabs;
+                if (a.window > 0) qhi = min(qhi, kabs + a.window);
+                const unsigned span = qhi > kabs ? (unsigned)(qhi - kabs) : 0u;
+                auto p_row = [&](auto masked) {
+#pragma unroll
+                    for (int c = 0; c < 128; c += 2) {
+                        float p[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const float lv = __shfl_sync(0xffffffffu, lreg[(c + u) >> 5], (c + u) & 31);
+                            p[u] = fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv));
+                            if (decltype(masked)::value && (unsigned)(q0 + c + u - kabs) >= span) p[u] = 0.f;
+                        }
+                        pk[c / 2] = pack_bf16x2(p[0], p[1]);
+                    }
+                };
+                if (edge) p_row(std::true_type{});
+                else p_row(std::false_type{});
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) w[e] = pk[e];
+                tmem_st32(tR0 + lane_base, w);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) w[e] = pk[32 + e];
+                tmem_st32(tR0 + 32 + lane_base, w);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(smem_u32(p_full));
+            }
+            // ---- dS^T = P^T (dP^T - Delta) -> shared memory ----------------------------------
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x4c));
+            if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x4d));
+            if (ok) {
+                tc_fence_after();
+                uint32_t rr[128];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t tmp[32];
+                    tmem_ld32(tR1 + c * 32 + lane_base, tmp);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int st = 0; st < 2; ++st) {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t out[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = st * 64 + ch * 8 + 2 * e;
+                            const uint32_t pw = pk[c / 2];
+                            const float d0 = __shfl_sync(0xffffffffu, dreg[c >> 5], c & 31);
+                            const float d1 = __shfl_sync(0xffffffffu, dreg[(c + 1) >> 5], (c + 1) & 31);
+                            out[e] = pack_bf16x2(__uint_as_float(pw << 16) * (__uint_as_float(rr[c]) - d0),
+                                                 __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(rr[c + 1]) - d1));
+                        }
+                        st_shared_v4(sDS + st * kSub + sw128_offset(j, ch * 8), out[0], out[1], out[2], out[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(smem_u32(ds_full));
+            }
+            if (ok) ok = drain_dq(t);
+            ok = named_bar_and(3, 128, ok);
+            if (!ok) break;
+        }
+        if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
+        // ---- epilogue: dV, dK rows (keys on lanes) -> bf16 ------------------------------------
+        // dq_full of the last step implies every earlier UMMA (all dV/dK updates) is done.
+        tc_fence_after();
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {  // warp-uniform: the TMEM loads below are warp collectives
+            const size_t row = (size_t)(a.cu_seqlens ? seq_start + kabs : seq * a.S + kabs) * a.Hkv + g;
+            uint16_t* dv_row = a.dV + row * D;
+            uint16_t* dk_row = a.dK + row * D;
+#pragma unroll 1
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t rv[32], rk[32];
+                tmem_ld32(tDV + c4 * 32 + lane_base, rv);
+                tmem_ld32(tDK + c4 * 32 + lane_base, rk);
+                tmem_ld_wait();
+                if (key_ok) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 wv, wk;
+                        wv.x = pack_bf16x2(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]));
+                        wv.y = pack_bf16x2(__uint_as_float(rv[e + 2]), __uint_as_float(rv[e + 3]));
+                        wv.z = pack_bf16x2(__uint_as_float(rv[e + 4]), __uint_as_float(rv[e + 5]));
+                        wv.w = pack_bf16x2(__uint_as_float(rv[e + 6]), __uint_as_float(rv[e + 7]));
+                        wk.x = pack_bf16x2(__uint_as_float(rk[e]) * a.scale, __uint_as_float(rk[e + 1]) * a.scale);
+                        wk.y = pack_bf16x2(__uint_as_float(rk[e + 2]) * a.scale, __uint_as_float(rk[e + 3]) * a.scale);
+                        wk.z = pack_bf16x2(__uint_as_float(rk[e + 4]) * a.scale, __uint_as_float(rk[e + 5]) * a.scale);
+                        wk.w = pack_bf16x2(__uint_as_float(rk[e + 6]) * a.scale, __uint_as_float(rk[e + 7]) * a.scale);
+                        *reinterpret_cast<uint4*>(dv_row + c4 * 32 + e) = wv;
+                        *reinterpret_cast<uint4*>(dk_row + c4 * 32 + e) = wk;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace
+
+template <int D>
+cudaError_t launch_bwd_small_main(const BwdLaunch& L, cudaStream_t stream) {
+    SmallArgs a;
+    a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV;
+    a.cu_seqlens = L.cu_seqlens, a.status = L.status;
+    a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.window = L.window, a.T = L.total_rows;
+    a.scale = L.scale, a.scale_log2 = L.scale * kLog2e;
+    constexpr uint32_t kSmem = SmallCfg<D>::kSmem;
+    cudaError_t e = cudaFuncSetAttribute(bwd_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(L.Hkv, L.nseq, (L.S + kB - 1) / kB);
+    const ProfMark m = prof_begin(stream, D == 128 ? "bwd_main_d128" : "bwd_main_d64");
+    bwd_small_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+    prof_end(stream, m);
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_bwd_small_main<64>(const BwdLaunch&, cudaStream_t);
+template cudaError_t launch_bwd_small_main<128>(const BwdLaunch&, cudaStream_t);
+
+}  // namespace attn

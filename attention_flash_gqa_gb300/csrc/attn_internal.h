@@ -79,6 +79,9 @@ struct BwdLaunch {
     float scale;
 };
 cudaError_t launch_bwd(const BwdLaunch& L, cudaStream_t stream);
+// main kernel of the backward at D = 64 / 128 (one CTA per key tile; attn_bwd_small.cu)
+template <int D>
+cudaError_t launch_bwd_small_main(const BwdLaunch& L, cudaStream_t stream);
 
 // ---- merge of attention results over disjoint key sets -----------------------------------
 struct MergeLaunch {

@@ -112,7 +112,7 @@ def test_bwd_argument_checks(lib):
     assert call(wsb=need - 1) == WORKSPACE
     assert call(ws=P(256 * 4096 + 16)) == MISALIGNED
     assert call(cu=P(A), B=2, nseq=1, maxlen=300) == INVALID  # packed layout wants B == 1
-    assert call(D=128) == UNSUPPORTED
+    assert call(D=96) == UNSUPPORTED
     assert call(B=0) == OK
 
 

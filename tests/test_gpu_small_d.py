@@ -60,3 +60,43 @@ def test_prefill_paged_small_d(orc, D, window):
     ro, rl = orc.prefill_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.cu_q, pp.scale, window)
     check("o", to_np(o), ro)
     check_lse("lse", to_np(lse), rl)
+
+
+def _bwd_dense(orc, p):
+    q, k, v, do = to_dev(p.q), to_dev(p.k), to_dev(p.v), to_dev(p.do)
+    o, lse = attn.attn_fwd(q, k, v, window=p.window, scale=p.scale)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, lse, do, window=p.window, scale=p.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    rdq, rdk, rdv, *_ = orc.bwd(p.q, p.k, p.v, p.do, p.scale, 1, p.window)
+    check("dq", to_np(dq), rdq)
+    check("dk", to_np(dk), rdk)
+    check("dv", to_np(dv), rdv)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("B,Hq,Hkv,S,W", [(2, 4, 2, 300, 0), (1, 8, 1, 385, 0), (1, 6, 2, 129, 0), (2, 4, 4, 700, 129),
+                                          (1, 2, 1, 1, 0), (1, 4, 1, 513, 1), (1, 4, 2, 640, 300)])
+def test_backward_small_d(orc, D, B, Hq, Hkv, S, W):
+    _bwd_dense(orc, synth.dense(B, Hq, Hkv, S, D, W, seed=S + D + W + 1))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_small_d_outliers(orc, D):
+    """Scaled outliers in q and k (1 % of entries x 30, as in the window workload): finite, in tolerance."""
+    _bwd_dense(orc, synth.dense(1, 4, 2, 520, D, 256, seed=D, outlier_frac=0.01, outlier_scale=30.0))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_small_d_varlen(orc, D):
+    vp = synth.varlen_from_lengths([1, 127, 128, 129, 300, 0, 513], 8, 2, D, seed=D + 5)
+    q, k, v, do = to_dev(vp.q), to_dev(vp.k), to_dev(vp.v), to_dev(vp.do)
+    cu = torch.from_numpy(vp.cu_seqlens).cuda()
+    o, lse = attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, scale=vp.scale)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, lse, do, scale=vp.scale, cu_seqlens=cu, max_seqlen=vp.max_seqlen)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    rdq, rdk, rdv, *_ = orc.bwd_varlen(vp.q, vp.k, vp.v, vp.do, vp.cu_seqlens, vp.scale)
+    check("dq", to_np(dq), rdq)
+    check("dk", to_np(dk), rdk)
+    check("dv", to_np(dv), rdv)
