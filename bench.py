@@ -369,7 +369,8 @@ def finish(args, rank, world, p, attn, value, ms_step_max, roofline, e2e, launch
 
 
 def bench_extra(args, attn, synth, peaks, peak_src, clocks):
-    """Sliding-window d256 fwd+bwd, varlen d512 fwd+bwd, paged-cache chunked prefill d512 (forward),
+    """Sliding-window d256 fwd+bwd, head_dim 128 / 64 fwd+bwd, varlen d512 fwd+bwd, paged-cache chunked
+    prefill d512 (forward),
     merge of results over disjoint key sets (GB/s), paged decode d128 and sliding-window d256 (GB/s)."""
     import numpy as np
     import torch
@@ -432,6 +433,25 @@ def bench_extra(args, attn, synth, peaks, peak_src, clocks):
                              "frac_of_bf16_peak_sustained": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
                              "all_grads_finite": fin, "kernel_ms": kern_ms}
     del q, k, v, do, o, lse, dq, dk, dv
+
+    # head_dim 128 and 64 (Qwen3-class heads), dense causal fwd+bwd
+    for name, make in (("dense_d128_causal", synth.dense_d128_causal), ("dense_d64_causal", synth.dense_d64_causal)):
+        p = make(seed=7)
+        q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        sd_step = lambda: (attn.attn_fwd(q, k, v, o, lse, scale=p.scale),
+                           attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=p.scale))
+        ms = timed(sd_step, steps)
+        kern_ms = per_kernel(sd_step)
+        fl = 14 * p.D * pairs_causal(p.S) * p.B * p.Hq
+        fin = all(bool(torch.isfinite(t.float()).all()) for t in (o, dq, dk, dv))
+        res[name] = {"value": fl / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+                     "frac_of_bf16_peak_sustained": fl / (ms * 1e-3) / 1e12 / peaks["bf16_tflops_sustained"],
+                     "shape": {"B": p.B, "Hq": p.Hq, "Hkv": p.Hkv, "S": p.S, "D": p.D}, "all_finite": fin,
+                     "kernel_ms": kern_ms}
+        del q, k, v, do, o, lse, dq, dk, dv
 
     # varlen d512
     vp = synth.varlen_d512_causal(seed=7)

@@ -335,6 +335,16 @@ def swa_d256_w1024(seed=0, with_do=True) -> Dense:
                  name="swa_d256_w1024", with_do=with_do)
 
 
+def dense_d128_causal(seed=0, with_do=True) -> Dense:
+    """Qwen3-class heads (head_dim 128, 32 query heads over 8 KV heads) at the dense workload's
+    batch and length."""
+    return dense(2, 32, 8, 4096, 128, 0, seed, name="dense_d128_causal", with_do=with_do)
+
+
+def dense_d64_causal(seed=0, with_do=True) -> Dense:
+    return dense(2, 32, 8, 4096, 64, 0, seed, name="dense_d64_causal", with_do=with_do)
+
+
 def varlen_d512_causal(seed=0, with_do=True) -> Varlen:
     return varlen(8, 512, 4096, 32, 4, 512, 0, seed, name="varlen_d512_causal", with_do=with_do)
 
