@@ -24,8 +24,13 @@
 //   the fp32 accumulator with TMA bulk reduce-adds.
 // Tensor memory (512 columns): D = 128: [0,128) dV, [128,256) dK, [256,384) R0, [384,512) R1
 // (dQ reuses R1 once dP^T has been read); D = 64: dV, dK 64 each, R0 and R1 128 each, dQ 64.
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 UMMA issuer and TMEM owner, warps 2..5
-// elementwise work and dQ readout (thread j owns key row j, or query row j for dQ).
+// Warp roles (448 threads): warps 0..7 elementwise work (two warps per key row quarter, one per
+// half of the 128 score columns, 32 columns at a time; the step's lse and Delta vectors are
+// staged in shared memory and read 4 at a time), warps 8..11 read dQ out (thread j owns query
+// row j) so the elementwise warps go on to the next step meanwhile, warp 12 TMA producer, warp 13
+// UMMA issuer and TMEM owner. The issuer computes dQ before dK, so the readout starts while dK
+// runs. Each half of the score columns keeps its P^T (bf16 pairs) in the first 32 columns of its
+// own half of R0.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -37,7 +42,11 @@ namespace attn {
 namespace {
 
 constexpr int kB = 128;  // query tile = key tile = 128 rows
-constexpr int kThreads = 192;
+// warps 0..7 elementwise (TMEM lane quarter = warp % 4, score-column half = warp / 4), 8..11 dQ
+// readout, 12 TMA producer, 13 UMMA issuer
+constexpr int kDrainWarp0 = 8, kProducerWarp = 12, kMmaWarp = 13;
+constexpr int kThreads = 448;
+constexpr int kEw = 256;  // elementwise threads
 constexpr uint32_t kSub = 16384;  // 128 rows x 64 bf16, 128-byte swizzle
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -52,7 +61,8 @@ struct SmallCfg {
     static constexpr uint32_t kOffDS = kOffV + kTile;     // dS^T [128 keys x 128 queries] bf16
     static constexpr uint32_t kOffStage = kOffDS + 2 * kSub;  // dQ staging, 2 x (128 rows x 32 fp32)
     static constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
-    static constexpr uint32_t kOffBar = kOffRing + kStages * kTile;
+    static constexpr uint32_t kOffVec = kOffRing + kStages * kTile;  // step's lse2[128], Delta[128]
+    static constexpr uint32_t kOffBar = kOffVec + 1024;
     static constexpr uint32_t kSmem = kOffBar + 512 + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -119,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(kv_full), 1);
         mbar_init(smem_u32(s_full), 1);
         mbar_init(smem_u32(dp_full), 1);
-        mbar_init(smem_u32(p_full), 128);
-        mbar_init(smem_u32(ds_full), 128);
+        mbar_init(smem_u32(p_full), kEw);
+        mbar_init(smem_u32(ds_full), kEw);
         mbar_init(smem_u32(ds_free), 1);
         mbar_init(smem_u32(dq_full), 1);
         mbar_init(smem_u32(dq_free), 128);
@@ -128,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -138,8 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDV = tbase, tDK = tbase + D, tR0 = tbase + 2 * D, tR1 = tR0 + 128;
     const uint32_t tDQ = C::ALIAS ? tR1 : tR1 + 128;
     const int krow = seq_start + k0;
+    // TMEM lanes a warp may access: 32 * (warp % 4) ..
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int j = (warp & 3) * 32 + lane;  // key row (S, dP, dV, dK) or query row (dQ)
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ---------------------------------- producer -------------------------------------
         if (lane == 0) {
             prefetch_tmap(&tq);
@@ -175,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_drain(smem_u32(kv_full), 0, a.status, 0x4e);
         }
-    } else if (warp == 1) {
+    } else if (warp == kMmaWarp) {
         // --------------------------------- UMMA issuer -----------------------------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // K x Q^T: both K-major
@@ -212,15 +225,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 umma_commit(smem_u32(dp_full));
             }
             for (int t = 0; ok && t < n; ++t) {
-                // dV += P^T dO: A = P^T (bf16, packed over R0's first 64 columns), B = dO (N-major)
+                // dV += P^T dO: A = P^T (bf16 pairs over R0), B = dO (N-major)
                 ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x44);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t dob = sRing + ds * C::kTile;
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_ts(tDV, tR0 + kk * 8, sdesc_sw128(dob + kk * 2048, kSub, 1024), idG,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk)  // queries 64h .. 64h+63 of P^T sit at R0 columns 64h .. 64h+31
+                    umma_bf16_ts(tDV, tR0 + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dob + kk * 2048, kSub, 1024),
+                                 idG, (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(smem_u32(&empty[ds]));
                 const int qs_t = qs;
                 // S^T(t+1) over R0: issued after the P V read of R0 (the MMA pipe runs in order)
@@ -230,17 +243,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rows_x_tile(tR0, sK, qs);
                     umma_commit(smem_u32(s_full));
                 }
-                // dK += dS^T Q: A = dS^T (K-major, shared memory), B = Q (N-major)
                 ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x45);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t qb = sRing + qs_t * C::kTile;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(qb + kk * 2048, kSub, 1024), idG, (t > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&empty[qs_t]));
-                // dQ(t) = dS K: A = dS^T read MN-major (queries contiguous), B = K (N-major)
+                // dQ(t) = dS K first, so its readout starts while dK(t) runs: A = dS^T read MN-major
+                // (queries contiguous), B = K (N-major)
                 if (!C::ALIAS && t > 0) {  // its own columns: the previous dQ has been read out
                     ok = mbar_wait(smem_u32(dq_free), (t - 1) & 1, abort_flag, a.status, 0x46);
                     if (!ok) break;
@@ -251,6 +258,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024), sdesc_sw128(sK + kk * 2048, kSub, 1024),
                                  idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
+                // dK += dS^T Q: A = dS^T (K-major, shared memory), B = Q (N-major)
+                const uint32_t qb = sRing + qs_t * C::kTile;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(qb + kk * 2048, kSub, 1024), idG, (t > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&empty[qs_t]));
                 umma_commit(smem_u32(ds_free));
                 // dP^T(t+1) over R1 (at D = 128 once dQ(t) has left it)
                 if (t + 1 < n) {
@@ -269,163 +283,176 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(smem_u32(mma_idle));
             mbar_drain(smem_u32(mma_idle), 0, a.status, 0x49);
         }
-    } else {
-        // ------------------------- elementwise / dQ readout warps ----------------------------
-        const int quad = warp & 3;
-        const int j = quad * 32 + lane;  // TMEM lane: key row (S, dP, dV, dK) or query row (dQ)
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int kabs = k0 + j;
-        const bool key_ok = kabs < L;
-        bool ok = true;
-
+    } else if (warp >= kDrainWarp0) {
+        // ------------------------------ dQ readout warps -----------------------------------
         // dQ(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory and add
         // into the fp32 accumulator with TMA bulk reduce-adds
-        auto drain_dq = [&](int t) -> bool {
-            bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x4a));
+        const bool leader = warp == kDrainWarp0 && lane == 0;
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x4a));
             tc_fence_after();
             const int h = g * G + t / n_qt;
             const int q0 = (i_begin + t % n_qt) * kB;
             const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
-#pragma unroll 1
+            // the whole row into registers first, so dQ's columns are handed back at once (at
+            // D = 128 the next dP^T waits for them)
+            uint32_t rq[D];
+            if (ok) {
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                    uint32_t tmp[32];
+                    tmem_ld32(tDQ + c4 * 32 + lane_base, tmp);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) rq[c4 * 32 + e] = tmp[e];
+                }
+                tmem_ld_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(dq_free));
+#pragma unroll
             for (int c4 = 0; c4 < D / 32; ++c4) {
                 const uint32_t buf = sStage + (c4 & 1) * kSub;
-                if (tid == 64) bulk_wait_group_read1();  // the reduce that last read `buf` is done
+                if (leader) bulk_wait_group_read1();  // the reduce that last read `buf` is done
                 named_bar_sync(2, 128);
-                if (w) {
-                    uint32_t rq[32];
-                    tmem_ld32(tDQ + c4 * 32 + lane_base, rq);
-                    tmem_ld_wait();
+                if (ok) {
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch)
                         st_shared_v4(buf + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4),
-                                     __float_as_uint(__uint_as_float(rq[4 * ch]) * f),
-                                     __float_as_uint(__uint_as_float(rq[4 * ch + 1]) * f),
-                                     __float_as_uint(__uint_as_float(rq[4 * ch + 2]) * f),
-                                     __float_as_uint(__uint_as_float(rq[4 * ch + 3]) * f));
+                                     __float_as_uint(__uint_as_float(rq[c4 * 32 + 4 * ch]) * f),
+                                     __float_as_uint(__uint_as_float(rq[c4 * 32 + 4 * ch + 1]) * f),
+                                     __float_as_uint(__uint_as_float(rq[c4 * 32 + 4 * ch + 2]) * f),
+                                     __float_as_uint(__uint_as_float(rq[c4 * 32 + 4 * ch + 3]) * f));
                 }
                 fence_proxy_async_smem();
-                w = named_bar_and(2, 128, w);
-                if (w && tid == 64) {
+                ok = named_bar_and(2, 128, ok);
+                if (ok && leader) {
                     tma_reduce_add_4d(&tdq, buf, 32 * c4, h, seq_start + q0, bcoord);
                     bulk_commit_group();
                 }
             }
-            tc_fence_before();
-            mbar_arrive(smem_u32(dq_free));
-            return w;
-        };
-
-        for (int t = 0; t < n; ++t) {
+            if (!ok) break;
+        }
+        if (leader) bulk_wait_group0();  // every reduce issued by this CTA has landed
+    } else {
+        // --------------------------- elementwise warps (0..7) --------------------------------
+        // warp w: key rows 32 (w % 4) .., score columns (queries) 64 hf .. 64 hf + 63, hf = w / 4
+        const int hf = warp >> 2;
+        const int kabs = k0 + j;
+        const bool key_ok = kabs < L;
+        float* vec = reinterpret_cast<float*>(smem + C::kOffVec);  // [0,128) lse2, [128,256) Delta
+        bool ok = true;
+        // this thread's element of the step's lse / Delta vector, loaded a step ahead
+        auto fetch = [&](int t) -> float {
+            if (t >= n) return 0.f;
             const int h = g * G + t / n_qt;
+            const int qa = (i_begin + t % n_qt) * kB + (tid & 127);
+            const size_t lbase = a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S;
+            if (tid < 128) return qa < L ? a.lse[lbase + qa] * kLog2e : INFINITY;  // +inf: P = 0 past the end
+            return qa < L ? a.delta[lbase + qa] : 0.f;
+        };
+        float vnext = fetch(0);
+        for (int t = 0; t < n; ++t) {
             const int q0 = (i_begin + t % n_qt) * kB;
-            // lse (log2 units; +inf past the end -> P = 0) and Delta of the tile's queries: lane l
-            // holds queries q0 + 32 i + l; columns are broadcast with shuffles
-            float lreg[4], dreg[4];
-            {
-                const size_t lbase = a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int qa = q0 + 32 * i + lane;
-                    lreg[i] = qa < L ? a.lse[lbase + qa] * kLog2e : INFINITY;
-                    dreg[i] = qa < L ? a.delta[lbase + qa] : 0.f;
-                }
-            }
+            vec[tid] = vnext;
+            vnext = fetch(t + 1);
+            named_bar_sync(3, kEw);
             // ---- P^T = exp2(S^T * scale * log2 e - lse2), written back over R0 as bf16 ----
+            // 32 score columns at a time; this half's P columns [64 hf + 16c, +16) overwrite
+            // scores of its own first chunk, already read
             ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(s_full), t & 1, abort_flag, a.status, 0x4b));
-            uint32_t pk[64];
+            uint32_t pk[32];
             if (ok) {
                 tc_fence_after();
-                uint32_t rr[128];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t tmp[32];
-                    tmem_ld32(tR0 + c * 32 + lane_base, tmp);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
-                }
-                tmem_ld_wait();
                 const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) &&
                                     q0 + kB <= L && k0 + kB <= L);
                 // on edge tiles key j sees the queries qa with 0 <= qa - kabs < span
                 int qhi = key_ok ? L : kabs;
                 if (a.window > 0) qhi = min(qhi, kabs + a.window);
                 const unsigned span = qhi > kabs ? (unsigned)(qhi - kabs) : 0u;
-                auto p_row = [&](auto masked) {
 #pragma unroll
-                    for (int c = 0; c < 128; c += 2) {
-                        float p[2];
+                for (int c = 0; c < 2; ++c) {
+                    const int col0 = 64 * hf + 32 * c;  // first query column of the chunk
+                    uint32_t rr[32];
+                    tmem_ld32(tR0 + col0 + lane_base, rr);
+                    tmem_ld_wait();
+                    auto p_chunk = [&](auto masked) {
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float lv = __shfl_sync(0xffffffffu, lreg[(c + u) >> 5], (c + u) & 31);
-                            p[u] = fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv));
-                            if (decltype(masked)::value && (unsigned)(q0 + c + u - kabs) >= span) p[u] = 0.f;
+                        for (int e = 0; e < 32; e += 4) {
+                            const float4 lv = *reinterpret_cast<const float4*>(vec + col0 + e);
+                            const float lvs[4] = {lv.x, lv.y, lv.z, lv.w};
+                            float p[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                p[u] = fast_exp2(fmaf(__uint_as_float(rr[e + u]), a.scale_log2, -lvs[u]));
+                                if (decltype(masked)::value && (unsigned)(q0 + col0 + e + u - kabs) >= span) p[u] = 0.f;
+                            }
+                            pk[16 * c + e / 2] = pack_bf16x2(p[0], p[1]);
+                            pk[16 * c + e / 2 + 1] = pack_bf16x2(p[2], p[3]);
                         }
-                        pk[c / 2] = pack_bf16x2(p[0], p[1]);
-                    }
-                };
-                if (edge) p_row(std::true_type{});
-                else p_row(std::false_type{});
-                uint32_t w[32];
+                    };
+                    if (edge) p_chunk(std::true_type{});
+                    else p_chunk(std::false_type{});
+                    uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pk[e];
-                tmem_st32(tR0 + lane_base, w);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pk[32 + e];
-                tmem_st32(tR0 + 32 + lane_base, w);
+                    for (int e = 0; e < 16; ++e) w[e] = pk[16 * c + e];
+                    tmem_st16(tR0 + 64 * hf + 16 * c + lane_base, w);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(smem_u32(p_full));
             }
-            // ---- dS^T = P^T (dP^T - Delta) -> shared memory ----------------------------------
+            // ---- dS^T = P^T (dP^T - Delta) -> shared memory (sub-tile hf), 32 columns at a time ----
             ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(dp_full), t & 1, abort_flag, a.status, 0x4c));
             if (ok && t > 0) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x4d));
             if (ok) {
                 tc_fence_after();
-                uint32_t rr[128];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t tmp[32];
-                    tmem_ld32(tR1 + c * 32 + lane_base, tmp);
+                for (int c = 0; c < 2; ++c) {
+                    const int col0 = 64 * hf + 32 * c;
+                    uint32_t rr[32];
+                    tmem_ld32(tR1 + col0 + lane_base, rr);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int st = 0; st < 2; ++st) {
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int ch = 0; ch < 4; ++ch) {  // 16-byte chunks: 8 queries each
+                        const float4 d0 = *reinterpret_cast<const float4*>(vec + 128 + col0 + 8 * ch);
+                        const float4 d1 = *reinterpret_cast<const float4*>(vec + 128 + col0 + 8 * ch + 4);
+                        const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
                         uint32_t out[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int c = st * 64 + ch * 8 + 2 * e;
-                            const uint32_t pw = pk[c / 2];
-                            const float d0 = __shfl_sync(0xffffffffu, dreg[c >> 5], c & 31);
-                            const float d1 = __shfl_sync(0xffffffffu, dreg[(c + 1) >> 5], (c + 1) & 31);
-                            out[e] = pack_bf16x2(__uint_as_float(pw << 16) * (__uint_as_float(rr[c]) - d0),
-                                                 __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(rr[c + 1]) - d1));
+                            const int cc = ch * 8 + 2 * e;  // column within the 32-column chunk
+                            const uint32_t pw = pk[16 * c + cc / 2];
+                            out[e] = pack_bf16x2(__uint_as_float(pw << 16) * (__uint_as_float(rr[cc]) - dv[2 * e]),
+                                                 __uint_as_float(pw & 0xffff0000u) * (__uint_as_float(rr[cc + 1]) - dv[2 * e + 1]));
                         }
-                        st_shared_v4(sDS + st * kSub + sw128_offset(j, ch * 8), out[0], out[1], out[2], out[3]);
+                        st_shared_v4(sDS + hf * kSub + sw128_offset(j, 32 * c + 8 * ch), out[0], out[1], out[2], out[3]);
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 mbar_arrive(smem_u32(ds_full));
             }
-            if (ok) ok = drain_dq(t);
-            ok = named_bar_and(3, 128, ok);
+            ok = named_bar_and(3, kEw, ok);  // also: every read of vec for this step is done
             if (!ok) break;
         }
-        if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
         // ---- epilogue: dV, dK rows (keys on lanes) -> bf16 ------------------------------------
-        // dq_full of the last step implies every earlier UMMA (all dV/dK updates) is done.
+        // the last step's dq_full (below) follows every dV / dK product of the CTA
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), (n - 1) & 1, abort_flag, a.status, 0x4f));
         tc_fence_after();
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {  // warp-uniform: the TMEM loads below are warp collectives
+            // dq_full(n-1) was committed after dQ(n-1) but before dK(n-1): wait for the idle
+            // commit of the UMMA issuer instead, which follows every product
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(mma_idle), 0, abort_flag, a.status, 0x50));
+            tc_fence_after();
+        }
+        if (ok) {
             const size_t row = (size_t)(a.cu_seqlens ? seq_start + kabs : seq * a.S + kabs) * a.Hkv + g;
             uint16_t* dv_row = a.dV + row * D;
             uint16_t* dk_row = a.dK + row * D;
 #pragma unroll 1
-            for (int c4 = 0; c4 < D / 32; ++c4) {
+            for (int c4 = hf; c4 < D / 32; c4 += 2) {  // the two warps of a lane quarter split the columns
                 uint32_t rv[32], rk[32];
                 tmem_ld32(tDV + c4 * 32 + lane_base, rv);
                 tmem_ld32(tDK + c4 * 32 + lane_base, rk);
@@ -451,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tbase, 512);
     }
