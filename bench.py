@@ -626,9 +626,12 @@ def bench_reference(args, rank, world):
 
 
 def profile_case(args):
-    """Run one workload's kernel W + K times and print its device time, for profiler captures
-    on a reduced case (no bench line). prefill_paged_d512: the first `--requests` requests of
-    the chunked-prefill workload."""
+    """Run one workload's kernels W + K times and print their device time, for profiler captures
+    on a reduced case (no bench line). Cases:
+      prefill_paged_d512: the first `--requests` requests of the chunked-prefill workload;
+      dense_d128: head_dim 128 forward + backward at batch `--batch`;
+      merge_cp8_d512: the 8-part merge;
+      decode_swa_d256: the sliding-window head_dim 256 decode."""
     import numpy as np
     import torch
 
@@ -637,27 +640,58 @@ def profile_case(args):
 
     attn.load_library()
     torch.cuda.set_device(0)
-    if args.profile_case != "prefill_paged_d512":
-        raise SystemExit(f"unknown profile case {args.profile_case}")
-    full = synth.prefill_paged_d512(seed=7)
-    n = max(1, min(args.requests, full.B))
-    pf = synth.prefill_paged_from_lengths(full.seq_lens[:n], full.q_lens[:n], full.Hq, full.Hkv, full.D, seed=7)
-    qp, kc, vc = to_dev(pf.q), to_dev(pf.k_cache), to_dev(pf.v_cache)
-    bt, sl, cu = (torch.from_numpy(x).cuda() for x in (pf.block_table, pf.seq_lens, pf.cu_q))
-    o = torch.empty_like(qp)
-    lse = torch.empty((pf.Hq, pf.total_q), dtype=torch.float32, device="cuda")
+    case = args.profile_case
+    extra = {}
+    if case == "prefill_paged_d512":
+        full = synth.prefill_paged_d512(seed=7)
+        n = max(1, min(args.requests, full.B))
+        pf = synth.prefill_paged_from_lengths(full.seq_lens[:n], full.q_lens[:n], full.Hq, full.Hkv, full.D, seed=7)
+        qp, kc, vc = to_dev(pf.q), to_dev(pf.k_cache), to_dev(pf.v_cache)
+        bt, sl, cu = (torch.from_numpy(x).cuda() for x in (pf.block_table, pf.seq_lens, pf.cu_q))
+        o = torch.empty_like(qp)
+        lse = torch.empty((pf.Hq, pf.total_q), dtype=torch.float32, device="cuda")
+        run = lambda: attn.attn_fwd_paged(qp, kc, vc, bt, sl, cu, pf.max_q, o, lse, scale=pf.scale)
+        outs = [o]
+        extra = {"requests": n, "seq_lens": [int(x) for x in pf.seq_lens]}
+    elif case == "dense_d128":
+        p = synth.dense(args.batch, 32, 8, 4096, 128, 0, seed=7)
+        q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        run = lambda: (attn.attn_fwd(q, k, v, o, lse, scale=p.scale),
+                       attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, scale=p.scale))
+        outs = [o, dq, dk, dv]
+        extra = {"B": p.B}
+    elif case == "merge_cp8_d512":
+        mg = synth.merge_cp8_d512(seed=7)
+        mo, ml = to_dev(mg.o_parts), torch.from_numpy(mg.lse_parts).cuda()
+        om = torch.empty(mo.shape[1:], dtype=torch.bfloat16, device="cuda")
+        lm = torch.empty(ml.shape[1:], dtype=torch.float32, device="cuda")
+        run = lambda: attn.attn_merge_lse(mo, ml, om, lm)
+        outs = [om]
+    elif case == "decode_swa_d256":
+        ps = synth.decode_paged_swa_d256(seed=7)
+        qs, kcs, vcs = to_dev(ps.q), to_dev(ps.k_cache), to_dev(ps.v_cache)
+        bts, sls = torch.from_numpy(ps.block_table).cuda(), torch.from_numpy(ps.seq_lens).cuda()
+        os_ = torch.empty_like(qs)
+        ls = torch.empty((ps.B, ps.Hq), dtype=torch.float32, device="cuda")
+        run = lambda: attn.attn_decode_paged(qs, kcs, vcs, bts, sls, os_, ls, scale=ps.scale, window=ps.window)
+        outs = [os_]
+    else:
+        raise SystemExit(f"unknown profile case {case}")
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
-        attn.attn_fwd_paged(qp, kc, vc, bt, sl, cu, pf.max_q, o, lse, scale=pf.scale)
+        run()
     torch.cuda.synchronize()
     ev0.record()
     for _ in range(args.steps):
-        attn.attn_fwd_paged(qp, kc, vc, bt, sl, cu, pf.max_q, o, lse, scale=pf.scale)
+        run()
     ev1.record()
     torch.cuda.synchronize()
-    ok = bool(torch.isfinite(o.float()).all()) and attn.attn_get_device_status() == 0
-    print(json.dumps({"profile_case": args.profile_case, "requests": n, "seq_lens": [int(x) for x in pf.seq_lens],
-                      "ms_per_call": ev0.elapsed_time(ev1) / args.steps, "ok": ok}), flush=True)
+    ok = all(bool(torch.isfinite(t.float()).all()) for t in outs) and attn.attn_get_device_status() == 0
+    print(json.dumps({"profile_case": case, **extra, "ms_per_call": ev0.elapsed_time(ev1) / args.steps, "ok": ok}),
+          flush=True)
     if not ok:
         raise SystemExit(1)
 
