@@ -35,8 +35,9 @@
  *  - Faults detected on the device (a page id outside the pool, a pipeline wait that
  *    exceeded its time limit) do not trap: the kernel records a flag and finishes,
  *    and attn_get_device_status() reports it.
- *  - Supported shapes: D in {256, 512} for prefill/backward (D = 128 for decode),
- *    Hq % Hkv == 0, causal = 1. bf16 values are passed as raw 16-bit patterns.
+ *  - Supported shapes: D in {64, 128, 256, 512} for prefill / backward, D in {128, 256} for
+ *    decode, D in {64, 128, 256, 512} for the merge; Hq % Hkv == 0, causal = 1. bf16 values
+ *    are passed as raw 16-bit patterns.
  */
 #ifndef ATTN_GB300_ATTN_H
 #define ATTN_GB300_ATTN_H
@@ -124,7 +125,8 @@ ATTN_API int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_
  *   as ATTN_ERR_DEVICE_BOUNDS by attn_get_device_status() (the bad request's rows are left
  *   unwritten; a bad page id is replaced by page 0). Cache slots past L_b in a request's
  *   last page are never used, whatever they hold.
- *   Supported: D in {256, 512}, page_size = 16, num_reqs <= 65535 / (D / 256). No workspace.
+ *   Supported: D in {64, 128, 256, 512}, page_size = 16, num_reqs <= 65535 / max(1, D / 256).
+ *   No workspace.
  *   With num_reqs, total_q or max_q_len zero there is nothing to compute: the call checks
  *   its scalar arguments and returns ATTN_OK, and the pointers may then be NULL.
  */

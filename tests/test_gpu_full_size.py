@@ -1,4 +1,5 @@
-"""The five workloads at full size, in the launch configuration the benchmark times.
+"""The benchmarked workloads at full size, in the launch configuration the benchmark times, and
+the largest shape the suite runs (2^32 elements of q).
 
 The oracle computes sampled output rows one by one (forward rows, dQ rows, and dK/dV
 rows of keys whose query set is affordable); every output tensor must be finite.
@@ -121,3 +122,22 @@ def test_decode_paged_d128_full(orc):
     ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale)
     check("o", to_np(o), ro)
     check_lse("lse", to_np(lse), rl)
+
+
+def test_forward_beyond_2_31_elements(orc):
+    """The largest shape this suite runs: q holds 2^32 elements (B 1, S 131072, Hq 32, D 512), so
+    any 32-bit element index in the output or lse addressing would wrap. Sampled rows, among
+    them the last, are checked against the oracle; every output is finite."""
+    p = synth.dense(1, 32, 1, 131072, 512, 0, seed=3, with_do=False)
+    q, k, v = to_dev(p.q), to_dev(p.k), to_dev(p.v)
+    o, lse = attn.attn_fwd(q, k, v, scale=p.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    assert all_finite(o, lse)
+    rows = np.array([[0, 0, 0], [0, 31, 131071], [0, 17, 131071], [0, 5, 65536], [0, 30, 100000], [0, 12, 4097]],
+                    dtype=np.int64)
+    ro, rl = orc.fwd_rows(p.q, p.k, p.v, rows, p.scale)
+    got_o = np.stack([to_np(o[0, s, hh]) for _, hh, s in rows])
+    got_l = np.array([float(lse[0, hh, s]) for _, hh, s in rows])
+    check("o[sampled rows]", got_o, ro)
+    check_lse("lse[sampled rows]", got_l, rl)
