@@ -1,5 +1,6 @@
-// Attention backward on tcgen05 tensor cores (D = 256 or 512), for the forward in
-// attn_fwd.cu. Given dO, lse and Delta = rowsum(dO * o):
+// Attention backward on tcgen05 tensor cores, for the forward in attn_fwd.cu. The main kernel here
+// (a thread-block cluster per key tile) serves D = 512; D = 64, 128 and 256 use the cluster-free
+// kernel in attn_bwd_small.cu. The prep and finalize kernels here serve every D. Given dO, lse and Delta = rowsum(dO * o):
 //   P  = exp(scale * Q K^T - lse)        (recomputed; never stored)
 //   dP = dO V^T,   dS = P * (dP - Delta)
 //   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K
@@ -656,7 +657,7 @@ cudaError_t launch_bwd_t(const BwdLaunch& L, cudaStream_t stream) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if constexpr (D < 256) {
+    if constexpr (D <= 256) {  // one CTA per key tile and 128-column slice, no cluster
         cudaError_t e = launch_bwd_small_main<D>(L, stream);
         if (e != cudaSuccess) return e;
     } else {

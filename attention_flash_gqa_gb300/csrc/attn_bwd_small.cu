@@ -1,9 +1,12 @@
-// Attention backward main kernel for head_dim 128 and 64 (Qwen3-class heads), for the forward in
-// attn_fwd.cu. The same gradient as the D = 256 / 512 kernel in attn_bwd.cu:
+// Attention backward main kernel for head_dim 64 and 128 (Qwen3-class heads) and, in its "sliced"
+// form, for head_dim 256, for the forward in attn_fwd.cu. The same gradient as the cluster kernel
+// in attn_bwd.cu (used at D = 512):
 //   P  = exp(scale * Q K^T - lse),   dP = dO V^T,   dS = P * (dP - Delta)
 //   dV = P^T dO,   dK = scale * dS^T Q,   dQ = scale * dS K
-// but at D <= 128 one CTA's tensor memory holds everything a key tile needs, so there is no
-// cluster and no exchange of P^T / dS^T between CTAs.
+// but with no cluster and no exchange of P^T / dS^T between CTAs: at D <= 128 one CTA's tensor
+// memory holds everything a key tile needs; at D = 256 two CTAs per key tile each own a 128-column
+// slice of dV / dK / dQ and recompute S^T and dP^T over all of D (1.4x the tensor work of the
+// algorithmic count, against the two shared-memory-to-peer exchanges per step of the cluster kernel).
 //
 // Source: the head_dim 128 attention of "flex_attention + paged KV + CUDA graphs vs vLLM"
 // ("Setup": Qwen3-4B heads) trained with the backward the FFPA page describes for its fused
@@ -50,18 +53,31 @@ constexpr int kEw = 256;  // elementwise threads
 constexpr uint32_t kSub = 16384;  // 128 rows x 64 bf16, 128-byte swizzle
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// D: head dim (the contraction of S^T and dP^T); DS: the columns of dV / dK / dQ this CTA owns.
+// DS = D (64, 128): K and V resident, one ring slot per Q or dO tile. DS = 128 < D = 256
+// ("sliced"): two CTAs per key tile, each recomputing S^T and dP^T over all of D. K stays
+// resident (its slice is also dQ's B operand); Q, V and dO stream through the ring as 64-column
+// sub-tiles (16 KB slots) in the issuer's order, each released as soon as its product has read
+// it. The V / dO pairs stream with the slice's sub-tiles last, so dV reads the slice's dO
+// sub-tiles in place (they are the newest slots, so holding them cannot block the strictly
+// ordered ring); the slice's Q sub-tiles, needed only after the elementwise step, are streamed
+// a second time for dK (held from the S^T stream they would block the ring when it wraps).
+template <int D, int DS>
 struct SmallCfg {
+    static constexpr bool SLICED = DS < D;
     static constexpr int NSUB = D / 64;                   // 64-column sub-tiles of a [128 x D] tile
-    static constexpr uint32_t kTile = NSUB * kSub;        // one Q or dO tile = one ring slot
-    static constexpr int kStages = D == 128 ? 3 : 8;
-    static constexpr bool ALIAS = D == 128;               // dQ reuses R1
+    static constexpr int NSL = D / DS;                    // CTAs per key tile
+    static constexpr uint32_t kTile = NSUB * kSub;        // a whole [128 x D] tile
+    static constexpr uint32_t kSlot = SLICED ? kSub : kTile;  // ring slot: a sub-tile (sliced) or a tile
+    static constexpr int kStages = SLICED ? 7 : D == 128 ? 3 : 8;
+    static constexpr int NSTAGE = SLICED ? 1 : 2;         // dQ staging buffers
+    static constexpr bool ALIAS = DS == 128;              // dQ reuses R1
     static constexpr uint32_t kOffK = 0;                  // K tile, resident
-    static constexpr uint32_t kOffV = kOffK + kTile;      // V tile, resident
-    static constexpr uint32_t kOffDS = kOffV + kTile;     // dS^T [128 keys x 128 queries] bf16
+    static constexpr uint32_t kOffV = kOffK + kTile;      // V tile, resident (not sliced)
+    static constexpr uint32_t kOffDS = kOffV + (SLICED ? 0 : kTile);  // dS^T [128 keys x 128 queries] bf16
     static constexpr uint32_t kOffStage = kOffDS + 2 * kSub;  // dQ staging, 2 x (128 rows x 32 fp32)
-    static constexpr uint32_t kOffRing = kOffStage + 2 * kSub;
-    static constexpr uint32_t kOffVec = kOffRing + kStages * kTile;  // step's lse2[128], Delta[128]
+    static constexpr uint32_t kOffRing = kOffStage + NSTAGE * kSub;
+    static constexpr uint32_t kOffVec = kOffRing + kStages * kSlot;  // step's lse2[128], Delta[128]
     static constexpr uint32_t kOffBar = kOffVec + 1024;
     static constexpr uint32_t kSmem = kOffBar + 512 + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
@@ -77,13 +93,14 @@ struct SmallArgs {
     float scale, scale_log2;
 };
 
-template <int D>
+template <int D, int DS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_small_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                      const __grid_constant__ CUtensorMap tdq, SmallArgs a) {
-    using C = SmallCfg<D>;
-    const int g = blockIdx.x;  // KV head
+    using C = SmallCfg<D, DS>;
+    const int g = blockIdx.x / C::NSL;        // KV head
+    const int c0 = (blockIdx.x % C::NSL) * DS;  // this CTA's columns of dV, dK, dQ
     const int seq = blockIdx.y;
     const int kv_tile = blockIdx.z;  // tile 0 sees the most queries: launched first
     int seq_start = 0, L = a.S, bcoord = seq;
@@ -145,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t tDV = tbase, tDK = tbase + D, tR0 = tbase + 2 * D, tR1 = tR0 + 128;
+    const uint32_t tDV = tbase, tDK = tbase + DS, tR0 = tbase + 2 * DS, tR1 = tR0 + 128;
     const uint32_t tDQ = C::ALIAS ? tR1 : tR1 + 128;
     const int krow = seq_start + k0;
     // TMEM lanes a warp may access: 32 * (warp % 4) ..
@@ -159,27 +176,62 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             prefetch_tmap(&tdo);
-            mbar_expect_tx(smem_u32(kv_full), 2 * C::kTile);
+            mbar_expect_tx(smem_u32(kv_full), (C::SLICED ? 1 : 2) * C::kTile);
             for (int u = 0; u < C::NSUB; ++u) {
                 tma_load_4d(sK + u * kSub, &tk, smem_u32(kv_full), 64 * u, g, krow, bcoord);
-                tma_load_4d(sV + u * kSub, &tv, smem_u32(kv_full), 64 * u, g, krow, bcoord);
+                if (!C::SLICED) tma_load_4d(sV + u * kSub, &tv, smem_u32(kv_full), 64 * u, g, krow, bcoord);
             }
             int slot = 0, round = 0;
             bool ok = true;
-            auto load_tile = [&](const CUtensorMap* map, int h, int qrow) -> bool {
+            // one ring slot: sub-tiles u0 .. u0 + nu - 1 of a [128 x D] tile (rows row0, head hh)
+            auto load_slot = [&](const CUtensorMap* map, int hh, int row0, int u0, int nu) -> bool {
                 if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x41))
                     return false;
                 const uint32_t fb = smem_u32(&full[slot]);
-                mbar_expect_tx(fb, C::kTile);
-                const uint32_t dst = sRing + slot * C::kTile;
-                for (int u = 0; u < C::NSUB; ++u) tma_load_4d(dst + u * kSub, map, fb, 64 * u, h, qrow, bcoord);
+                mbar_expect_tx(fb, nu * kSub);
+                const uint32_t dst = sRing + slot * C::kSlot;
+                for (int u = 0; u < nu; ++u) tma_load_4d(dst + u * kSub, map, fb, 64 * (u0 + u), hh, row0, bcoord);
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
-            // consumption order of the UMMA issuer: Q(0) dO(0) Q(1) dO(1) ...
+            // sliced: the issuer's order is, for every step t, Q(t), VdO(t) and the slice's Q
+            // sub-tiles of step t again; Q(t) = the Q_u (u = 0..), VdO(t) = the V_u dO_u pairs with
+            // the slice's pairs last
+            auto step_rows = [&](int t, int& hh, int& qrow) {
+                hh = g * G + t / n_qt;
+                qrow = seq_start + (i_begin + t % n_qt) * kB;
+            };
+            auto load_q = [&](int t) -> bool {
+                int hh, qrow;
+                step_rows(t, hh, qrow);
+                for (int u = 0; u < C::NSUB; ++u)
+                    if (!load_slot(&tq, hh, qrow, u, 1)) return false;
+                return true;
+            };
+            auto load_vdo = [&](int t) -> bool {
+                int hh, qrow;
+                step_rows(t, hh, qrow);
+                for (int i = 0; i < C::NSUB; ++i) {  // the slice's sub-tiles last
+                    const int u = (c0 / 64 + DS / 64 + i) % C::NSUB;
+                    if (!load_slot(&tv, g, krow, u, 1) || !load_slot(&tdo, hh, qrow, u, 1)) return false;
+                }
+                return true;
+            };
+            auto load_qc = [&](int t) -> bool {
+                int hh, qrow;
+                step_rows(t, hh, qrow);
+                for (int u = 0; u < DS / 64; ++u)
+                    if (!load_slot(&tq, hh, qrow, c0 / 64 + u, 1)) return false;
+                return true;
+            };
             for (int t = 0; ok && t < n; ++t) {
                 const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
-                ok = load_tile(&tq, h, qrow) && load_tile(&tdo, h, qrow);
+                if (C::SLICED) {
+                    ok = load_q(t) && load_vdo(t) && load_qc(t);
+                } else {
+                    // consumption order of the UMMA issuer: Q(0) dO(0) Q(1) dO(1) ...
+                    ok = load_slot(&tq, h, qrow, 0, C::NSUB) && load_slot(&tdo, h, qrow, 0, C::NSUB);
+                }
             }
             const int issued = round * C::kStages + slot;
             for (int s = 0; s < C::kStages && s < issued; ++s) {
@@ -187,6 +239,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x47);
             }
             mbar_drain(smem_u32(kv_full), 0, a.status, 0x4e);
+        }
+    } else if (warp == kMmaWarp && C::SLICED) {
+        // ------------------------ UMMA issuer, sliced (D = 256) ---------------------------
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // X_u x Y_u^T: both K-major
+            constexpr uint32_t idG = idesc_bf16_f32(128, 64, false, true);    // P^T / dS^T x 64 slice columns
+            constexpr uint32_t idQ = idesc_bf16_f32(128, 64, true, true);     // dS (MN-major) x 64 columns of K
+            int slot = 0, round = 0;
+            auto acquire = [&](int& s) -> bool {
+                if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x42)) return false;
+                tc_fence_after();
+                s = slot;
+                if (++slot == C::kStages) slot = 0, ++round;
+                return true;
+            };
+            auto ring = [&](int s) { return sRing + (uint32_t)s * C::kSlot; };
+            const int us0 = c0 / 64;  // the slice's first sub-tile
+            // S^T = sum_u K_u (resident) Q_u^T, each Q_u released once read
+            auto issue_s = [&]() -> bool {
+                for (int u = 0; u < C::NSUB; ++u) {
+                    int ys;
+                    if (!acquire(ys)) return false;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ss(tR0, sdesc_sw128(sK + u * kSub + kk * 32, 16, 1024),
+                                     sdesc_sw128(ring(ys) + kk * 32, 16, 1024), idS, (u | kk) ? 1u : 0u);
+                    umma_commit(smem_u32(&empty[ys]));
+                }
+                umma_commit(smem_u32(s_full));
+                return true;
+            };
+            // dP^T = sum_u V_u dO_u^T, both streamed, the slice's pairs last; the slice's dO
+            // sub-tiles are kept (doc) for dV
+            int doc[2] = {0, 0};
+            auto issue_dp = [&]() -> bool {
+                for (int i = 0; i < C::NSUB; ++i) {
+                    int xs, ys;
+                    if (!acquire(xs) || !acquire(ys)) return false;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        umma_bf16_ss(tR1, sdesc_sw128(ring(xs) + kk * 32, 16, 1024),
+                                     sdesc_sw128(ring(ys) + kk * 32, 16, 1024), idS, (i | kk) ? 1u : 0u);
+                    umma_commit(smem_u32(&empty[xs]));
+                    if (i >= C::NSUB - DS / 64) doc[i - (C::NSUB - DS / 64)] = ys;
+                    else umma_commit(smem_u32(&empty[ys]));
+                }
+                umma_commit(smem_u32(dp_full));
+                return true;
+            };
+            bool ok = mbar_wait(smem_u32(kv_full), 0, abort_flag, a.status, 0x43);
+            tc_fence_after();
+            if (ok) ok = issue_s();   // S^T(0)
+            if (ok) ok = issue_dp();  // dP^T(0)
+            for (int t = 0; ok && t < n; ++t) {
+                // dV_c += P^T dO_c: A = P^T (bf16 pairs over R0), B = the slice's two dO sub-tiles
+                ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x44);
+                if (!ok) break;
+                tc_fence_after();
+                int b0 = doc[0], b1 = doc[1];
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t at = tR0 + (kk >> 2) * 64 + (kk & 3) * 8;
+                    const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
+                    umma_bf16_ts(tDV, at, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
+                    umma_bf16_ts(tDV + 64, at, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                }
+                umma_commit(smem_u32(&empty[b0]));
+                umma_commit(smem_u32(&empty[b1]));
+                ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x45);
+                if (!ok) break;
+                tc_fence_after();
+                // dQ_c = dS K_c first (its readout starts while dK runs), into R1; K_c is resident
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sDS + kk * 2048, kSub, 1024);
+                    umma_bf16_ss(tDQ, ad, sdesc_sw128(sK + us0 * kSub + kk * 2048, kSub, 1024), idQ, kk > 0 ? 1u : 0u);
+                    umma_bf16_ss(tDQ + 64, ad, sdesc_sw128(sK + (us0 + 1) * kSub + kk * 2048, kSub, 1024), idQ,
+                                 kk > 0 ? 1u : 0u);
+                }
+                umma_commit(smem_u32(dq_full));
+                // dK_c += dS^T Q_c: B = the slice's two Q sub-tiles
+                ok = acquire(b0) && acquire(b1);
+                if (!ok) break;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                    const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
+                    umma_bf16_ss(tDK, ad, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
+                    umma_bf16_ss(tDK + 64, ad, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                }
+                umma_commit(smem_u32(&empty[b0]));
+                umma_commit(smem_u32(&empty[b1]));
+                umma_commit(smem_u32(ds_free));
+                if (t + 1 < n) {
+                    // S^T(t+1) over R0 (after the dV read of R0: the MMA pipe runs in order). Issued
+                    // after dQ(t) / dK(t): issuing it first made the issuer wait for Q(t+1) before
+                    // it could start dQ(t), lengthening the dQ -> readout -> dP chain.
+                    ok = issue_s();
+                    if (!ok) break;
+                    // dP^T(t+1) over R1 once dQ(t) has left it
+                    ok = mbar_wait(smem_u32(dq_free), t & 1, abort_flag, a.status, 0x48);
+                    if (!ok) break;
+                    tc_fence_after();
+                    ok = issue_dp();
+                }
+            }
+            // every issued UMMA has finished before TMEM may be released
+            umma_commit(smem_u32(mma_idle));
+            mbar_drain(smem_u32(mma_idle), 0, a.status, 0x49);
         }
     } else if (warp == kMmaWarp) {
         // --------------------------------- UMMA issuer -----------------------------------
@@ -204,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // acc(128 x 128) = X (resident [keys x D], K-major) x Y^T (ring tile [queries x D], K-major)
             auto rows_x_tile = [&](uint32_t dacc, uint32_t x, int ys) {
-                const uint32_t y = sRing + ys * C::kTile;
+                const uint32_t y = sRing + ys * C::kSlot;
                 for (int u = 0; u < C::NSUB; ++u)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
@@ -229,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x44);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t dob = sRing + ds * C::kTile;
+                const uint32_t dob = sRing + ds * C::kSlot;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // queries 64h .. 64h+63 of P^T sit at R0 columns 64h .. 64h+31
                     umma_bf16_ts(tDV, tR0 + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dob + kk * 2048, kSub, 1024),
@@ -259,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 // dK += dS^T Q: A = dS^T (K-major, shared memory), B = Q (N-major)
-                const uint32_t qb = sRing + qs_t * C::kTile;
+                const uint32_t qb = sRing + qs_t * C::kSlot;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
@@ -297,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
             // the whole row into registers first, so dQ's columns are handed back at once (at
             // D = 128 the next dP^T waits for them)
-            uint32_t rq[D];
+            uint32_t rq[DS];
             if (ok) {
 #pragma unroll
-                for (int c4 = 0; c4 < D / 32; ++c4) {
+                for (int c4 = 0; c4 < DS / 32; ++c4) {
                     uint32_t tmp[32];
                     tmem_ld32(tDQ + c4 * 32 + lane_base, tmp);
 #pragma unroll
@@ -311,9 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(dq_free));
 #pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-                const uint32_t buf = sStage + (c4 & 1) * kSub;
-                if (leader) bulk_wait_group_read1();  // the reduce that last read `buf` is done
+            for (int c4 = 0; c4 < DS / 32; ++c4) {
+                const uint32_t buf = sStage + (c4 % C::NSTAGE) * kSub;
+                if (leader) {  // the reduce that last read `buf` is done
+                    if (C::NSTAGE == 2) bulk_wait_group_read1();
+                    else bulk_wait_group_read0();
+                }
                 named_bar_sync(2, 128);
                 if (ok) {
 #pragma unroll
@@ -327,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 ok = named_bar_and(2, 128, ok);
                 if (ok && leader) {
-                    tma_reduce_add_4d(&tdq, buf, 32 * c4, h, seq_start + q0, bcoord);
+                    tma_reduce_add_4d(&tdq, buf, c0 + 32 * c4, h, seq_start + q0, bcoord);
                     bulk_commit_group();
                 }
             }
@@ -449,10 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ok) {
             const size_t row = (size_t)(a.cu_seqlens ? seq_start + kabs : seq * a.S + kabs) * a.Hkv + g;
-            uint16_t* dv_row = a.dV + row * D;
-            uint16_t* dk_row = a.dK + row * D;
+            uint16_t* dv_row = a.dV + row * D + c0;
+            uint16_t* dk_row = a.dK + row * D + c0;
 #pragma unroll 1
-            for (int c4 = hf; c4 < D / 32; c4 += 2) {  // the two warps of a lane quarter split the columns
+            for (int c4 = hf; c4 < DS / 32; c4 += 2) {  // the two warps of a lane quarter split the columns
                 uint32_t rv[32], rk[32];
                 tmem_ld32(tDV + c4 * 32 + lane_base, rv);
                 tmem_ld32(tDK + c4 * 32 + lane_base, rk);
@@ -488,22 +652,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_small_main(const BwdLaunch& L, cudaStream_t stream) {
+    constexpr int DS = D < 128 ? D : 128;
     SmallArgs a;
     a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV;
     a.cu_seqlens = L.cu_seqlens, a.status = L.status;
     a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.window = L.window, a.T = L.total_rows;
     a.scale = L.scale, a.scale_log2 = L.scale * kLog2e;
-    constexpr uint32_t kSmem = SmallCfg<D>::kSmem;
-    cudaError_t e = cudaFuncSetAttribute(bwd_small_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    constexpr uint32_t kSmem = SmallCfg<D, DS>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_small_kernel<D, DS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(L.Hkv, L.nseq, (L.S + kB - 1) / kB);
-    const ProfMark m = prof_begin(stream, D == 128 ? "bwd_main_d128" : "bwd_main_d64");
-    bwd_small_kernel<D><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
+    const dim3 grid(L.Hkv * (D / DS), L.nseq, (L.S + kB - 1) / kB);
+    const ProfMark m = prof_begin(stream, D == 256 ? "bwd_main_d256" : D == 128 ? "bwd_main_d128" : "bwd_main_d64");
+    bwd_small_kernel<D, DS><<<grid, kThreads, kSmem, stream>>>(L.tq, L.tk, L.tv, L.tdo, L.tdq, a);
     prof_end(stream, m);
     return cudaGetLastError();
 }
 
 template cudaError_t launch_bwd_small_main<64>(const BwdLaunch&, cudaStream_t);
 template cudaError_t launch_bwd_small_main<128>(const BwdLaunch&, cudaStream_t);
+template cudaError_t launch_bwd_small_main<256>(const BwdLaunch&, cudaStream_t);
 
 }  // namespace attn
