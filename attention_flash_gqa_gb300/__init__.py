@@ -168,7 +168,6 @@ def _ptr(t):
 
 
 _ws_cache: dict = {}
-_decode_layout: dict = {}  # device -> shape of the last decode call on the cached workspace
 
 
 def _workspace(nbytes: int, device, zero: bool, key: str):
@@ -319,13 +318,7 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=No
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
     need = attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D)
     if workspace is None:
-        workspace = _workspace(need, q.device, True, "decode")
-        # the arrival counters sit at the start and their extent depends on the shape: when the
-        # shape changes, the region may hold the previous call's partials, so clear it
-        key = (str(q.device), B, Hq, Hkv, D)
-        if _decode_layout.get(str(q.device)) != key:
-            workspace[:min(workspace.numel(), 4 * B * Hkv + 256)].zero_()
-            _decode_layout[str(q.device)] = key
+        workspace = _workspace(need, q.device, False, "decode")
     rc = load_library().attn_decode_paged(_bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
                                           _ptr(block_table), _ptr(seq_lens), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D,
                                           page_size, block_table.shape[1], num_pages, scale, int(window),

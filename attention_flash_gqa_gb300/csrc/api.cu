@@ -150,12 +150,12 @@ size_t bwd_ws(long long rows, int Hq, int D) {
 // CTAs per KV-head block of a decode launch at most: the blocks share decode_max_grid() CTAs.
 int decode_grid_cap(int nhb) { return attn::decode_max_grid() / nhb > 1 ? attn::decode_max_grid() / nhb : 1; }
 
-// Decode workspace: per-(request, head block) arrival counters, then the split partials (slot
-// (b + k) * 2 + half for CTA k of a head block, every head block writing only its own heads).
+// Decode workspace: the split partials (slot (b + k) * 2 + half for CTA k of a head block, every
+// head block writing only its own heads). Every call writes all of it that it reads: contents on
+// entry do not matter.
 size_t decode_ws(int B, int Hq, int Hkv, int D) {
     const int nhb = Hkv > 0 && D > 0 && Hq > 0 ? Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv) : 1;
-    return align256((size_t)B * nhb * 4) +
-           align256((size_t)(B + decode_grid_cap(nhb)) * 2 * Hq * attn::decode_row_floats(D > 0 ? D : 0) * 4);
+    return align256((size_t)(B + decode_grid_cap(nhb)) * 2 * Hq * attn::decode_row_floats(D > 0 ? D : 0) * 4);
 }
 
 // 3-D map over a paged cache [num_pages * 16 tokens, heads, dim]: box = dim x hb heads x 16 tokens,
@@ -447,8 +447,7 @@ int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_b
     L.q = q, L.k_cache = k_cache, L.v_cache = v_cache, L.block_table = block_table, L.seq_lens = seq_lens;
     L.o = o, L.lse = lse, L.status = dev->status;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    L.counters = reinterpret_cast<int32_t*>(ws);
-    L.part = reinterpret_cast<float*>(ws + align256((size_t)B * nhb * 4));
+    L.part = reinterpret_cast<float*>(ws);
     L.B = B, L.Hq = Hq, L.Hkv = Hkv, L.D = D, L.max_pages = max_pages_per_seq, L.num_pages = num_pages;
     L.scale = scale, L.window = window;
     // the head blocks share the SMs: each block's pages are split over sms / nhb CTAs

@@ -27,7 +27,6 @@ struct DecodeLaunch {
     uint16_t* o;
     float* lse;
     float* part;
-    int32_t* counters;  // [B][Hkv / hb]
     unsigned* status;
     int B, Hq, Hkv, D, max_pages, num_pages, grid, window;
     float scale;

@@ -28,8 +28,13 @@
 //    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
 //    a butterfly reduce-scatter across the lanes that split a token.
 //  * fp32 online softmax in the log2 domain. Every (CTA, token half) touching a request
-//    leaves unnormalised partials (o, m, l) in the workspace; the last CTA to finish that
-//    request (arrival counter) merges them and resets the counter to zero.
+//    leaves unnormalised partials (o, m, l) in the workspace, with no wait of any kind, and
+//    streams on. A second, small kernel merges each request's partials once the decode grid
+//    has finished: it is launched with programmatic stream serialisation, so it is resident
+//    before that and its launch costs nothing on the critical path. (A first version had the
+//    last CTA to finish a request merge it in-kernel, behind an arrival counter: CTAs whose
+//    range ended a request mid-stream stalled for the write-back, the atomic and the merge,
+//    and finished the grid late.)
 #include <cuda_runtime.h>
 
 #include "attn_internal.h"
@@ -74,7 +79,6 @@ struct DecodeArgs {
     uint16_t* o;
     float* lse;
     float* part;       // [(B + grid) * 2 slots][Hq][D + 4]
-    int32_t* counters; // [B][nhb]
     unsigned* status;
     int B, Hq, Hkv, max_pages, num_pages;
     int window;        // <= 0: none
@@ -132,12 +136,14 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = bars + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
-    int* last_flag = const_cast<int*>(abort_flag) + 1;
-    int* warp_sums = last_flag + 1;  // [8]
+    int* warp_sums = const_cast<int*>(abort_flag) + 2;  // [8]
     int32_t* unit_tab = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [kMaxUnits]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
+    // the merge kernel that follows may be scheduled now: it waits for this grid's completion
+    // before it reads anything, and its small CTAs fit beside this one
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -189,18 +195,6 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     const int Gc = (int)(P < (long long)gridDim.x ? P : (long long)gridDim.x);
     const int k = blockIdx.x;
 
-    // Requests with no cached token: o = 0, lse = -inf (CTA 0 of each head block writes its heads).
-    if (k == 0) {
-        const int nh = h1 - h0;
-        for (int idx = tid; idx < B * nh; idx += kThreads) {
-            const int b = idx / nh, h = h0 + idx % nh;
-            if (start[b + 1] == start[b]) {
-                a.lse[(size_t)b * a.Hq + h] = -INFINITY;
-                uint16_t* orow = a.o + ((size_t)b * a.Hq + h) * D;
-                for (int d = 0; d < D; d += 8) *reinterpret_cast<uint4*>(orow + d) = make_uint4(0, 0, 0, 0);
-            }
-        }
-    }
     if (P == 0 || k >= Gc) return;
     const long long u0 = (long long)k * P / Gc, u1 = (long long)(k + 1) * P / Gc;
     if (u0 >= u1) return;
@@ -243,6 +237,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     // The producer warp stages the first units itself and issues their pages at once, so
     // the copies are in flight while the rest of the table is staged.
     const int n_pre = min(n_units, kStages);
+    // every cached byte is read once per step: evict-first keeps the stream from displacing
+    // (or forcing the write-back of) other lines in L2
+    const uint64_t policy = l2_policy_evict_first();
     auto issue = [&](int i, int32_t entry) {
         const int s = i % kStages;
         const uint32_t fb = smem_u32(&full[s]);
@@ -251,11 +248,11 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             const uint32_t dk = smem_u32(stage_base + (size_t)s * 2 * page_bytes), dv = dk + page_bytes;
             if (a.nhb == 1) {  // every head: the page is contiguous
                 const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * D;
-                bulk_load(dk, a.kc + off, page_bytes, fb);
-                bulk_load(dv, a.vc + off, page_bytes, fb);
+                bulk_load_hint(dk, a.kc + off, page_bytes, fb, policy);
+                bulk_load_hint(dv, a.vc + off, page_bytes, fb, policy);
             } else {  // 16 tokens x hb heads x D of the page
-                tma_load_3d(dk, &tk, fb, 0, g0, (entry >> 5) * kPage);
-                tma_load_3d(dv, &tv, fb, 0, g0, (entry >> 5) * kPage);
+                tma_load_3d_hint(dk, &tk, fb, 0, g0, (entry >> 5) * kPage, policy);
+                tma_load_3d_hint(dv, &tv, fb, 0, g0, (entry >> 5) * kPage, policy);
             }
         } else {
             mbar_arrive(fb);
@@ -511,10 +508,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
 
-        // ---- end of this request inside this CTA: write partials, last CTA merges -------
-        const long long req_end = start[b + 1];
-        if (u + 1 == req_end || u + 1 == u1) {
-            const int kf = owner_of(start[b], P, Gc), kl = owner_of(req_end - 1, P, Gc);
+        // ---- end of this request inside this CTA: write its partials (o, m, l) -----------
+        // The merge kernel that follows this grid combines each request's slots.
+        if (u + 1 == start[b + 1] || u + 1 == u1) {
             // slot of (request b, CTA k, token half): (b + k) * 2 + half
             float* slot = a.part + ((size_t)(b + k) * 2 + half) * a.Hq * kRowF;
             if (active) {
@@ -540,100 +536,6 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                     }
                 }
             }
-            __threadfence();
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-            if (tid == 0) {
-                const int prev = atomicAdd(&a.counters[(size_t)b * a.nhb + hbk], 1);
-                *last_flag = prev == kl - kf;
-            }
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-            if (*last_flag) {
-                __threadfence();
-                // merge the partials of CTAs kf..kl (both token halves) for every (head, dim):
-                // slots (b + kk) * 2 + hf for kk in kf..kl and hf < WPH. Pass 1: per head the
-                // running max and sum over the slots (online rescaling, one thread per head);
-                // pass 2: every thread combines IPT (head, 4-dim) items, issuing the loads of all
-                // its items for a slot together. The consumer warps' score scratch is free here.
-                const int nslots = DC::WPH * (kl - kf + 1);
-                auto slot_row = [&](int q, int h) -> const float* {
-                    return a.part + ((size_t)(b + kf + q / DC::WPH) * 2 + q % DC::WPH) * a.Hq * kRowF + (size_t)h * kRowF;
-                };
-                float* mM = scratch;               // [h1 - h0] max over the slots
-                float* mI = scratch + (h1 - h0);   // [h1 - h0] 1 / sum
-                for (int h = h0 + tid; h < h1; h += kConsumerWarps * 32) {
-                    float M = -INFINITY, Ls = 0.f;
-                    for (int q0 = 0; q0 < nslots; q0 += 8) {  // 8 slots' loads in flight at once
-                        float mk[8], lk[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            mk[j] = -INFINITY, lk[j] = 0.f;
-                            if (q0 + j < nslots) {
-                                const float* row = slot_row(q0 + j, h);
-                                mk[j] = __ldcg(row + D), lk[j] = __ldcg(row + D + 1);
-                            }
-                        }
-                        float Mc = M;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) Mc = fmaxf(Mc, mk[j]);
-                        if (Mc == -INFINITY) continue;
-                        Ls = M == -INFINITY ? 0.f : Ls * fast_exp2(M - Mc);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) Ls += mk[j] == -INFINITY ? 0.f : lk[j] * fast_exp2(mk[j] - Mc);
-                        M = Mc;
-                    }
-                    mM[h - h0] = M;
-                    mI[h - h0] = Ls > 0.f ? 1.f / Ls : 0.f;
-                    a.lse[(size_t)b * a.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
-                }
-                asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-                constexpr int IPT = 4;
-                const int nitems = (h1 - h0) * (D / 4);
-                for (int base = tid; base < nitems; base += kConsumerWarps * 32 * IPT) {
-                    float4 O[IPT];
-                    int hI[IPT], dI[IPT];
-#pragma unroll
-                    for (int k2 = 0; k2 < IPT; ++k2) {
-                        const int idx = min(base + k2 * kConsumerWarps * 32, nitems - 1);
-                        hI[k2] = h0 + idx / (D / 4), dI[k2] = idx % (D / 4);
-                        O[k2] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                    for (int q0 = 0; q0 < nslots; q0 += 2) {  // loads of 2 slots x IPT items in flight
-                        float mk[2][IPT];
-                        float4 ov[2][IPT];
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int k2 = 0; k2 < IPT; ++k2) {
-                                mk[j][k2] = -INFINITY;
-                                ov[j][k2] = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (q0 + j < nslots) {
-                                    const float* row = slot_row(q0 + j, hI[k2]);
-                                    mk[j][k2] = __ldcg(row + D);
-                                    ov[j][k2] = __ldcg(reinterpret_cast<const float4*>(row) + dI[k2]);
-                                }
-                            }
-#pragma unroll
-                        for (int j = 0; j < 2; ++j)
-#pragma unroll
-                            for (int k2 = 0; k2 < IPT; ++k2) {
-                                const float wgt = mk[j][k2] == -INFINITY ? 0.f : fast_exp2(mk[j][k2] - mM[hI[k2] - h0]);
-                                O[k2].x += wgt * ov[j][k2].x, O[k2].y += wgt * ov[j][k2].y;
-                                O[k2].z += wgt * ov[j][k2].z, O[k2].w += wgt * ov[j][k2].w;
-                            }
-                    }
-#pragma unroll
-                    for (int k2 = 0; k2 < IPT; ++k2) {
-                        if (base + k2 * kConsumerWarps * 32 >= nitems) break;
-                        const float inv = mI[hI[k2] - h0];
-                        uint2 w;
-                        w.x = pack_bf16x2(O[k2].x * inv, O[k2].y * inv);
-                        w.y = pack_bf16x2(O[k2].z * inv, O[k2].w * inv);
-                        *reinterpret_cast<uint2*>(a.o + ((size_t)b * a.Hq + hI[k2]) * D + 4 * dI[k2]) = w;
-                    }
-                }
-                if (tid == 0) a.counters[(size_t)b * a.nhb + hbk] = 0;
-            }
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
             // reset the running state for the next request
             m_run = -INFINITY, l_run = 0.f;
 #pragma unroll
@@ -641,6 +543,121 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < QD; ++e) acc_o[hh][e] = 0.f;
         }
+    }
+}
+
+
+// Combines the split partials of every (request, head block): the partial slots of request b are
+// those of CTAs kf..kl of the decode grid that covered its units (both token halves when two
+// warps share a head). Launched right after the decode kernel with programmatic stream
+// serialisation, so its CTAs are resident while the decode grid runs; griddepcontrol.wait
+// returns once that grid has finished and its writes are visible. A thread owns one head's 16
+// dims and folds the slots in a running maximum, SB slots at a time with all of their loads
+// (each slot's m, l and 16 o values) in flight together: a request split over up to SB slots
+// is merged in one round trip. A request with no visible key gets o = 0 and lse = -inf.
+struct MergeArgs {
+    const float* part;
+    const int32_t* seq_lens;
+    uint16_t* o;
+    float* lse;
+    unsigned* status;
+    int B, Hq, hb, decode_grid, max_pages, window;
+};
+
+// Heads of a (request, head block) are split over gridDim.z CTAs of kMergeThreads, one
+// 16-dim item per thread, so the merge of a batch runs on every SM.
+constexpr int kMergeThreads = 64;
+
+template <int G, int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(MergeArgs m) {
+    using DC = DecCfg<G, D>;
+    constexpr int kRowF = DC::kRowF;
+    constexpr int SB = 8;
+    constexpr int DI = 8;  // dims per thread
+    const int b = blockIdx.x;
+    const int nh = m.hb * G / gridDim.z;  // heads of this CTA
+    const int h0 = blockIdx.y * m.hb * G + blockIdx.z * nh;
+    // Which decode CTAs covered request b follows from the request lengths alone (inputs, not
+    // written by the decode grid): this runs before the wait, beside the decode grid.
+    // Every warp sums the unit counts over all requests itself (no shared memory, so these
+    // CTAs fit beside a decode CTA).
+    DecodeArgs la;  // the fields req_len / req_units read
+    la.seq_lens = m.seq_lens, la.max_pages = m.max_pages, la.window = m.window, la.status = m.status;
+    long long before = 0, total = 0;
+    for (int i = threadIdx.x & 31; i < m.B; i += 32) {
+        const int n = req_units(la, req_len(la, i));
+        total += n;
+        if (i < b) before += n;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+    }
+    const long long s0 = before, P = total;
+    const long long s1 = s0 + req_units(la, req_len(la, b));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int Gc = (int)(P < (long long)m.decode_grid ? P : (long long)m.decode_grid);
+    const int nitems = nh * (D / DI);
+    if (s1 == s0) {
+        for (int it = threadIdx.x; it < nitems; it += blockDim.x) {
+            const int h = h0 + it / (D / DI), d0 = DI * (it % (D / DI));
+            *reinterpret_cast<uint4*>(m.o + ((size_t)b * m.Hq + h) * D + d0) = make_uint4(0, 0, 0, 0);
+            if (d0 == 0) m.lse[(size_t)b * m.Hq + h] = -INFINITY;
+        }
+        return;
+    }
+    const int kf = owner_of(s0, P, Gc), kl = owner_of(s1 - 1, P, Gc);
+    const int nslots = DC::WPH * (kl - kf + 1);
+    auto slot_row = [&](int q, int h) -> const float* {
+        return m.part + ((size_t)(b + kf + q / DC::WPH) * 2 + q % DC::WPH) * m.Hq * kRowF + (size_t)h * kRowF;
+    };
+    for (int it = threadIdx.x; it < nitems; it += blockDim.x) {
+        const int h = h0 + it / (D / DI), d0 = DI * (it % (D / DI));
+        float M = -INFINITY, Ls = 0.f;
+        float O[DI];
+#pragma unroll
+        for (int e = 0; e < DI; ++e) O[e] = 0.f;
+        for (int q0 = 0; q0 < nslots; q0 += SB) {
+            float2 ml[SB];
+            float4 ov[SB][2];
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                ml[j] = make_float2(-INFINITY, 0.f);
+                ov[j][0] = ov[j][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (q0 + j < nslots) {
+                    const float* row = slot_row(q0 + j, h);
+                    ml[j] = __ldcg(reinterpret_cast<const float2*>(row + D));
+                    ov[j][0] = __ldcg(reinterpret_cast<const float4*>(row + d0));
+                    ov[j][1] = __ldcg(reinterpret_cast<const float4*>(row + d0) + 1);
+                }
+            }
+            float Mc = M;
+#pragma unroll
+            for (int j = 0; j < SB; ++j) Mc = fmaxf(Mc, ml[j].x);
+            if (Mc == -INFINITY) continue;
+            const float rs = M == -INFINITY ? 0.f : fast_exp2(M - Mc);
+            Ls *= rs;
+#pragma unroll
+            for (int e = 0; e < DI; ++e) O[e] *= rs;
+#pragma unroll
+            for (int j = 0; j < SB; ++j) {
+                const float w = ml[j].x == -INFINITY ? 0.f : fast_exp2(ml[j].x - Mc);  // an empty slot adds nothing
+                Ls += w * ml[j].y;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    O[4 * c] += w * ov[j][c].x, O[4 * c + 1] += w * ov[j][c].y;
+                    O[4 * c + 2] += w * ov[j][c].z, O[4 * c + 3] += w * ov[j][c].w;
+                }
+            }
+            M = Mc;
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        uint4 w0;
+        w0.x = pack_bf16x2(O[0] * inv, O[1] * inv), w0.y = pack_bf16x2(O[2] * inv, O[3] * inv);
+        w0.z = pack_bf16x2(O[4] * inv, O[5] * inv), w0.w = pack_bf16x2(O[6] * inv, O[7] * inv);
+        *reinterpret_cast<uint4*>(m.o + ((size_t)b * m.Hq + h) * D + d0) = w0;
+        if (d0 == 0) m.lse[(size_t)b * m.Hq + h] = Ls > 0.f ? (M + __log2f(Ls)) * 0.69314718055994531f : -INFINITY;
     }
 }
 
@@ -664,7 +681,7 @@ int decode_heads_per_unit(int Hkv, int D, int G) {
 cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     DecodeArgs a;
     a.q = L.q, a.kc = L.k_cache, a.vc = L.v_cache, a.block_table = L.block_table, a.seq_lens = L.seq_lens;
-    a.o = L.o, a.lse = L.lse, a.part = L.part, a.counters = L.counters, a.status = L.status;
+    a.o = L.o, a.lse = L.lse, a.part = L.part, a.status = L.status;
     a.B = L.B, a.Hq = L.Hq, a.Hkv = L.Hkv, a.max_pages = L.max_pages, a.num_pages = L.num_pages;
     a.window = L.window;
     const int G = L.Hq / L.Hkv;
@@ -672,31 +689,57 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     a.nhb = L.Hkv / a.hb;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     const size_t smem = decode_smem_bytes(a.hb, L.D);
-    auto go = [&](auto kern, int threads) -> cudaError_t {
+    MergeArgs mg;
+    mg.part = L.part, mg.seq_lens = L.seq_lens, mg.o = L.o, mg.lse = L.lse, mg.status = L.status;
+    mg.B = L.B, mg.Hq = L.Hq, mg.hb = a.hb, mg.decode_grid = L.grid, mg.max_pages = L.max_pages, mg.window = L.window;
+    auto go = [&](auto kern, auto merge, int threads) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        const ProfMark m = prof_begin(stream, L.D == 128 ? "decode_paged" : "decode_paged_d256");
+        ProfMark m = prof_begin(stream, L.D == 128 ? "decode_paged" : "decode_paged_d256");
         kern<<<dim3(L.grid, a.nhb), threads, smem, stream>>>(L.tk, L.tv, a);
         prof_end(stream, m);
-        return cudaGetLastError();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        // the merge may start while the decode grid still runs (it waits for that grid's
+        // completion on the device), which hides its launch behind the decode tail
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        const int nh = a.hb * G;  // query heads of a head block
+        int nz = nh * (L.D / 8) / kMergeThreads;
+        if (nz < 1) nz = 1;
+        while (nh % nz) --nz;
+        cfg.gridDim = dim3(L.B, a.nhb, nz);
+        cfg.blockDim = dim3(kMergeThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        m = prof_begin(stream, "decode_merge");
+        e = cudaLaunchKernelEx(&cfg, merge, mg);
+        prof_end(stream, m);
+        return e != cudaSuccess ? e : cudaGetLastError();
     };
+#define ATTN_DECODE_CASE(G_, D_) \
+    case G_: return go(decode_paged_kernel<G_, D_>, decode_merge_kernel<G_, D_>, DecCfg<G_, D_>::kThreads);
     if (L.D == 128) {
         switch (G) {
-            case 1: return go(decode_paged_kernel<1, 128>, DecCfg<1, 128>::kThreads);
-            case 2: return go(decode_paged_kernel<2, 128>, DecCfg<2, 128>::kThreads);
-            case 4: return go(decode_paged_kernel<4, 128>, DecCfg<4, 128>::kThreads);
-            case 8: return go(decode_paged_kernel<8, 128>, DecCfg<8, 128>::kThreads);
+            ATTN_DECODE_CASE(1, 128)
+            ATTN_DECODE_CASE(2, 128)
+            ATTN_DECODE_CASE(4, 128)
+            ATTN_DECODE_CASE(8, 128)
             default: return cudaErrorInvalidValue;
         }
     }
     if (L.D == 256) {
         switch (G) {
-            case 1: return go(decode_paged_kernel<1, 256>, DecCfg<1, 256>::kThreads);
-            case 2: return go(decode_paged_kernel<2, 256>, DecCfg<2, 256>::kThreads);
-            case 4: return go(decode_paged_kernel<4, 256>, DecCfg<4, 256>::kThreads);
+            ATTN_DECODE_CASE(1, 256)
+            ATTN_DECODE_CASE(2, 256)
+            ATTN_DECODE_CASE(4, 256)
             default: return cudaErrorInvalidValue;
         }
     }
+#undef ATTN_DECODE_CASE
     return cudaErrorInvalidValue;
 }
 

@@ -4,8 +4,8 @@
 // for example a plug-in inside a host application that owns the whole device-memory
 // budget through its own pool, or a latency-critical token loop where cudaMalloc's
 // implicit device synchronisation would stall every other stream. For them this entry
-// point takes the decode kernel's scratch (split partials and per-request arrival
-// counters) from a fixed buffer compiled into the library instead of from a workspace.
+// point takes the decode kernel's scratch (split partials and per-request offsets into
+// them) from a fixed buffer compiled into the library instead of from a workspace.
 //
 // The buffer is a file-scope __device__ array of kScratchBytes (16 MiB). Every GPU that
 // loads this part of the library holds it until the process exits. In host code the
@@ -30,7 +30,6 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Device address of the scratch array on the current device (looked up once per device).
 void* scratch_for_current_device() {
@@ -62,12 +61,6 @@ ATTN_API int attn_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_ca
                                          max_pages_per_seq, num_pages, scale, window, nullptr, 0, stream);
     void* scratch = scratch_for_current_device();
     if (!scratch) return ATTN_ERR_NO_DEVICE;
-    // The arrival counters (one per request and KV-head block) at the start of the scratch must
-    // be zero when the kernel starts. The buffer keeps whatever the previous call left, so clear
-    // them on this stream.
-    const int nhb = Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv);
-    if (cudaMemsetAsync(scratch, 0, align256((size_t)B * nhb * 4), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return ATTN_ERR_LAUNCH;
     return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, D, page_size,
                              max_pages_per_seq, num_pages, scale, window, scratch, kScratchBytes, stream);
 }

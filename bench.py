@@ -631,7 +631,8 @@ def profile_case(args):
       prefill_paged_d512: the first `--requests` requests of the chunked-prefill workload;
       dense_d128: head_dim 128 forward + backward at batch `--batch`;
       merge_cp8_d512: the 8-part merge;
-      decode_swa_d256: the sliding-window head_dim 256 decode."""
+      decode_swa_d256: the sliding-window head_dim 256 decode;
+      decode_d128: the head_dim 128 paged decode (batch 64, Hq 32, Hkv 8)."""
     import numpy as np
     import torch
 
@@ -678,6 +679,14 @@ def profile_case(args):
         ls = torch.empty((ps.B, ps.Hq), dtype=torch.float32, device="cuda")
         run = lambda: attn.attn_decode_paged(qs, kcs, vcs, bts, sls, os_, ls, scale=ps.scale, window=ps.window)
         outs = [os_]
+    elif case == "decode_d128":
+        pd = synth.decode_paged_d128(seed=7)
+        qd, kcd, vcd = to_dev(pd.q), to_dev(pd.k_cache), to_dev(pd.v_cache)
+        btd, sld = torch.from_numpy(pd.block_table).cuda(), torch.from_numpy(pd.seq_lens).cuda()
+        od = torch.empty_like(qd)
+        ld = torch.empty((pd.B, pd.Hq), dtype=torch.float32, device="cuda")
+        run = lambda: attn.attn_decode_paged(qd, kcd, vcd, btd, sld, od, ld, scale=pd.scale)
+        outs = [od]
     else:
         raise SystemExit(f"unknown profile case {case}")
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

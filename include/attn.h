@@ -170,12 +170,13 @@ ATTN_API int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v
  *   skipped and ATTN_ERR_DEVICE_BOUNDS is recorded for attn_get_device_status().
  *   Supported: D = 128 with Hq / Hkv in {1, 2, 4, 8}, D = 256 with Hq / Hkv in {1, 2, 4};
  *   page_size = 16, Hkv <= 256, B <= 4096.
- *   workspace: at least attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, ...) bytes;
- *   it holds split partials and arrival counters (one per request and block of KV heads) at its
- *   start. The counters must be zero before the first call on a workspace, and again when a
- *   call's (B, Hq, Hkv, D) differs from the previous call's on it: clear the first 4 * B * Hkv
- *   bytes (e.g. cudaMemsetAsync), since the previous call's partials may lie there. Every call
- *   leaves its own counters zero. Calls that share a workspace must not overlap on the GPU.
+ *   workspace: at least attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, ...) bytes,
+ *   256-byte aligned; it holds the split partials of the requests that several CTAs share and
+ *   each request's offset into them. Contents on entry do not matter. Calls that share a
+ *   workspace must not overlap on the GPU.
+ *   Enqueues two kernels on `stream`: the split decode and the merge of its partials. The merge
+ *   is launched with programmatic stream serialisation (it may become resident while the decode
+ *   grid runs and waits on the device for that grid's completion).
  */
 ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                       const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
