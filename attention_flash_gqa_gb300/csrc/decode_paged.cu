@@ -212,6 +212,20 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         while (b_first < B && start[b_first + 1] <= u0) ++b_first;
     }
 
+    // The query rows of the later requests in this range travel to L2 now, so the consumers'
+    // switch to such a request waits on L2 rather than on HBM.
+    {
+        int lo = b_first, hi = B - 1;  // request of the range's last unit
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start[mid] <= u1 - 1) lo = mid;
+            else hi = mid - 1;
+        }
+        const int lines = (h1 - h0) * D * 2 / 128;  // the head block's query rows of one request
+        for (int idx = tid; idx < (lo - b_first) * lines; idx += kThreads)
+            prefetch_l2(reinterpret_cast<const uint8_t*>(a.q + ((size_t)(b_first + 1 + idx / lines) * a.Hq + h0) * D) +
+                        (size_t)(idx % lines) * 128);
+    }
     // Page table of this CTA's range, gathered once by all threads: entry = page id << 5 |
     // valid tokens in the page (1..16), or -1 for a page id outside the pool. The loops below
     // then never wait on a dependent global load.
@@ -419,47 +433,56 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                 }
             }
             __syncwarp();
-            // softmax layout: lane holds idx = lane + 32*j (head lane % G, token idx / G)
+            // softmax layout: lane holds idx = lane + 32*j (head lane % G, token idx / G).
+            // Lazy running max (as in the prefill forward): m_run, shared by the lanes of a head,
+            // moves only when a page's score exceeds it by more than 8 (log2 units), so p <= 2^8
+            // and most pages need neither the max reduction nor a rescale of o and l. l_run is
+            // this lane's share of the head's sum, reduced across the head's lanes per piece.
             float sv[NH];
-            float mx = -INFINITY;
+            bool over = false;
 #pragma unroll
             for (int j = 0; j < NH; ++j) {
                 const int idx = lane + 32 * j;
                 sv[j] = idx < NV ? sc[idx] : -INFINITY;
-                mx = fmaxf(mx, sv[j]);
+                over |= sv[j] > m_run + 8.f;
             }
+            if (__any_sync(0xffffffffu, over)) {
+                float mx = -INFINITY;
 #pragma unroll
-            for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = m_run == -INFINITY ? (m_new == -INFINITY ? 1.f : 0.f) : fast_exp2(m_run - m_use);
-            float psum = 0.f;
+                for (int j = 0; j < NH; ++j) mx = fmaxf(mx, sv[j]);
+#pragma unroll
+                for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float m_new = mx > m_run + 8.f ? mx : m_run;
+                // o and l are zero while m_run is -inf
+                const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
+                l_run *= alpha;
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float al = __shfl_sync(0xffffffffu, alpha, hh);
+#pragma unroll
+                    for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
+                }
+                m_run = m_new;
+            }
+            const float m_use = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
             for (int j = 0; j < NH; ++j) {
                 const int idx = lane + 32 * j;
                 const float pj = sv[j] == -INFINITY ? 0.f : fast_exp2(sv[j] - m_use);
                 if (idx < NV) sp[idx] = pj;
-                psum += pj;
+                l_run += pj;
             }
-#pragma unroll
-            for (int off = G; off < 32; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-            l_run = l_run * alpha + psum;
-            m_run = m_new;
             __syncwarp();
-            // o update: rescale, then add this lane's tokens
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float al = __shfl_sync(0xffffffffu, alpha, hh);
-#pragma unroll
-                for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
-            }
+            // o update: add this lane's tokens
             if constexpr (PACKED) {
+                // every token of the page visible (the common case): no per-token masking
+                const bool all_valid = nt >= TPW && tlo <= 0;
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     const int tw = NT * sub + t;
                     const uint4 w = *reinterpret_cast<const uint4*>(vp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2);
                     // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
-                    const bool valid = tw < nt && tw >= tlo;
+                    const bool valid = all_valid || (tw < nt && tw >= tlo);
                     const uint32_t ws[4] = {valid ? w.x : 0u, valid ? w.y : 0u, valid ? w.z : 0u, valid ? w.w : 0u};
                     float2 v2[4];
 #pragma unroll
@@ -521,6 +544,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < QD; ++e) acc_o[hh][e] += __shfl_xor_sync(0xffffffffu, acc_o[hh][e], 16);
                 }
+                // the head's sum: its lanes (lane % G) each hold a share
+#pragma unroll
+                for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float* row = slot + (size_t)(g * G + hh) * kRowF;
