@@ -104,3 +104,37 @@ def test_decode_swa_d256_full_workload(orc):
     ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, pp.window)
     check("o", o, ro)
     check_lse("lse", lse, rl)
+
+
+def test_decode_all_requests_empty():
+    """No request has a cached token: the decode grid does nothing and the merge writes o = 0,
+    lse = -inf for every (request, head)."""
+    pp = synth.paged_from_lengths([0, 0, 0], 32, 8, 128, page_size=16, num_pages=16, seed=1, max_pages=4)
+    o, lse = run(pp)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("lens", [[152 * 16 * 3 + 5], [152 * 16 * 2, 3]])
+def test_decode_one_request_over_every_cta(orc, lens):
+    """A request longer than the grid has CTAs: every CTA holds a piece of it, so the merge
+    folds more than a hundred partial slots in several rounds."""
+    pp = synth.paged_from_lengths(lens, 32, 8, 128, page_size=16, num_pages=1024, seed=len(lens), max_pages=512)
+    compare(orc, pp, 0)
+
+
+@pytest.mark.parametrize("direction", ["rising", "falling"])
+def test_decode_scores_drifting_along_the_context(orc, direction):
+    """Keys scaled by a factor that grows (or shrinks) along the context, so a page's scores keep
+    exceeding the running maximum by far more than the lazy-update threshold (or never do)."""
+    pp = synth.paged_from_lengths([1500, 700, 40], 32, 8, 128, page_size=16, num_pages=256, seed=9, max_pages=128)
+    kc = pp.k_cache.view(np.uint16).copy()
+    kf = (kc.astype(np.uint32) << 16).view(np.float32)
+    for b, L in enumerate(pp.seq_lens):
+        for p in range((int(L) + 15) // 16):
+            pos = p * 16 + np.arange(16)
+            f = 1.0 + pos / 60.0 if direction == "rising" else 1.0 + (int(L) - pos) / 60.0
+            page = pp.block_table[b, p]
+            kf[page] *= f[:, None, None].astype(np.float32)
+    k_new = (kf.view(np.uint32) + 0x8000 >> 16).astype(np.uint16)  # round to bf16
+    pp = synth.Paged(**{**pp.__dict__, "k_cache": k_new.view(pp.k_cache.dtype)})
+    compare(orc, pp, 0)
