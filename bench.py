@@ -632,7 +632,8 @@ def profile_case(args):
       dense_d128: head_dim 128 forward + backward at batch `--batch`;
       merge_cp8_d512: the 8-part merge;
       decode_swa_d256: the sliding-window head_dim 256 decode;
-      decode_d128: the head_dim 128 paged decode (batch 64, Hq 32, Hkv 8)."""
+      decode_d128: the head_dim 128 paged decode (batch 64, Hq 32, Hkv 8);
+      swa_d256: the sliding-window head_dim 256 forward + backward at batch `--batch`."""
     import numpy as np
     import torch
 
@@ -679,6 +680,16 @@ def profile_case(args):
         ls = torch.empty((ps.B, ps.Hq), dtype=torch.float32, device="cuda")
         run = lambda: attn.attn_decode_paged(qs, kcs, vcs, bts, sls, os_, ls, scale=ps.scale, window=ps.window)
         outs = [os_]
+    elif case == "swa_d256":
+        p = synth.dense(args.batch, 32, 16, 8192, 256, 1024, seed=7, outlier_frac=0.01, outlier_scale=30.0)
+        q, k, v, do = (to_dev(x) for x in (p.q, p.k, p.v, p.do))
+        o = torch.empty_like(q)
+        lse = torch.empty((p.B, p.Hq, p.S), dtype=torch.float32, device="cuda")
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        run = lambda: (attn.attn_fwd(q, k, v, o, lse, window=p.window, scale=p.scale),
+                       attn.attn_bwd(q, k, v, o, lse, do, dq, dk, dv, window=p.window, scale=p.scale))
+        outs = [o, dq, dk, dv]
+        extra = {"B": p.B}
     elif case == "decode_d128":
         pd = synth.decode_paged_d128(seed=7)
         qd, kcd, vcd = to_dev(pd.q), to_dev(pd.k_cache), to_dev(pd.v_cache)
