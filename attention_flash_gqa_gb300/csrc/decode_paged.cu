@@ -141,8 +141,11 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
-    // the merge kernel that follows may be scheduled now: it waits for this grid's completion
-    // before it reads anything, and its small CTAs fit beside this one
+    // Launched with programmatic stream serialisation: wait for the previous kernel on the stream
+    // to finish (and its writes to be visible) before touching anything, so the call keeps plain
+    // stream order while its CTAs become resident and start early. Then let the merge kernel that
+    // follows be scheduled: it waits for this grid's completion before it reads its outputs.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
@@ -600,6 +603,9 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(MergeArgs m
     constexpr int kRowF = DC::kRowF;
     constexpr int SB = 8;
     constexpr int DI = 8;  // dims per thread
+    // a kernel launched after this one with programmatic serialisation may be scheduled now (it
+    // waits for this grid's completion before it reads anything)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.x;
     const int nh = m.hb * G / gridDim.z;  // heads of this CTA
     const int h0 = blockIdx.y * m.hb * G + blockIdx.z * nh;
@@ -721,15 +727,24 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream) {
     auto go = [&](auto kern, auto merge, int threads) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        ProfMark m = prof_begin(stream, L.D == 128 ? "decode_paged" : "decode_paged_d256");
-        kern<<<dim3(L.grid, a.nhb), threads, smem, stream>>>(L.tk, L.tv, a);
-        prof_end(stream, m);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        // the merge may start while the decode grid still runs (it waits for that grid's
-        // completion on the device), which hides its launch behind the decode tail
+        // Both kernels are launched with programmatic stream serialisation: each may be scheduled
+        // while its predecessor on the stream still runs, and waits on the device
+        // (griddepcontrol.wait) for that predecessor's completion before it reads anything the
+        // predecessor may write.
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t dcfg = {};
+        dcfg.gridDim = dim3(L.grid, a.nhb);
+        dcfg.blockDim = dim3(threads);
+        dcfg.dynamicSmemBytes = smem;
+        dcfg.stream = stream;
+        dcfg.attrs = attr;
+        dcfg.numAttrs = 1;
+        ProfMark m = prof_begin(stream, L.D == 128 ? "decode_paged" : "decode_paged_d256");
+        e = cudaLaunchKernelEx(&dcfg, kern, L.tk, L.tv, a);
+        prof_end(stream, m);
+        if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         const int nh = a.hb * G;  // query heads of a head block
         int nz = nh * (L.D / 8) / kMergeThreads;
