@@ -401,14 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[buf]), (j >> 1) & 1, abort_flag, a.status, 0x15));
             if (!ok) break;
             tc_fence_after();
+            // the row's 128 scores: all four loads in flight under one wait
             float s[128];
+            {
+                uint32_t raw[4][32];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                tmem_ld32(tS0 + buf * 128 + c * 32 + lane_base, raw);
+                for (int c = 0; c < 4; ++c) tmem_ld32(tS0 + buf * 128 + c * 32 + lane_base, raw[c]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[e]);
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[c][e]);
             }
             const int key0 = (t_begin + j) * kBKV;
             const bool edge = (key0 + kBKV - 1 > qp0) || (a.window > 0 && qp0 + kBQ - 1 - key0 >= a.window) ||
@@ -421,9 +424,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!allowed) s[c] = -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            // row max and row sum over eight independent partials: a single thread owns the row,
+            // so one long dependent chain would be latency, not throughput
+            float m8[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < 128; c += 8)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             const float m_tile = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
             float alpha = 1.f;
             const bool moved = m_tile > m_ref + kRescaleLog2;
@@ -432,15 +443,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = m_tile;
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            float rowsum = 0.f;
+            float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[64];
 #pragma unroll
             for (int c = 0; c < 128; c += 2) {
                 const float p0 = fast_exp2(fmaf(s[c], a.scale_log2, -m_use));
                 const float p1 = fast_exp2(fmaf(s[c + 1], a.scale_log2, -m_use));
-                rowsum += p0 + p1;
+                rs[(c >> 1) & 7] += p0 + p1;
                 pk[c >> 1] = pack_bf16x2(p0, p1);
             }
+            const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
             l = l * alpha + rowsum;
             if (j > 0 && __any_sync(0xffffffffu, moved)) {
                 // rescale O: P(j-1) V(j-1) must be complete (phase j-2 is, by s_full(j))
