@@ -1,4 +1,4 @@
-// Causal / sliding-window attention forward on tcgen05 tensor cores (D = 256 or 512).
+// Causal / sliding-window attention forward on tcgen05 tensor cores (D = 64, 128, 256 or 512).
 //
 // Sources: "Gemma4 FFPA attention backend support ..." (operator table: fused
 // attention instead of the MATH path that materialises S x S; "Integration": head_dim
@@ -7,26 +7,29 @@
 //
 // One CTA computes a 128-query tile of one head against all keys it may see, for one
 // 256-wide half of the output columns (D = 512 runs two CTAs per tile, each recomputing
-// the full-width scores; D = 256 runs one). Tensor memory (512 columns x 128 lanes):
-//   cols [0, 256)   O accumulator, fp32, row i = lane i
-//   cols [256, 384) S buffer 0, [384, 512) S buffer 1 (double-buffered scores); once a
-//                   buffer's scores are in registers, the bf16 P tile of that step is written
-//                   over its first 64 columns and read from there as the A operand of P V
+// the full-width scores; D <= 256 runs one). Tensor memory (512 columns x 128 lanes):
+//   O accumulator, fp32, row i = lane i: cols [0, 256) (D >= 256), [0, D) otherwise
+//   score buffers of 128 columns at the top: two at D >= 256, three at D <= 128 (the issuer
+//   then runs two softmax steps ahead). Once a buffer's scores are in registers, the bf16 P
+//   tile of that step is written over the first 32 columns of each 64-column half and read
+//   from there as the A operand of P V
 // Shared memory: the Q tile (resident) and a ring of 32 KB slots (one slot = 128 rows x
 // 128 columns of K or V as two 128-byte-swizzled 64-column sub-tiles, filled by TMA):
-// 5 slots at D = 256, 3 at D = 512.
+// 5 slots at D = 256, 3 at D = 512; 16 KB slots of one sub-tile at D = 64.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer (one thread): Q once, then K/V slots in MMA order. Over a
 //               paged cache the whole warp works: eight lanes fetch one tile's page ids a
 //               tile ahead and each issues its page's box into every slot of the tile, and
 //               the warp zeroes the last tile's V rows past the sequence end before its P V
 //   warp 1      TMEM owner; one thread issues every UMMA and commit
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r). Masking, fp32 online
-//               softmax in the log2 domain with lazy rescaling (the running max moves
-//               only when a tile's max exceeds it by more than 2^8), P -> TMEM, O
-//               rescale in TMEM (only then do they wait for the previous P V), and the
-//               epilogue (O / l -> bf16, lse).
+//   warps 2..9  softmax: warps w and w + 4 share query rows 32 (w & 3) .. (TMEM lane quarter
+//               w & 3), one thread per row, each warp on one half of the step's 128 keys.
+//               Masking, fp32 online softmax in the log2 domain with lazy rescaling (the
+//               running max moves only when a tile's max exceeds it by more than 2^8; the
+//               pair exchanges its row maxima through shared memory), P -> TMEM, O rescale
+//               in TMEM (only then do they wait for the previous P V), and the epilogue
+//               (O / l -> bf16, lse), each warp on half of the O columns.
 // KV tiles outside the causal / window range are never loaded (tile-granular skipping);
 // only tiles that straddle the diagonal, the window edge or the sequence end are masked.
 #include <cuda_runtime.h>
@@ -38,13 +41,17 @@ namespace attn {
 namespace {
 
 constexpr int kBQ = 128, kBKV = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kSubBytes = 16384;  // 128 rows x 64 bf16
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int DQK>
 struct FwdCfg {
     static constexpr int kDV = DQK < 256 ? DQK : 256;      // O columns per CTA
+    // score buffers in tensor memory: three when O takes at most 128 of the 512 columns, so the
+    // issuer runs two softmax steps ahead instead of one
+    static constexpr int kSBuf = kDV <= 128 ? 3 : 2;
     static constexpr int kSubs = DQK >= 128 ? 2 : 1;        // 64-column sub-tiles per slot
     static constexpr int kSlotCols = 64 * kSubs;
     static constexpr uint32_t kSlotBytes = kSubs * kSubBytes;
@@ -54,7 +61,8 @@ struct FwdCfg {
     static constexpr int kStages = DQK == 512 ? 3 : DQK == 256 ? 5 : DQK == 128 ? 6 : 12;
     static constexpr uint32_t kQBytes = DQK * 256;  // 128 rows x DQK bf16
     static constexpr uint32_t kOffSlots = kQBytes;
-    static constexpr uint32_t kOffBar = kOffSlots + kStages * kSlotBytes;
+    static constexpr uint32_t kOffXch = kOffSlots + kStages * kSlotBytes;  // [2 halves][128 rows] fp32
+    static constexpr uint32_t kOffBar = kOffXch + 1024;
     static constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
     // paged slots: the slot's sub-tiles interleaved per 8-row group
     static constexpr uint32_t kPagedGroupStride = 1024 * kSubs;
@@ -130,10 +138,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = bars;                     // [kStages]
     uint64_t* empty = bars + C::kStages;       // [kStages]
     uint64_t* q_full = bars + 2 * C::kStages;  // 1
-    uint64_t* s_full = q_full + 1;             // [2]
-    uint64_t* p_full = s_full + 2;             // 1
-    uint64_t* pv_done = p_full + 1;            // 1
-    uint64_t* mma_idle = pv_done + 1;          // 1
+    // per score buffer b (step j uses b = j % kSBuf): one pending phase at most on each, since a
+    // buffer's next step cannot start before the issuer has consumed its current one
+    uint64_t* s_full = q_full + 1;             // [3]: S(j) in TMEM
+    uint64_t* p_full = s_full + 3;             // [3]: P(j) in TMEM (all softmax threads)
+    uint64_t* pv_done = p_full + 3;            // [3]: P V(j) complete
+    uint64_t* mma_idle = pv_done + 3;          // 1
     uint64_t* vfix = mma_idle + 1;             // 1 (paged): the last tile's V rows past the end are zeroed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vfix + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -146,10 +156,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(q_full), 1);
-        mbar_init(smem_u32(&s_full[0]), 1);
-        mbar_init(smem_u32(&s_full[1]), 1);
-        mbar_init(smem_u32(p_full), 128);
-        mbar_init(smem_u32(pv_done), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&s_full[b]), 1);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&p_full[b]), kSoftmaxThreads);
+        for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&pv_done[b]), 1);
         mbar_init(smem_u32(mma_idle), 1);
         mbar_init(smem_u32(vfix), 1);
         *abort_flag = 0;
@@ -162,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    const uint32_t tO = tbase, tS0 = tbase + 256;
+    const uint32_t tO = tbase, tS0 = tbase + 512 - C::kSBuf * 128;
 
     // keys past the end in the last tile (paged: their cache rows may hold any bits)
     const bool tail_fix = PAGED && (t_end * kBKV > L);
@@ -230,16 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             v_cur = v_nxt;
             v_nxt = vt + 1 < n ? page_id(t_begin + vt + 1) : 0;
         };
-        ok = load_k();
-        next_k();
-        if (ok && n > 1) {
+        // the issuer's order: K(0) .. K(kSBuf - 1), then V(j), K(j + kSBuf) for every step j
+        for (int b = 0; ok && b < C::kSBuf && b < n; ++b) {
             ok = load_k();
             next_k();
         }
         for (int j = 0; ok && j < n; ++j) {
             ok = load_v();
             next_v();
-            if (ok && j + 2 < n) {
+            if (ok && j + C::kSBuf < n) {
                 ok = load_k();
                 next_k();
             }
@@ -305,11 +313,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!load_chunk(&tv, dv0 + c * C::kSlotCols, seq_start + (t_begin + t) * kBKV)) return false;
                 return true;
             };
-            ok = load_k(0);
-            if (ok && n > 1) ok = load_k(1);
+            // the issuer's order: K(0) .. K(kSBuf - 1), then V(j), K(j + kSBuf) for every step j
+            for (int b = 0; ok && b < C::kSBuf && b < n; ++b) ok = load_k(b);
             for (int j = 0; ok && j < n; ++j) {
                 ok = load_v(j);
-                if (ok && j + 2 < n) ok = load_k(j + 2);
+                if (ok && j + C::kSBuf < n) ok = load_k(j + C::kSBuf);
             }
             // Drain: wait (bounded) for the last copy issued into every slot.
             const int issued = round * C::kStages + slot;
@@ -363,26 +371,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                     }
                     const uint32_t vslot = sSlots + slot * C::kSlotBytes;
-                    const uint32_t tP = tS0 + (j & 1) * 128;  // P of step j, packed bf16 pairs
-                    for (int kk = 0; kk < 8; ++kk) {          // 16 keys per step
+                    // P of step j, packed bf16 pairs: keys 64 hf .. 64 hf + 63 at columns 64 hf .. 64 hf + 31
+                    const uint32_t tP = tS0 + (j % C::kSBuf) * 128;
+                    for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
                         const uint64_t bd =
                             PAGED ? sdesc_sw128(vslot + kk * 2 * C::kPagedGroupStride, 1024, C::kPagedGroupStride)
                                   : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
-                        umma_bf16_ts(tO + c * C::kSlotCols, tP + kk * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ts(tO + c * C::kSlotCols, tP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     release_slot();
                 }
-                umma_commit(smem_u32(pv_done));
+                umma_commit(smem_u32(&pv_done[j % C::kSBuf]));
                 return true;
             };
-            if (ok) ok = issue_s(0);
-            if (ok && n > 1) ok = issue_s(1);
+            for (int b = 0; ok && b < C::kSBuf && b < n; ++b) ok = issue_s(b);
             for (int j = 0; ok && j < n; ++j) {
-                ok = mbar_wait(smem_u32(p_full), j & 1, abort_flag, a.status, 0x14);
+                ok = mbar_wait(smem_u32(&p_full[j % C::kSBuf]), (j / C::kSBuf) & 1, abort_flag, a.status, 0x14);
                 if (!ok) break;
                 tc_fence_after();
                 ok = issue_pv(j);
-                if (ok && j + 2 < n) ok = issue_s(j & 1);
+                // S(j + kSBuf) over the buffer P(j) came from: the pipe runs in order, so P V(j)
+                // has read P(j) first
+                if (ok && j + C::kSBuf < n) ok = issue_s(j % C::kSBuf);
             }
             // every issued UMMA has finished before TMEM may be released
             umma_commit(smem_u32(mma_idle));
@@ -390,52 +401,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------------------- softmax --------------------------------------
+        // Warps w and w + 4 share TMEM lane quarter w & 3 (query rows 32 (w & 3) ..); warp half
+        // hf takes the step's score columns (keys) 64 hf .. 64 hf + 63 and the O columns
+        // kDV/2 hf .. kDV/2 hf + kDV/2 - 1 of every rescale and of the epilogue. The pair
+        // exchanges its row maxima through shared memory every step (named barrier 1 + quarter,
+        // 64 threads) and its row sums once at the end. Every exit decision is taken jointly
+        // (bar.red.and), so neither warp leaves its partner waiting at a barrier.
         const int quad = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int r = quad * 32 + lane;  // query row within the tile == TMEM lane
         const int qi = qp0 + r;          // position of the query in its sequence
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint32_t pair_bar = 1 + quad;
+        float* xch = reinterpret_cast<float*>(smem + C::kOffXch);  // [2][128]
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const int buf = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s_full[buf]), (j >> 1) & 1, abort_flag, a.status, 0x15));
-            if (!ok) break;
-            tc_fence_after();
-            // the row's 128 scores: all four loads in flight under one wait
-            float s[128];
-            {
-                uint32_t raw[4][32];
+            const int buf = j % C::kSBuf;
+            bool okw = __all_sync(0xffffffffu,
+                                  mbar_wait(smem_u32(&s_full[buf]), (j / C::kSBuf) & 1, abort_flag, a.status, 0x15));
+            float s[64];
+            float mx = -INFINITY;
+            if (okw) {
+                tc_fence_after();
+                {
+                    uint32_t raw[2][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tS0 + buf * 128 + c * 32 + lane_base, raw[c]);
-                tmem_ld_wait();
+                    for (int c = 0; c < 2; ++c) tmem_ld32(tS0 + buf * 128 + 64 * hf + c * 32 + lane_base, raw[c]);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[c][e]);
-            }
-            const int key0 = (t_begin + j) * kBKV;
-            const bool edge = (key0 + kBKV - 1 > qp0) || (a.window > 0 && qp0 + kBQ - 1 - key0 >= a.window) ||
-                              (key0 + kBKV > L);
-            if (edge) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int key = key0 + c;
-                    const bool allowed = key <= qi && key < L && (a.window <= 0 || qi - key < a.window);
-                    if (!allowed) s[c] = -INFINITY;
+                        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(raw[c][e]);
                 }
+                const int key0 = (t_begin + j) * kBKV + 64 * hf;
+                const bool edge = (key0 + 63 > qp0) || (a.window > 0 && qp0 + kBQ - 1 - key0 >= a.window) ||
+                                  (key0 + 64 > L);
+                if (edge) {
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const int key = key0 + c;
+                        const bool allowed = key <= qi && key < L && (a.window <= 0 || qi - key < a.window);
+                        if (!allowed) s[c] = -INFINITY;
+                    }
+                }
+                // this half's row max over eight independent partials
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+                for (int c = 8; c < 64; c += 8)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                xch[hf * 128 + r] = mx;
             }
-            // row max and row sum over eight independent partials: a single thread owns the row,
-            // so one long dependent chain would be latency, not throughput
-            float m8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) m8[i] = s[i];
-#pragma unroll
-            for (int c = 8; c < 128; c += 8)
-#pragma unroll
-                for (int i = 0; i < 8; ++i) m8[i] = fmaxf(m8[i], s[c + i]);
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            const float m_tile = mx * a.scale_log2;  // -inf stays -inf (scale > 0)
+            ok = named_bar_and(pair_bar, 64, okw);
+            if (!ok) break;
+            mx = fmaxf(mx, xch[(1 - hf) * 128 + r]);  // the row's max over all 128 keys
+            named_bar_sync(pair_bar, 64);             // both read before the buffer is reused
+            const float m_tile = mx * a.scale_log2;   // -inf stays -inf (scale > 0)
             float alpha = 1.f;
             const bool moved = m_tile > m_ref + kRescaleLog2;
             if (moved) {
@@ -444,24 +470,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
             float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[64];
+            uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
+            for (int c = 0; c < 64; c += 2) {
                 const float p0 = fast_exp2(fmaf(s[c], a.scale_log2, -m_use));
                 const float p1 = fast_exp2(fmaf(s[c + 1], a.scale_log2, -m_use));
                 rs[(c >> 1) & 7] += p0 + p1;
                 pk[c >> 1] = pack_bf16x2(p0, p1);
             }
             const float rowsum = ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-            l = l * alpha + rowsum;
+            l = l * alpha + rowsum;  // this half's share of the row sum
+            // the pair takes the same branches: `moved` depends on the row only
             if (j > 0 && __any_sync(0xffffffffu, moved)) {
-                // rescale O: P(j-1) V(j-1) must be complete (phase j-2 is, by s_full(j))
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done), (j - 1) & 1, abort_flag, a.status, 0x16));
+                // rescale O: P V(j-1), and so every earlier P V (the MMA pipe completes in order),
+                // must be complete. Its barrier has no older phase pending: s_full(j) implies
+                // P V(j - kSBuf) is complete.
+                const int jp = j - 1;
+                okw = __all_sync(0xffffffffu, mbar_wait(smem_u32(&pv_done[jp % C::kSBuf]), (jp / C::kSBuf) & 1,
+                                                        abort_flag, a.status, 0x16));
+                ok = named_bar_and(pair_bar, 64, okw);
                 if (!ok) break;
                 tc_fence_after();
                 const float f = moved ? alpha : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < C::kDV / 32; ++c) {
+                for (int c = hf * (C::kDV / 64); c < (hf + 1) * (C::kDV / 64); ++c) {
                     uint32_t raw[32];
                     tmem_ld32(tO + c * 32 + lane_base, raw);
                     tmem_ld_wait();
@@ -469,39 +501,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int e = 0; e < 32; ++e) raw[e] = __float_as_uint(__uint_as_float(raw[e]) * f);
                     tmem_st32(tO + c * 32 + lane_base, raw);
                 }
-            } else if (j == n - 1 && j > 0) {
-                // last step: P(j-1) V(j-1) completes before this P is released, so the epilogue
-                // waits on exactly one pending phase of pv_done (no parity aliasing)
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(pv_done), (j - 1) & 1, abort_flag, a.status, 0x1d));
-                if (!ok) break;
             }
-            // P row r -> the first 64 columns of this step's S buffer (S is in registers)
-            {
-                uint32_t w[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pk[e];
-                tmem_st32(tS0 + buf * 128 + lane_base, w);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) w[e] = pk[32 + e];
-                tmem_st32(tS0 + buf * 128 + 32 + lane_base, w);
-            }
+            // P: this half's 64 keys -> the first 32 columns of its half of the step's S buffer
+            // (its own scores, already in registers)
+            tmem_st32(tS0 + buf * 128 + 64 * hf + lane_base, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(p_full));
+            mbar_arrive(smem_u32(&p_full[buf]));
         }
         // ---- epilogue: O / l -> bf16, lse -------------------------------------------------
-        // the last P V (phase n-1); every earlier one is complete (waited in the last step)
-        if (ok) ok = mbar_wait(smem_u32(pv_done), (n - 1) & 1, abort_flag, a.status, 0x17);
-        ok = __all_sync(0xffffffffu, ok);
+        // the last P V, and so every earlier one; its barrier has no older phase pending
+        bool okw = ok;
+        if (okw)
+            okw = mbar_wait(smem_u32(&pv_done[(n - 1) % C::kSBuf]), ((n - 1) / C::kSBuf) & 1, abort_flag, a.status, 0x17);
+        okw = __all_sync(0xffffffffu, okw);
+        if (ok) xch[hf * 128 + r] = l;  // the exchange buffer is free: both read it before the last barrier
+        ok = named_bar_and(pair_bar, 64, ok && okw);
         tc_fence_after();
         if (ok) {
+            l += xch[(1 - hf) * 128 + r];
             const int qrow = q0 + r;  // query row index within the sequence's rows
             const bool row_ok = qrow < nq;
             const bool packed = PAGED || a.cu_seqlens;
             const float inv = l > 0.f ? 1.f / l : 0.f;
             uint16_t* orow = a.o + ((size_t)(packed ? seq_start + qrow : seq * a.S + qrow) * a.Hq + h) * a.D + dv0;
 #pragma unroll 1
-            for (int c = 0; c < C::kDV / 32; ++c) {
+            for (int c = hf * (C::kDV / 64); c < (hf + 1) * (C::kDV / 64); ++c) {
                 uint32_t raw[32];
                 tmem_ld32(tO + c * 32 + lane_base, raw);
                 tmem_ld_wait();
@@ -517,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (row_ok && split == 0) {
+            if (row_ok && split == 0 && hf == 0) {
                 const float lse = l > 0.f ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
                 const size_t li = packed ? (size_t)h * a.T + seq_start + qrow : ((size_t)seq * a.Hq + h) * a.S + qrow;
                 a.lse[li] = lse;
