@@ -100,3 +100,23 @@ def test_backward_small_d_varlen(orc, D):
     check("dq", to_np(dq), rdq)
     check("dk", to_np(dk), rdk)
     check("dv", to_np(dv), rdv)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256, 512])
+@pytest.mark.parametrize("W", [0, 300])
+def test_forward_running_max_keeps_moving(orc, D, W):
+    """Keys scaled up along the sequence, so the scores of every later key tile exceed the
+    running maximum by far more than the lazy-rescale threshold: O is rescaled in tensor memory
+    on almost every step (with two score buffers at D >= 256 and three at D <= 128)."""
+    p = synth.dense(1, 4, 2, 700, D, W, seed=D + W, with_do=False)
+    kb = p.k.view(np.uint16).copy()
+    kf = (kb.astype(np.uint32) << 16).view(np.float32)
+    kf *= (1.0 + np.arange(p.S, dtype=np.float32) / 40.0)[None, :, None, None]
+    k_new = ((kf.view(np.uint32) + 0x8000) >> 16).astype(np.uint16)
+    q, k, v = to_dev(p.q), to_dev(k_new.view(p.k.dtype)), to_dev(p.v)
+    o, lse = attn.attn_fwd(q, k, v, window=W, scale=p.scale)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.fwd(p.q, k_new.view(p.k.dtype), p.v, p.scale, 1, W)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
