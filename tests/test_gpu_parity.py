@@ -73,6 +73,19 @@ def test_d512_window(orc):
     compare_dense(orc, synth.dense(1, 4, 1, 400, 512, 200, seed=9))
 
 
+@pytest.mark.parametrize("D,scale,window", [(512, 0.3, 0), (256, 0.02, 0), (256, 0.15, 90), (128, 0.5, 0), (64, 0.05, 40)])
+def test_scale_other_than_inverse_sqrt_d(orc, D, scale, window):
+    """A softmax scale that is not 1/sqrt(D), larger and smaller: the scale must enter S, the
+    saved lse, dS and dK (every place it appears), not a constant derived from D."""
+    compare_dense(orc, synth.dense(1, 4, 2, 260, D, window, seed=D + window, scale=scale))
+
+
+@pytest.mark.parametrize("D", [512, 256])
+def test_wide_gqa_group(orc, D):
+    """16 query heads over one KV head: the backward sums dK / dV over the whole group."""
+    compare_dense(orc, synth.dense(1, 16, 1, 200, D, 0, seed=16 + D))
+
+
 def test_forward_is_deterministic():
     p = synth.dense(1, 4, 2, 300, 512, 0, seed=4, with_do=False)
     q, k, v = to_dev(p.q), to_dev(p.k), to_dev(p.v)
@@ -86,6 +99,28 @@ def test_forward_is_deterministic():
 def test_varlen(orc, D, window):
     lens = [1, 127, 128, 129, 300, 0, 513]
     vp = synth.varlen_from_lengths(lens, 4, 1, D, window, seed=D + window)
+    q, k, v, do = (to_dev(x) for x in (vp.q, vp.k, vp.v, vp.do))
+    cu = torch.from_numpy(vp.cu_seqlens).cuda()
+    o, lse = attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, window=window, scale=vp.scale)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, lse, do, window=window, scale=vp.scale, cu_seqlens=cu,
+                               max_seqlen=vp.max_seqlen)
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    ro, rl = orc.fwd_varlen(vp.q, vp.k, vp.v, vp.cu_seqlens, vp.scale, 1, window)
+    rdq, rdk, rdv, _ = orc.bwd_varlen(vp.q, vp.k, vp.v, vp.do, vp.cu_seqlens, vp.scale, 1, window)
+    check("o", to_np(o), ro)
+    check_lse("lse", to_np(lse), rl)
+    check("dq", to_np(dq), rdq)
+    check("dk", to_np(dk), rdk)
+    check("dv", to_np(dv), rdv)
+
+
+@pytest.mark.parametrize("D,window", [(512, 0), (256, 64)])
+def test_varlen_many_short_sequences(orc, D, window):
+    """Forty sequences, many shorter than a tile, some empty or of one or two tokens: every query
+    tile stays inside its own sequence and every key range ends at its own sequence's end."""
+    lens = [int(x) for x in np.random.default_rng(D + window).choice([0, 1, 2, 3, 17, 64, 127, 128, 129, 200], 40)]
+    vp = synth.varlen_from_lengths(lens, 4, 2, D, window, seed=D + 1)
     q, k, v, do = (to_dev(x) for x in (vp.q, vp.k, vp.v, vp.do))
     cu = torch.from_numpy(vp.cu_seqlens).cuda()
     o, lse = attn.attn_fwd_varlen(q, k, v, cu, vp.max_seqlen, window=window, scale=vp.scale)
