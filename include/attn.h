@@ -60,7 +60,7 @@ typedef uint16_t attn_bf16; /* raw bf16 bit pattern */
 typedef enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,    /* null pointer, negative size, Hq % Hkv != 0, bad scale ... */
-    ATTN_ERR_UNSUPPORTED = 2,    /* a legal problem this build has no kernel for (e.g. D = 64) */
+    ATTN_ERR_UNSUPPORTED = 2,    /* a legal problem the library has no kernel for (e.g. D = 96) */
     ATTN_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
     ATTN_ERR_WORKSPACE = 4,      /* workspace missing or smaller than attn_workspace_size() */
     ATTN_ERR_LAUNCH = 5,         /* the CUDA runtime refused a launch or a tensor map */
