@@ -138,3 +138,18 @@ def test_decode_scores_drifting_along_the_context(orc, direction):
     k_new = (kf.view(np.uint32) + 0x8000 >> 16).astype(np.uint16)  # round to bf16
     pp = synth.Paged(**{**pp.__dict__, "k_cache": k_new.view(pp.k_cache.dtype)})
     compare(orc, pp, 0)
+
+
+def test_decode_max_batch_tiny_contexts(orc):
+    """The largest batch the call accepts (4096 requests), contexts of 0 to 33 tokens: every CTA's
+    range spans many requests, most of them in one page, some empty."""
+    lens = [int(x) for x in np.random.default_rng(4096).choice([0, 1, 2, 5, 15, 16, 17, 33], 4096)]
+    pp = synth.paged_from_lengths(lens, 8, 2, 128, page_size=16, num_pages=8192, seed=40, max_pages=3)
+    compare(orc, pp, 0)
+
+
+@pytest.mark.parametrize("window", [1, 17, 300])
+def test_decode_window_head_blocks_group8(orc, window):
+    """A GQA group of 8 at head_dim 128 (KV heads in blocks of 4) with a sliding window."""
+    pp = synth.paged_from_lengths(LENS, 64, 8, 128, page_size=16, num_pages=512, seed=window, max_pages=160)
+    compare(orc, pp, window)
