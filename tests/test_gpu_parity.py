@@ -95,7 +95,7 @@ def test_forward_is_deterministic():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
 
 
-@pytest.mark.parametrize("D,window", [(512, 0), (256, 0), (256, 100)])
+@pytest.mark.parametrize("D,window", [(512, 0), (512, 150), (256, 0), (256, 100)])
 def test_varlen(orc, D, window):
     lens = [1, 127, 128, 129, 300, 0, 513]
     vp = synth.varlen_from_lengths(lens, 4, 1, D, window, seed=D + window)
