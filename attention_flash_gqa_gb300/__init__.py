@@ -194,8 +194,9 @@ def attn_fwd(q, k, v, o=None, lse=None, *, causal: bool = True, window: int = 0,
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
-    rc = load_library().attn_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv,
-                                 S, D, scale, int(causal), int(window), None, 0, _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_fwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv,
+                                     S, D, scale, int(causal), int(window), None, 0, _stream_ptr(stream, q.device))
     _check(rc, "attn_fwd")
     return o, lse
 
@@ -214,9 +215,10 @@ def attn_fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, o=None, lse=None, *, c
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    rc = load_library().attn_fwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse),
-                                        _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, D,
-                                        scale, int(causal), int(window), None, 0, _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_fwd_varlen(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse),
+                                            _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, int(max_seqlen), Hq, Hkv, D,
+                                            scale, int(causal), int(window), None, 0, _stream_ptr(stream, q.device))
     _check(rc, "attn_fwd_varlen")
     return o, lse
 
@@ -237,10 +239,11 @@ def attn_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, cu_q, max_q_len: 
         o = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, T), dtype=torch.float32, device=q.device)
-    rc = load_library().attn_fwd_paged(
-        _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
-        _ptr(cu_q), _bf16(o, "o"), _ptr(lse), cu_q.numel() - 1, T, int(max_q_len), Hq, Hkv, D, page_size,
-        block_table.shape[1], num_pages, scale, int(causal), int(window), _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_fwd_paged(
+            _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
+            _ptr(cu_q), _bf16(o, "o"), _ptr(lse), cu_q.numel() - 1, T, int(max_q_len), Hq, Hkv, D, page_size,
+            block_table.shape[1], num_pages, scale, int(causal), int(window), _stream_ptr(stream, q.device))
     _check(rc, "attn_fwd_paged")
     return o, lse
 
@@ -265,8 +268,9 @@ def attn_merge_lse(o_parts, lse_parts, o=None, lse=None, *, stream=None):
         o = torch.empty(o_parts.shape[1:], dtype=torch.bfloat16, device=o_parts.device)
     if lse is None:
         lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
-    rc = load_library().attn_merge_lse(_bf16(o_parts, "o_parts"), _ptr(lse_parts), _bf16(o, "o"), _ptr(lse), P, B,
-                                       S, H, D, _stream_ptr(stream, o_parts.device))
+    with torch.cuda.device(o_parts.device):  # the library works on the current device
+        rc = load_library().attn_merge_lse(_bf16(o_parts, "o_parts"), _ptr(lse_parts), _bf16(o, "o"), _ptr(lse), P, B,
+                                           S, H, D, _stream_ptr(stream, o_parts.device))
     _check(rc, "attn_merge_lse")
     return o, lse
 
@@ -291,11 +295,12 @@ def attn_bwd(q, k, v, o, lse, dO, dq=None, dk=None, dv=None, *, causal: bool = T
     need = attn_workspace_size(ATTN_OP_BWD if cu_seqlens is None else ATTN_OP_BWD_VARLEN, B, Hq, Hkv, S, D, nseq)
     if workspace is None:
         workspace = _workspace(need, q.device, False, "bwd")
-    rc = load_library().attn_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse),
-                                 _bf16(dO, "dO"), _bf16(dq, "dQ"), _bf16(dk, "dK"), _bf16(dv, "dV"), B, Hq, Hkv, S, D,
-                                 scale, int(causal), int(window), _ptr(cu_seqlens), nseq, int(max_seqlen),
-                                 _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                 _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_bwd(_bf16(q, "q"), _bf16(k, "k"), _bf16(v, "v"), _bf16(o, "o"), _ptr(lse),
+                                     _bf16(dO, "dO"), _bf16(dq, "dQ"), _bf16(dk, "dK"), _bf16(dv, "dV"), B, Hq, Hkv, S, D,
+                                     scale, int(causal), int(window), _ptr(cu_seqlens), nseq, int(max_seqlen),
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream_ptr(stream, q.device))
     _check(rc, "attn_bwd")
     return dq, dk, dv
 
@@ -319,11 +324,12 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o=None, lse=No
     need = attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D)
     if workspace is None:
         workspace = _workspace(need, q.device, False, "decode")
-    rc = load_library().attn_decode_paged(_bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
-                                          _ptr(block_table), _ptr(seq_lens), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D,
-                                          page_size, block_table.shape[1], num_pages, scale, int(window),
-                                          _ptr(workspace),
-                                          workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_decode_paged(_bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"),
+                                              _ptr(block_table), _ptr(seq_lens), _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D,
+                                              page_size, block_table.shape[1], num_pages, scale, int(window),
+                                              _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _stream_ptr(stream, q.device))
     _check(rc, "attn_decode_paged")
     return o, lse
 
@@ -344,9 +350,10 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, block_table, seq_lens, o, lse
     for t, n in ((block_table, "block_table"), (seq_lens, "seq_lens")):
         if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous int32 CUDA tensor")
-    rc = load_library().attn_decode_paged_noalloc(
-        _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
-        _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, scale, int(window),
-        _stream_ptr(stream, q.device))
+    with torch.cuda.device(q.device):  # the library works on the current device
+        rc = load_library().attn_decode_paged_noalloc(
+            _bf16(q, "q"), _bf16(k_cache, "k_cache"), _bf16(v_cache, "v_cache"), _ptr(block_table), _ptr(seq_lens),
+            _bf16(o, "o"), _ptr(lse), B, Hq, Hkv, D, page_size, block_table.shape[1], num_pages, scale, int(window),
+            _stream_ptr(stream, q.device))
     _check(rc, "attn_decode_paged_noalloc")
     return o, lse

@@ -153,9 +153,16 @@ int decode_grid_cap(int nhb) { return attn::decode_max_grid() / nhb > 1 ? attn::
 // Decode workspace: the split partials (slot (b + k) * 2 + half for CTA k of a head block, every
 // head block writing only its own heads). Every call writes all of it that it reads: contents on
 // entry do not matter.
+// Returns 0 for a problem the decode kernels do not take (its call is rejected before any use).
+bool decode_shape_ok(int Hq, int Hkv, int D) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return false;
+    const int G = Hq / Hkv;
+    return D == 128 ? (G == 1 || G == 2 || G == 4 || G == 8) : D == 256 ? (G == 1 || G == 2 || G == 4) : false;
+}
 size_t decode_ws(int B, int Hq, int Hkv, int D) {
-    const int nhb = Hkv > 0 && D > 0 && Hq > 0 ? Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv) : 1;
-    return align256((size_t)(B + decode_grid_cap(nhb)) * 2 * Hq * attn::decode_row_floats(D > 0 ? D : 0) * 4);
+    if (B < 0 || !decode_shape_ok(Hq, Hkv, D)) return 0;
+    const int nhb = Hkv / attn::decode_heads_per_unit(Hkv, D, Hq / Hkv);
+    return align256((size_t)(B + decode_grid_cap(nhb)) * 2 * Hq * attn::decode_row_floats(D) * 4);
 }
 
 // 3-D map over a paged cache [num_pages * 16 tokens, heads, dim]: box = dim x hb heads x 16 tokens,
@@ -427,8 +434,7 @@ int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_b
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    const bool groups_ok = D == 128 ? (G == 1 || G == 2 || G == 4 || G == 8) : (G == 1 || G == 2 || G == 4);
-    if ((D != 128 && D != 256) || !groups_ok || page_size != 16 || Hkv > 256 || B > 4096 || num_pages > (1 << 26))
+    if (!decode_shape_ok(Hq, Hkv, D) || page_size != 16 || Hkv > 256 || B > 4096 || num_pages > (1 << 26))
         return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse) ||
         (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))

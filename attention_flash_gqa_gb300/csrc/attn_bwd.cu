@@ -106,6 +106,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         seq_start = a.cu_seqlens[seq];
         L = a.cu_seqlens[seq + 1] - seq_start;
         bcoord = 0;
+        // every CTA of the cluster reads the same slice and returns together, before any barrier
+        if (!varlen_seq_ok(seq_start, L, a.T, a.S)) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && kv_tile == 0) atomicOr(a.status, DEVSTAT_BOUNDS);
+            return;
+        }
     }
     const int k0 = kv_tile * kB;
     if (k0 >= L) return;  // the same for every CTA of the cluster

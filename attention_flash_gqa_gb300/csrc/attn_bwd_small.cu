@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         seq_start = a.cu_seqlens[seq];
         L = a.cu_seqlens[seq + 1] - seq_start;
         bcoord = 0;
+        if (!varlen_seq_ok(seq_start, L, a.T, a.S)) {  // reported; nothing of the slice is touched
+            if (threadIdx.x == 0 && blockIdx.x == 0 && kv_tile == 0) atomicOr(a.status, DEVSTAT_BOUNDS);
+            return;
+        }
     }
     const int k0 = kv_tile * kB;
     if (k0 >= L) return;  // uniform: before any barrier or TMEM use

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         nq = a.cu_q[seq + 1] - seq_start;
         L = a.seq_lens[seq];
         bcoord = 0;
-        if (seq_start < 0 || nq < 0 || seq_start + nq > a.T || nq > L || L > a.max_pages * 16) {
+        if (seq_start < 0 || nq < 0 || nq > a.S || seq_start > a.T - nq || nq > L || L > a.max_pages * 16) {
             // inconsistent request: reported, nothing read or written
             if (threadIdx.x == 0 && split == 0 && h == 0 && q_tile == a.n_qtiles - 1) atomicOr(a.status, DEVSTAT_BOUNDS);
             return;
@@ -119,6 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         L = a.cu_seqlens[seq + 1] - seq_start;
         nq = L;
         bcoord = 0;
+        if (!varlen_seq_ok(seq_start, L, a.T, a.S)) {
+            // a slice outside the packed rows, or longer than the grid covers: reported, and no
+            // row of it is read or written
+            if (threadIdx.x == 0 && split == 0 && h == 0 && q_tile == a.n_qtiles - 1) atomicOr(a.status, DEVSTAT_BOUNDS);
+            return;
+        }
     }
     const int q0 = q_tile * kBQ;
     if (q0 >= nq) return;  // uniform: before any barrier or TMEM use

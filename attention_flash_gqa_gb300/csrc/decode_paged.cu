@@ -704,8 +704,10 @@ int decode_max_grid() { return 256; }
 int decode_row_floats(int D) { return D + 4; }
 
 int decode_heads_per_unit(int Hkv, int D, int G) {
-    const int cap = (D == 128 && G == 8) ? 4 : kUnitBytes / (kPage * D * 2);
+    int cap = (D == 128 && G == 8) ? 4 : D > 0 ? (int)(kUnitBytes / (kPage * D * 2)) : 1;
+    if (cap < 1) cap = 1;  // head sizes no decode kernel takes: callers reject them, but never divide by 0
     int hb = Hkv < cap ? Hkv : cap;
+    if (hb < 1) hb = 1;
     while (hb > 1 && Hkv % hb) --hb;
     return hb;
 }

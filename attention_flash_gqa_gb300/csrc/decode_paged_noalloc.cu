@@ -54,7 +54,8 @@ ATTN_API int attn_decode_paged_noalloc(const attn_bf16* q, const attn_bf16* k_ca
                                        const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse,
                                        int B, int Hq, int Hkv, int D, int page_size, int max_pages_per_seq,
                                        int num_pages, float scale, int window, void* stream) {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (D != 128 && D != 256) return ATTN_ERR_UNSUPPORTED;  // before sizing: no other head size has a size
     const size_t need = attn_workspace_size(ATTN_OP_DECODE_PAGED, B, Hq, Hkv, 0, D, 0, max_pages_per_seq);
     if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;  // beyond the built-in buffer
     if (B == 0) return attn_decode_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B, Hq, Hkv, D, page_size,

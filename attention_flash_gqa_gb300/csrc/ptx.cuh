@@ -22,6 +22,13 @@ enum : unsigned {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legal wait
 
+// A packed sequence's slice [start, start + len) of the rows, read from a caller's cu_seqlens,
+// is usable when it lies inside the T packed rows and is no longer than max_len (the length the
+// launch grid was sized for). Kernels test it before any access derived from the slice.
+__device__ __forceinline__ bool varlen_seq_ok(int start, int len, int T, int max_len) {
+    return start >= 0 && len >= 0 && len <= max_len && start <= T - len;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -99,7 +99,12 @@ ATTN_API int attn_fwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v
  *   cu_seqlens: DEVICE int32 [num_seqs + 1], non-decreasing, cu_seqlens[0] = 0,
  *   cu_seqlens[num_seqs] = total_tokens. Each sequence is its own causal problem.
  *   max_seqlen: an upper bound on every sequence length (sizes the grid without reading
- *   cu_seqlens on the host). Rows of sequences longer than max_seqlen are not computed.
+ *   cu_seqlens on the host).
+ *   The kernels check every sequence's slice on the device before touching it: a slice
+ *   with cu_seqlens[s] < 0, cu_seqlens[s+1] < cu_seqlens[s] (a decreasing prefix sum),
+ *   cu_seqlens[s+1] > total_tokens, or a length above max_seqlen is never read or written
+ *   (its rows of o and lse keep what they held) and ATTN_ERR_DEVICE_BOUNDS is recorded for
+ *   attn_get_device_status(). The other sequences are computed as usual.
  */
 ATTN_API int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_bf16* o, float* lse,
                     const int32_t* cu_seqlens, int num_seqs, int total_tokens, int max_seqlen, int Hq, int Hkv, int D,
@@ -120,8 +125,8 @@ ATTN_API int attn_fwd_varlen(const attn_bf16* q, const attn_bf16* k, const attn_
  *   `window` of them). n_b = 1 is single-token decode; n_b = L_b is a first prefill.
  *   o [total_q, Hq, D] bf16 out; lse [Hq, total_q] fp32 out (natural log).
  *   max_q_len: an upper bound on every n_b (sizes the grid without reading cu_q on the
- *   host); query rows past it are not computed. A request with n_b > L_b or
- *   L_b > max_pages_per_seq * page_size, or a page id outside [0, num_pages), is reported
+ *   host). A request whose cu_q slice leaves [0, total_q) or decreases, with n_b > max_q_len,
+ *   n_b > L_b or L_b > max_pages_per_seq * page_size, or a page id outside [0, num_pages), is reported
  *   as ATTN_ERR_DEVICE_BOUNDS by attn_get_device_status() (the bad request's rows are left
  *   unwritten; a bad page id is replaced by page 0). Cache slots past L_b in a request's
  *   last page are never used, whatever they hold.
@@ -143,7 +148,9 @@ ATTN_API int attn_fwd_paged(const attn_bf16* q, const attn_bf16* k_cache, const 
  *   the contributions of every query head of the KV head's group).
  *   cu_seqlens == NULL: dense [B, S, ...] layout, lse [B, Hq, S].
  *   cu_seqlens != NULL: packed layout with B == 1, S == total tokens, lse [Hq, S], and
- *   num_seqs / max_seqlen as in attn_fwd_varlen.
+ *   num_seqs / max_seqlen as in attn_fwd_varlen. A sequence whose slice fails the device
+ *   check described there is reported as ATTN_ERR_DEVICE_BOUNDS: its dK / dV rows are not
+ *   written and its dQ rows are zero.
  *   workspace: at least attn_workspace_size(ATTN_OP_BWD[_VARLEN], ...) bytes, 256-byte
  *   aligned; holds an fp32 dQ accumulator and per-row Delta = rowsum(dO * o). Contents on
  *   entry do not matter.
@@ -197,10 +204,12 @@ ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, con
  *   not exceed attn_decode_paged_noalloc_max_bytes() (e.g. Hq = 32 allows B up to 240);
  *   larger problems are rejected with ATTN_ERR_WORKSPACE before anything is enqueued.
  *   The first call made while a given device is current looks up the buffer's device
- *   address (cudaGetSymbolAddress) for that device; make that first call before any
- *   stream capture on the device.
- *   All calls on a device share the one buffer, and it keeps the previous call's
- *   contents; each call clears the parts that must start at zero on its own stream.
+ *   address (cudaGetSymbolAddress) for that device and caches it for the life of the
+ *   process; make that first call before any stream capture on the device. The cached
+ *   address does not survive cudaDeviceReset(): after a reset of a device, do not call this
+ *   entry point on it again in the same process.
+ *   All calls on a device share the one buffer, and it keeps the previous call's contents.
+ *   Nothing in it needs to start at zero: every call writes all of it that it reads.
  *   Calls whose execution overlaps on the GPU (different streams without ordering) race
  *   on the buffer and give wrong results: order them.
  */
@@ -236,7 +245,9 @@ ATTN_API int attn_merge_lse(const attn_bf16* o_parts, const float* lse_parts, at
  * attn_workspace_size -- bytes of workspace an operation needs (0 if none).
  *   For ATTN_OP_BWD: B, Hq, S, D; for ATTN_OP_BWD_VARLEN pass B = 1 and S = total tokens.
  *   For ATTN_OP_DECODE_PAGED: B, Hq, Hkv, D. Unused arguments are ignored. Returns 0 for an
- *   unknown op. Pure host arithmetic; needs no GPU.
+ *   unknown op, and for a decode problem no decode kernel takes (D not 128 / 256, Hq not a
+ *   supported multiple of Hkv), whose call is rejected anyway. Pure host arithmetic; needs no
+ *   GPU.
  */
 ATTN_API size_t attn_workspace_size(int op, int B, int Hq, int Hkv, int S, int D, int num_seqs, int max_pages_per_seq);
 

@@ -67,10 +67,14 @@ def dense_case(orc, p, key_rows):
 
 
 def test_dense_d512_causal_full(orc):
-    """B=2, Hq=32, Hkv=4, S=4096, D=512: dK/dV sampled on keys near the end (few queries see them)."""
+    """B=2, Hq=32, Hkv=4, S=4096, D=512: dK/dV on keys near the end (few queries see them) and on
+    the first keys and one mid-sequence key of two (batch, KV head) pairs. Key 0 is seen by all
+    4096 queries of all 8 heads of its group: the longest accumulation in tensor memory (256
+    steps of its key tile) checked at full size."""
     p = synth.dense_d512_causal(seed=0)
     S = p.S
-    keys = [(0, 0, S - 1), (1, 3, S - 2), (0, 2, S - 129), (1, 1, S - 200), (0, 3, S - 128), (1, 0, S - 64)]
+    keys = [(0, 0, S - 1), (1, 3, S - 2), (0, 2, S - 129), (1, 1, S - 200), (0, 3, S - 128), (1, 0, S - 64),
+            (0, 0, 0), (0, 0, 1), (0, 0, 127), (1, 2, 0), (1, 2, S // 2), (1, 2, S // 2 - 1)]
     dense_case(orc, p, keys)
 
 
@@ -102,8 +106,9 @@ def test_varlen_d512_causal_full(orc):
     check("o rows", np.stack([on[cu_np[s] + i, h] for s, h, i in rows]), ro)
     check_lse("lse rows", np.array([ln[h, cu_np[s] + i] for s, h, i in rows]), rl)
     check("dq rows", np.stack([dqn[cu_np[s] + i, h] for s, h, i in rows]), rdq)
+    # late keys of every sequence, and the first key of every sequence (seen by all its queries)
     krows = np.array([(s, int(rng.integers(vp.Hkv)), int(vp.seqlens[s]) - 1 - int(rng.integers(100)))
-                      for s in range(ns)], np.int64)
+                      for s in range(ns)] + [(s, int(rng.integers(vp.Hkv)), 0) for s in range(ns)], np.int64)
     rdk, rdv = orc.dkv_rows(vp.q, vp.k, vp.v, vp.do, krows, vp.scale, cu_seqlens=vp.cu_seqlens)
     dkn, dvn = to_np(dk), to_np(dv)
     check("dk rows", np.stack([dkn[cu_np[s] + j, g] for s, g, j in krows]), rdk)

@@ -153,6 +153,61 @@ def test_varlen_equals_dense_per_sequence():
         assert torch.equal(lse[:, a:a + L], ld[0])
 
 
+# (planted cu_seqlens, max_seqlen, indices of the sequences whose slices stay valid); the true
+# lengths are [200, 100, 300] (cu [0, 200, 300, 600], T = 600)
+_BAD_CU = {
+    "decreasing": ([0, 200, 100, 600], 300, [0]),         # seq 1 ends before it starts; seq 2 then exceeds 300
+    "past_the_end": ([0, 200, 300, 700], 300, [0, 1]),    # seq 2 ends beyond the 600 packed rows
+    "negative_start": ([-5, 200, 300, 600], 300, [1, 2]), # seq 0 starts before row 0
+    "longer_than_max": ([0, 200, 300, 600], 250, [0, 1]), # seq 2 (300 tokens) is longer than max_seqlen
+}
+
+
+@pytest.mark.parametrize("D", [512, 256, 128])
+@pytest.mark.parametrize("case", sorted(_BAD_CU))
+def test_varlen_bad_cu_seqlens_is_reported_not_touched(orc, D, case):
+    """A malformed prefix sum from the caller (the varlen path stands in for a 2-D padding mask)
+    must not turn into out-of-range accesses: each sequence's slice is checked on the device, a
+    bad one is reported as ATTN_ERR_DEVICE_BOUNDS and none of its rows is read or written, and
+    the sequences whose slices are valid are still computed (forward and backward)."""
+    lens = [200, 100, 300]
+    bad_cu, max_seqlen, good = _BAD_CU[case]
+    vp = synth.varlen_from_lengths(lens, 4, 2, D, 0, seed=D + len(case))
+    T = int(vp.cu_seqlens[-1])
+    q, k, v, do = (to_dev(x) for x in (vp.q, vp.k, vp.v, vp.do))
+    cu_ok = torch.from_numpy(vp.cu_seqlens).cuda()
+    cu_bad = torch.tensor(bad_cu, dtype=torch.int32, device="cuda")
+    # reference rows: the valid slices of the planted prefix sum are slices of the true one
+    ro, rl = orc.fwd_varlen(vp.q, vp.k, vp.v, vp.cu_seqlens, vp.scale, 1, 0)
+    rdq, rdk, rdv, _ = orc.bwd_varlen(vp.q, vp.k, vp.v, vp.do, vp.cu_seqlens, vp.scale, 1, 0)
+    good_rows = np.concatenate([np.arange(vp.cu_seqlens[s], vp.cu_seqlens[s + 1]) for s in good])
+    untouched = np.setdiff1d(np.arange(T), good_rows)
+
+    o = torch.zeros_like(q)
+    lse = torch.full((4, T), 7.0, dtype=torch.float32, device="cuda")
+    attn.attn_fwd_varlen(q, k, v, cu_bad, max_seqlen, o, lse, scale=vp.scale)
+    assert attn.attn_get_device_status() == 7  # ATTN_ERR_DEVICE_BOUNDS
+    on, ln = to_np(o), to_np(lse)
+    check("o[valid]", on[good_rows], ro[good_rows])
+    check_lse("lse[valid]", ln[:, good_rows], rl[:, good_rows])
+    assert np.all(on[untouched] == 0) and np.all(ln[:, untouched] == 7.0)
+
+    # backward with the forward of the true prefix sum as input, then the planted one
+    o_ok, lse_ok = attn.attn_fwd_varlen(q, k, v, cu_ok, vp.max_seqlen, scale=vp.scale)
+    dq = torch.full_like(q, 3.0)
+    dk = torch.full_like(k, 3.0)
+    dv = torch.full_like(v, 3.0)
+    attn.attn_bwd(q, k, v, o_ok, lse_ok, do, dq, dk, dv, scale=vp.scale, cu_seqlens=cu_bad, max_seqlen=max_seqlen)
+    assert attn.attn_get_device_status() == 7
+    dqn, dkn, dvn = to_np(dq), to_np(dk), to_np(dv)
+    check("dq[valid]", dqn[good_rows], rdq[good_rows])
+    check("dk[valid]", dkn[good_rows], rdk[good_rows])
+    check("dv[valid]", dvn[good_rows], rdv[good_rows])
+    assert np.all(dqn[untouched] == 0)  # the accumulator of a skipped slice stays zero
+    assert np.all(dkn[untouched] == 3.0) and np.all(dvn[untouched] == 3.0)
+    assert attn.attn_get_device_status() == 0  # cleared by the previous read
+
+
 def run_decode(pp, workspace=None):
     q, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
     bt = torch.from_numpy(pp.block_table).cuda()

@@ -36,22 +36,38 @@ def _device_case(pp):
     return q, kc, vc, bt, sl
 
 
+_CASES = [
+    # (problem, window): the benchmarked head_dim 128 decode, a ragged batch with empty and one-page
+    # requests, and a windowed head_dim 256 batch (KV heads in blocks, contexts past the window)
+    (lambda: synth.decode_paged_d128(seed=3), 0),
+    (lambda: synth.paged_from_lengths([5, 1024, 0, 17, 300, 640], 32, 8, 128, page_size=16, num_pages=512,
+                                      seed=4, max_pages=64), 0),
+    (lambda: synth.paged_from_lengths([300, 17, 1024, 2000, 1500], 32, 16, 256, page_size=16, num_pages=512,
+                                      seed=5, max_pages=128), 1024),
+]
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_path_on_two_calls(lib):
+    """Both entry points run the same kernels on the same inputs, so their results must be the
+    same bits; each case makes two calls in a row on the shared buffer (the second finds the
+    first call's leftovers, and the cases change the batch and head size between calls)."""
     torch.cuda.set_device(0)
-    cases = [synth.decode_paged_d128(seed=3),
-             synth.paged_from_lengths([5, 1024, 0, 17, 300, 640], 32, 8, 128, page_size=16, num_pages=512,
-                                      seed=4, max_pages=64)]
-    for pp in cases:  # two calls in a row on the shared buffer, different batches
+    for make, window in _CASES:
+        pp = make()
         q, kc, vc, bt, sl = _device_case(pp)
-        ref_o, ref_lse = attn.attn_decode_paged(q, kc, vc, bt, sl, scale=pp.scale)
-        o = torch.empty_like(q)
-        lse = torch.empty((pp.B, pp.Hq), dtype=torch.float32, device="cuda")
-        attn.attn_decode_paged_noalloc(q, kc, vc, bt, sl, o, lse, scale=pp.scale)
-        torch.cuda.synchronize()
-        assert attn.attn_get_device_status() == 0
-        check("o", to_np(o), to_np(ref_o))
-        check_lse("lse", to_np(lse), to_np(ref_lse))
+        ref_o, ref_lse = attn.attn_decode_paged(q, kc, vc, bt, sl, scale=pp.scale, window=window)
+        for _ in range(2):
+            o = torch.full_like(q, 5.0)
+            lse = torch.full((pp.B, pp.Hq), 5.0, dtype=torch.float32, device="cuda")
+            attn.attn_decode_paged_noalloc(q, kc, vc, bt, sl, o, lse, scale=pp.scale, window=window)
+            torch.cuda.synchronize()
+            assert attn.attn_get_device_status() == 0
+            assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16))
+            assert torch.equal(lse, ref_lse)
+            # and so within the tolerance of every parity test
+            check("o", to_np(o), to_np(ref_o))
+            check_lse("lse", to_np(lse), to_np(ref_lse))
 
 
 def test_noalloc_rejects_problems_beyond_the_buffer(lib):
@@ -68,3 +84,15 @@ def test_noalloc_rejects_problems_beyond_the_buffer(lib):
     assert call(481, 32) == 4  # ATTN_ERR_WORKSPACE
     assert call(4096, 64) == 4
     assert call(-1, 32) == 1  # ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_rejects_unsupported_head_sizes_without_sizing_them(lib):
+    """Needs no GPU: a head size no decode kernel takes is rejected as unsupported (and the
+    workspace size of such a problem is 0) instead of reaching the size arithmetic."""
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 7
+    for D in (2048, 64, 100):
+        assert attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, 8, 32, 8, 0, D) == 0
+        assert lib.attn_decode_paged_noalloc(*args, 8, 32, 8, D, 16, 64, 4096, 0.088, 0, None) == 2
+    assert attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, 8, 32, 6, 0, 128) == 0  # 32 % 6 != 0
+    assert lib.attn_decode_paged_noalloc(*args, 8, 32, 6, 128, 16, 64, 4096, 0.088, 0, None) == 1
