@@ -268,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idRole = idesc_bf16_f32(128, C::NQ, false, false);  // K tile x query rows
             constexpr uint32_t idG = idesc_bf16_f32(128, 64, false, true);  // P^T / dS^T K-major, B N-major
+            constexpr uint32_t idG128 = idesc_bf16_f32(128, 128, false, true);  // the same over both halves
             constexpr uint32_t idQ = idesc_bf16_f32(128, 128, true, true);  // dS (MN-major) x K_c (N-major)
             const uint16_t mask_s = (uint16_t)((1u << C::NHALF) - 1u);       // writers of P^T
             const uint16_t mask_d = (uint16_t)(mask_s << C::NHALF);          // writers of dS^T
@@ -312,12 +313,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t b0, b1;
                 int s0, s1;
                 if (!acquire(b0, s0) || !acquire(b1, s1)) return false;
+                if (s1 == s0 + 1) {
+                    // the halves sit in adjacent slots (unless the ring wrapped between them): one
+                    // N = 128 product per K step reads the A tile once instead of twice
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                    const uint32_t accf = (acc_in || kk > 0) ? 1u : 0u;
-                    umma_bf16_ss(dacc, ad, sdesc_sw128(b0 + kk * 2048, kSub, 1024), idG, accf);
-                    umma_bf16_ss(dacc + 64, ad, sdesc_sw128(b1 + kk * 2048, kSub, 1024), idG, accf);
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_ss(dacc, sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
+                                     sdesc_sw128(b0 + kk * 2048, kSlot, 1024), idG128, (acc_in || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                        const uint32_t accf = (acc_in || kk > 0) ? 1u : 0u;
+                        umma_bf16_ss(dacc, ad, sdesc_sw128(b0 + kk * 2048, kSub, 1024), idG, accf);
+                        umma_bf16_ss(dacc + 64, ad, sdesc_sw128(b1 + kk * 2048, kSub, 1024), idG, accf);
+                    }
                 }
                 umma_commit(smem_u32(&empty[s0]));
                 umma_commit(smem_u32(&empty[s1]));
