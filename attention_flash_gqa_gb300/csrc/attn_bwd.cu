@@ -12,25 +12,28 @@
 // Kernels:
 //  1. bwd_prep: Delta per query row (fp32) and zeroing of the fp32 dQ accumulator.
 //  2. bwd_main: one thread-block cluster per (KV tile of 128 keys, KV head); its
-//     NC = D / 128 CTAs each own one 128-wide column slice c of D and accumulate dV_c
+//     NC = D / 128 = 4 CTAs each own one 128-wide column slice c of D and accumulate dV_c
 //     and dK_c for the tile in tensor memory while looping over every query head of the
 //     GQA group and every query tile that can see the keys (causal / window tile
-//     skipping), so dK and dV are summed over the group without atomics.
-//     The two full-width contractions of a step are split across the cluster instead of
-//     being recomputed per slice: the first NC/2 CTAs ("S role") compute
-//     S^T = K Q^T, the other NC/2 ("dP role") dP^T = V dO^T, each for its own share of
-//     the step's 128 query columns (keys on TMEM lanes). An S-role CTA turns its share
-//     into P^T (bf16) and copies it into every CTA of the cluster; its dP-role partner
-//     (same query share) reads that P^T, forms dS^T = P^T (dP^T - Delta) and copies it
-//     to every CTA. Each CTA then runs its slice of the three gradient products from the
-//     assembled P^T / dS^T tiles in shared memory:
+//     skipping), so dK and dV are summed over the group without atomics. A step is one
+//     (head, query tile); steps are taken two at a time ("pair-steps").
+//     The two full-width contractions are split across the cluster instead of being
+//     recomputed per slice: CTAs 0, 1 ("S role") compute S = Q K^T, CTAs 2, 3 ("dP role")
+//     dP = dO V^T, each for its own 64-query share of both steps of a pair-step at once:
+//     one M = 128 product (rows = the two steps' shares, queries on TMEM lanes) over the
+//     128 keys, so the full-width key (or value) tile streams once per two steps. An
+//     S-role CTA turns its rows into P (bf16) and copies them into every CTA of the
+//     cluster; its dP-role partner (same share) reads those rows, forms
+//     dS = P (dP - Delta) and copies it likewise. Each CTA then runs its slice of the
+//     three gradient products from the assembled per-step P / dS tiles [128 queries x 128
+//     keys] in shared memory (P^T and dS^T read MN-major):
 //       dV_c += P^T dO_c,   dK_c += dS^T Q_c,   dQ_c = dS K_c
 //     dQ_c leaves tensor memory after every step and is added into an fp32 accumulator
 //     with TMA bulk reduce-adds. Consumption of the exchanged tiles is signalled back to
-//     their writers with multicast tcgen05.commit arrivals. P^T is double-buffered, so a
-//     share for step t can be written while step t-1's dV products are still pending.
+//     their writers with multicast tcgen05.commit arrivals. P is double-buffered (one
+//     buffer per step of a pair-step); dS is single-buffered.
 //     Tensor memory (512 columns): [0,128) dV_c, [128,256) dK_c, [256,384) dQ_c,
-//     [384,512) the role result (two 64-column buffers when NC = 4, one of 128 when 2).
+//     [384,512) the role result of a pair-step.
 //  3. bwd_finalize: dQ accumulator -> bf16.
 #include <cuda_runtime.h>
 
@@ -51,30 +54,25 @@ constexpr uint32_t kSmemMax = 232448;
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Configuration of the cluster kernel (D = 512: four CTAs, two per role).
 template <int D>
 struct Cfg {
     static constexpr int NC = D / 128;        // cluster size = slices of D
     static constexpr int NHALF = NC / 2;      // CTAs per role
-    static constexpr int NQ = 128 / NHALF;    // query columns of one role share (128 or 64)
-    static constexpr int RB = NQ == 64 ? 2 : 1;  // role result buffers in tensor memory
-    static constexpr int YPS = 128 / NQ;      // role B-operand sub-tiles per ring slot
+    static constexpr int NQ = 128 / NHALF;    // queries of one role share per step
     static constexpr int NSUB = D / 64;       // 64-wide sub-tiles across D
-    static constexpr uint32_t kPieceBytes = 128u * NQ * 2u;  // one role share of P^T or dS^T
+    static constexpr uint32_t kPieceBytes = 128u * NQ * 2u;  // one role share of a step's P or dS
     static constexpr uint32_t kRemoteBytes = (NHALF - 1) * kPieceBytes;  // from the other writers
-    // Shared memory. At D = 512 the P^T tile is double-buffered (a share for step t can be
-    // written while step t-1's dV products are pending), paid for with one ring slot and one
-    // dQ staging buffer; at D = 256 the deeper ring pays more.
-    static constexpr int PBUF = D == 512 ? 2 : 1;    // P^T buffers
-    static constexpr int STAGEBUF = D == 512 ? 1 : 2;  // dQ staging buffers (128 rows x 32 fp32 each)
-    static constexpr int kStages = D == 512 ? 5 : 6;  // ring slots
-    static constexpr uint32_t kOffP = 0;                              // P^T [128 keys x 128 queries] bf16
-    static constexpr uint32_t kOffDS = kOffP + PBUF * 2 * kSub;       // dS^T, same layout
+    static constexpr int kStages = 5;                                 // ring slots
+    static constexpr uint32_t kOffP = 0;                              // P, two steps: [128 queries x 128 keys] bf16
+    static constexpr uint32_t kOffDS = kOffP + 2 * 2 * kSub;          // dS, same layout
     static constexpr uint32_t kOffKc = kOffDS + 2 * kSub;             // K_c [128 keys x 128 dims], resident
-    static constexpr uint32_t kOffStage = kOffKc + 2 * kSub;          // dQ staging
-    static constexpr uint32_t kOffRing = kOffStage + STAGEBUF * kSub;
+    static constexpr uint32_t kOffStage = kOffKc + 2 * kSub;          // dQ staging (128 rows x 32 fp32)
+    static constexpr uint32_t kOffRing = kOffStage + kSub;
     static constexpr uint32_t kOffBar = kOffRing + kStages * kSlot;
     static constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // + slack for the 1024-byte alignment
     static_assert(kSmem <= kSmemMax, "shared memory budget");
+    static_assert(NQ == 64, "the role split is written for D = 512");
 };
 
 struct BwdArgs {
@@ -118,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q_last = a.window > 0 ? min(L, k0 + kB - 1 + a.window) : L;  // exclusive bound on queries
     const int i_begin = k0 / kB, i_end = (q_last + kB - 1) / kB;
     const int n_qt = i_end - i_begin;
-    const int n = G * n_qt;  // steps: (head, query tile)
+    const int n = G * n_qt;    // steps: (head, query tile)
+    const int np = (n + 1) / 2;  // pair-steps: steps 2T and 2T + 1 (the latter absent when n is odd)
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,12 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::kStages;
-    uint64_t* r_full = bars + 2 * C::kStages;  // role result in TMEM complete [RB]
-    uint64_t* r_free = r_full + 2;          // role result read out by the softmax warps [RB]
-    uint64_t* p_full = r_free + 2;          // all of P^T(t) present in buffer t & 1 [2]
-    uint64_t* ds_full = p_full + 2;         // all of dS^T(t) present
-    uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's P^T share in buffer b is done [2]
-    uint64_t* ds_free = p_free + 2;         // (dP role) every reader of this CTA's dS^T share is done
+    uint64_t* r_full = bars + 2 * C::kStages;  // role result of a pair-step in TMEM complete
+    uint64_t* r_free = r_full + 1;          // role result read out by the elementwise warps (128)
+    uint64_t* p_full = r_free + 1;          // all of P(t) present in buffer t & 1 [2]
+    uint64_t* ds_full = p_full + 2;         // all of dS(t) present
+    uint64_t* p_free = ds_full + 1;         // (S role) every reader of this CTA's share of P in buffer b is done [2]
+    uint64_t* ds_free = p_free + 2;         // (dP role) every reader of this CTA's share of dS is done
     uint64_t* dq_full = ds_free + 1;
     uint64_t* dq_free = dq_full + 1;
     uint64_t* kc_full = dq_free + 1;
@@ -147,16 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&r_full[b]), 1);
-            mbar_init(smem_u32(&r_free[b]), 128);
-        }
+        mbar_init(smem_u32(r_full), 1);
+        mbar_init(smem_u32(r_free), 128);
         // exchange barriers: one arming arrive (with the bytes expected from other CTAs)
-        // plus, for the share this CTA writes itself, its 128 writer threads
-        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_full[b]), 1 + (s_role ? 128 : 0));
-        mbar_init(smem_u32(ds_full), 1 + (s_role ? 0 : 128));
+        // plus, for the share this CTA writes itself, the 64 threads that hold a step's rows
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_full[b]), 1 + (s_role ? 64 : 0));
+        mbar_init(smem_u32(ds_full), 1 + (s_role ? 0 : 64));
         // one multicast commit from every CTA's MMA (a dP-role CTA commits only after its
-        // elementwise warps have also read P^T)
+        // elementwise warps have also read P)
         for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_free[b]), C::NC);
         mbar_init(smem_u32(ds_free), C::NC);
         mbar_init(smem_u32(dq_full), 1);
@@ -182,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int krow = seq_start + k0;
     const uint32_t p_rem = s_role ? C::kRemoteBytes : C::NHALF * C::kPieceBytes;
     const uint32_t ds_rem = s_role ? C::NHALF * C::kPieceBytes : C::kRemoteBytes;
+    auto head_of = [&](int t) { return g * G + t / n_qt; };
+    auto qtile_of = [&](int t) { return (i_begin + t % n_qt) * kB; };  // first query of step t's tile
 
     if (warp == 0) {
         // ---------------------------------- producer -------------------------------------
@@ -206,25 +205,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
-            const CUtensorMap* X = s_role ? &tk : &tv;    // role A operand: the key tile, full width
-            const CUtensorMap* Y = s_role ? &tqh : &tdoh; // role B operand: this share's query rows
-            auto load_role = [&](int t) -> bool {
-                const int h = g * G + t / n_qt;
-                const int yrow = seq_start + (i_begin + t % n_qt) * kB + share * C::NQ;
-                for (int u = 0; u < C::NSUB; ++u) {
+            const CUtensorMap* X = s_role ? &tk : &tv;    // role B operand: the key tile, full width
+            const CUtensorMap* Y = s_role ? &tqh : &tdoh; // role A operand: this share's query rows
+            // per 64-column sub-tile u: X_u (128 keys), then Y_u = the share's 64 rows of both
+            // steps stacked (an absent second step repeats the first; its result is unused)
+            auto load_role = [&](int T, int u_begin, int u_end) -> bool {
+                const int t0 = 2 * T, t1 = min(2 * T + 1, n - 1);
+                const int h0 = head_of(t0), h1 = head_of(t1);
+                const int y0 = seq_start + qtile_of(t0) + share * C::NQ, y1 = seq_start + qtile_of(t1) + share * C::NQ;
+                for (int u = u_begin; u < u_end; ++u) {
                     uint32_t dst, fb;
                     if (!next(dst, fb)) return false;
                     tma_load_4d(dst, X, fb, 64 * u, g, krow, bcoord);
-                    if (u % C::YPS == 0) {
-                        if (!next(dst, fb)) return false;
-                        for (int v = 0; v < C::YPS; ++v)
-                            tma_load_4d(dst + v * (C::NQ * 128), Y, fb, 64 * (u + v), h, yrow, bcoord);
-                    }
+                    if (!next(dst, fb)) return false;
+                    tma_load_4d(dst, Y, fb, 64 * u, h0, y0, bcoord);
+                    tma_load_4d(dst + C::NQ * 128, Y, fb, 64 * u, h1, y1, bcoord);
                 }
                 return true;
             };
             auto load_grad = [&](int t) -> bool {  // B operands of dV_c and dK_c
-                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
+                const int h = head_of(t), qrow = seq_start + qtile_of(t);
                 for (int e = 0; e < 2; ++e) {
                     uint32_t dst, fb;
                     if (!next(dst, fb)) return false;
@@ -238,23 +238,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             // Q and dO tiles are new every step and mostly miss L2: warm it with this CTA's
-            // future operands two steps ahead.
-            constexpr int kAhead = 2;
+            // future operands ahead of their loads.
             auto prefetch = [&](int t) {
                 if (t >= n) return;
-                const int h = g * G + t / n_qt, qrow = seq_start + (i_begin + t % n_qt) * kB;
+                const int h = head_of(t), qrow = seq_start + qtile_of(t);
                 const CUtensorMap* Ym = s_role ? &tq : &tdo;
                 for (int c = 0; c < D; c += 64) tma_prefetch_4d(Ym, c, h, qrow, bcoord);
                 tma_prefetch_4d(s_role ? &tdo : &tq, c0, h, qrow, bcoord);
                 tma_prefetch_4d(s_role ? &tdo : &tq, c0 + 64, h, qrow, bcoord);
             };
-            for (int t = 1; t <= kAhead; ++t) prefetch(t);
-            // consumption order of the UMMA issuer: role(0) | role(t+1) grad(t) | ...
-            bool ok = load_role(0);
-            for (int t = 0; ok && t < n; ++t) {
-                prefetch(t + 1 + kAhead);
-                if (t + 1 < n) ok = load_role(t + 1);
-                ok = ok && load_grad(t);
+            for (int t = 2; t < 6; ++t) prefetch(t);
+            // consumption order of the UMMA issuer: role(0) | first half of role(T+1), grad(2T),
+            // second half of role(T+1), grad(2T+1) | ...
+            constexpr int kHalfU = C::NSUB / 2;
+            bool ok = load_role(0, 0, C::NSUB);
+            for (int T = 0; ok && T < np; ++T) {
+                prefetch(2 * T + 6);
+                prefetch(2 * T + 7);
+                const bool more = T + 1 < np;
+                if (more) ok = load_role(T + 1, 0, kHalfU);
+                ok = ok && load_grad(2 * T);
+                if (ok && more) ok = load_role(T + 1, kHalfU, C::NSUB);
+                if (2 * T + 1 < n) ok = ok && load_grad(2 * T + 1);
             }
             const int issued = round * C::kStages + slot;
             for (int s = 0; s < C::kStages && s < issued; ++s) {
@@ -266,12 +271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // --------------------------------- UMMA issuer -----------------------------------
         if (lane == 0) {
-            constexpr uint32_t idRole = idesc_bf16_f32(128, C::NQ, false, false);  // K tile x query rows
-            constexpr uint32_t idG = idesc_bf16_f32(128, 64, false, true);  // P^T / dS^T K-major, B N-major
-            constexpr uint32_t idG128 = idesc_bf16_f32(128, 128, false, true);  // the same over both halves
-            constexpr uint32_t idQ = idesc_bf16_f32(128, 128, true, true);  // dS (MN-major) x K_c (N-major)
-            const uint16_t mask_s = (uint16_t)((1u << C::NHALF) - 1u);       // writers of P^T
-            const uint16_t mask_d = (uint16_t)(mask_s << C::NHALF);          // writers of dS^T
+            constexpr uint32_t idRole = idesc_bf16_f32(128, 128, false, false);  // query rows x key tile
+            constexpr uint32_t idG128 = idesc_bf16_f32(128, 128, true, true);    // P^T / dS^T x slice, MN-major
+            constexpr uint32_t idG64 = idesc_bf16_f32(128, 64, true, true);      // the same, one 64-column half
+            constexpr uint32_t idQ = idesc_bf16_f32(128, 128, false, true);      // dS (K-major) x K_c (N-major)
+            const uint16_t mask_s = (uint16_t)((1u << C::NHALF) - 1u);       // writers of P
+            const uint16_t mask_d = (uint16_t)(mask_s << C::NHALF);          // writers of dS
             int slot = 0, round = 0;
             auto acquire = [&](uint32_t& addr, int& s) -> bool {
                 if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x22)) return false;
@@ -281,52 +286,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
-            auto role = [&](int t) -> bool {
-                const int b = t % C::RB;
-                if (t >= C::RB) {
-                    if (!mbar_wait(smem_u32(&r_free[b]), ((t / C::RB) - 1) & 1, abort_flag, a.status, 0x29))
-                        return false;
+            // S (or dP) rows of pair-step T: A = the stacked query rows (K-major), B = the key tile
+            auto role = [&](int T, int u_begin, int u_end) -> bool {
+                if (T > 0 && u_begin == 0) {
+                    if (!mbar_wait(smem_u32(r_free), (T - 1) & 1, abort_flag, a.status, 0x29)) return false;
                     tc_fence_after();
                 }
-                const uint32_t d = tR + b * C::NQ;
-                uint32_t ya = 0;
-                int ys = 0;
-                for (int u = 0; u < C::NSUB; ++u) {
-                    uint32_t xa;
-                    int xs;
-                    if (!acquire(xa, xs)) return false;
-                    if (u % C::YPS == 0 && !acquire(ya, ys)) return false;
-                    const uint32_t yb = ya + (u % C::YPS) * (C::NQ * 128);
+                for (int u = u_begin; u < u_end; ++u) {
+                    uint32_t xa, ya;
+                    int xs, ys;
+                    if (!acquire(xa, xs) || !acquire(ya, ys)) return false;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(d, sdesc_sw128(xa + kk * 32, 16, 1024), sdesc_sw128(yb + kk * 32, 16, 1024),
+                        umma_bf16_ss(tR, sdesc_sw128(ya + kk * 32, 16, 1024), sdesc_sw128(xa + kk * 32, 16, 1024),
                                      idRole, (u | kk) ? 1u : 0u);
                     umma_commit(smem_u32(&empty[xs]));
-                    if (u % C::YPS == C::YPS - 1) umma_commit(smem_u32(&empty[ys]));
+                    umma_commit(smem_u32(&empty[ys]));
                 }
-                umma_commit(smem_u32(&r_full[b]));
+                if (u_end == C::NSUB) umma_commit(smem_u32(r_full));
                 return true;
             };
-            // acc += A x B over 128 query rows, B = one 128-column slice held as two 64-column
-            // ring sub-tiles (N-major): two N = 64 products per K step of 16 rows
+            // acc += A^T x B over a step's 128 queries: A^T read MN-major from a [128 queries x 128 keys]
+            // tile (two 64-key sub-tiles), B = one 128-column slice held as two 64-column ring
+            // sub-tiles (N-major); one N = 128 product per K step when they sit in adjacent slots
             auto grad_pair = [&](uint32_t dacc, uint32_t sa, bool acc_in) -> bool {
                 uint32_t b0, b1;
                 int s0, s1;
                 if (!acquire(b0, s0) || !acquire(b1, s1)) return false;
                 if (s1 == s0 + 1) {
-                    // the halves sit in adjacent slots (unless the ring wrapped between them): one
-                    // N = 128 product per K step reads the A tile once instead of twice
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16_ss(dacc, sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
-                                     sdesc_sw128(b0 + kk * 2048, kSlot, 1024), idG128, (acc_in || kk > 0) ? 1u : 0u);
+                        umma_bf16_ss(dacc, sdesc_sw128(sa + kk * 2048, kSub, 1024), sdesc_sw128(b0 + kk * 2048, kSlot, 1024),
+                                     idG128, (acc_in || kk > 0) ? 1u : 0u);
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sa + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                        const uint64_t ad = sdesc_sw128(sa + kk * 2048, kSub, 1024);
                         const uint32_t accf = (acc_in || kk > 0) ? 1u : 0u;
-                        umma_bf16_ss(dacc, ad, sdesc_sw128(b0 + kk * 2048, kSub, 1024), idG, accf);
-                        umma_bf16_ss(dacc + 64, ad, sdesc_sw128(b1 + kk * 2048, kSub, 1024), idG, accf);
+                        umma_bf16_ss(dacc, ad, sdesc_sw128(b0 + kk * 2048, kSub, 1024), idG64, accf);
+                        umma_bf16_ss(dacc + 64, ad, sdesc_sw128(b1 + kk * 2048, kSub, 1024), idG64, accf);
                     }
                 }
                 umma_commit(smem_u32(&empty[s0]));
@@ -334,14 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto grads = [&](int t) -> bool {
-                const int pb = t % C::PBUF;
-                if (!mbar_wait(smem_u32(&p_full[pb]), (t / C::PBUF) & 1, abort_flag, a.status, 0x23)) return false;
+                const int pb = t & 1;
+                if (!mbar_wait(smem_u32(&p_full[pb]), (t >> 1) & 1, abort_flag, a.status, 0x23)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(&p_full[pb]), p_rem);  // arm the buffer's next use
                 if (!grad_pair(tDV, sP + pb * 2 * kSub, t > 0)) return false;  // dV_c += P^T dO_c
-                // an S-role CTA is done with P^T(t) here; a dP-role CTA also reads it in its
-                // elementwise warps (before writing dS^T(t)), so it releases the buffer after
-                // the dS^T products below
+                // an S-role CTA is done with P(t) here; a dP-role CTA also reads it in its
+                // elementwise warps (before writing dS(t)), so it releases the buffer after the
+                // dS products below
                 if (s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 if (!mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x24)) return false;
                 tc_fence_after();
@@ -352,28 +350,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // dQ_c = dS K_c: queries on lanes, K = keys
-                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024), sdesc_sw128(sKc + kk * 2048, kSub, 1024),
-                                 idQ, kk > 0 ? 1u : 0u);
+                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
+                                 sdesc_sw128(sKc + kk * 2048, kSub, 1024), idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 umma_commit_multicast(smem_u32(ds_free), mask_d);
                 if (!s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 return true;
             };
-            bool ok = role(0);
-            for (int t = 0; ok && t < n; ++t) {
-                if (t + 1 < n) ok = role(t + 1);
-                ok = ok && grads(t);
+            constexpr int kHalfU = C::NSUB / 2;
+            bool ok = role(0, 0, C::NSUB);
+            for (int T = 0; ok && T < np; ++T) {
+                const bool more = T + 1 < np;
+                if (more) ok = role(T + 1, 0, kHalfU);
+                ok = ok && grads(2 * T);
+                if (ok && more) ok = role(T + 1, kHalfU, C::NSUB);
+                if (2 * T + 1 < n) ok = ok && grads(2 * T + 1);
             }
             umma_commit(smem_u32(mma_idle));
             mbar_drain(smem_u32(mma_idle), 0, a.status, 0x28);
         }
     } else {
         // ------------------------- elementwise / dQ readout warps ----------------------------
+        // Thread j = TMEM lane j of the role result: rows 0..63 belong to step 2T, rows 64..127 to
+        // step 2T + 1; within a step, row r is query share * 64 + r of the step's tile. For the
+        // dQ readout thread j is query row j of the step's tile; for dV / dK, key row j.
         const int quad = warp & 3;
-        const int j = quad * 32 + lane;  // TMEM lane: key row (role, dV, dK) or query row (dQ)
+        const int j = quad * 32 + lane;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int kabs = k0 + j;
-        const bool key_ok = kabs < L;
+        const int half = quad >> 1;              // which step of the pair this thread's row belongs to
+        const int trow = share * C::NQ + (j & 63);  // its row within that step's [128 x 128] tile
+        const int kabs = k0 + j;                 // key row (epilogue)
         bool ok = true;
 
         // dQ_c(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory
@@ -381,16 +387,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto drain_dq = [&](int t) -> bool {
             bool w = __all_sync(0xffffffffu, mbar_wait(smem_u32(dq_full), t & 1, abort_flag, a.status, 0x26));
             tc_fence_after();
-            const int h = g * G + t / n_qt;
-            const int q0 = (i_begin + t % n_qt) * kB;
+            const int h = head_of(t);
+            const int q0 = qtile_of(t);
             const float f = (q0 + j < L) ? a.scale : 0.f;  // rows past the sequence end add zeros
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                const uint32_t buf = sStage + (c4 % C::STAGEBUF) * kSub;
-                if (tid == 64) {  // the reduce that last read `buf` is done
-                    if (C::STAGEBUF == 2) bulk_wait_group_read1();
-                    else bulk_wait_group_read0();
-                }
+                if (tid == 64) bulk_wait_group_read0();  // the reduce that last read the buffer is done
                 named_bar_sync(2, 128);
                 if (w) {
                     uint32_t rq[32];
@@ -398,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int ch = 0; ch < 8; ++ch)
-                        st_shared_v4(buf + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4),
+                        st_shared_v4(sStage + j * 128 + (((uint32_t)ch ^ (uint32_t)(j & 7)) << 4),
                                      __float_as_uint(__uint_as_float(rq[4 * ch]) * f),
                                      __float_as_uint(__uint_as_float(rq[4 * ch + 1]) * f),
                                      __float_as_uint(__uint_as_float(rq[4 * ch + 2]) * f),
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 w = named_bar_and(2, 128, w);
                 if (w && tid == 64) {
-                    tma_reduce_add_4d(&tdq, buf, c0 + 32 * c4, h, seq_start + q0, bcoord);
+                    tma_reduce_add_4d(&tdq, sStage, c0 + 32 * c4, h, seq_start + q0, bcoord);
                     bulk_commit_group();
                 }
             }
@@ -416,128 +418,136 @@ __global__ void __launch_bounds__(kThreads, 1)
             return w;
         };
 
-        for (int t = 0; t < n; ++t) {
-            const int h = g * G + t / n_qt;
-            const int q0 = (i_begin + t % n_qt) * kB;
-            const int qb = q0 + share * C::NQ;  // first query of this CTA's share
-            // the share's lse (log2 units; +inf past the end -> P = 0) or Delta: lane l of every
-            // warp holds queries qb + 32 i + l; columns are broadcast with shuffles
-            float vreg[C::NQ / 32];
-            {
-                const float* src = s_role ? a.lse : a.delta;
-                const size_t lbase = a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S;
+        // this thread's row of the share -> the step's tile, then the warp's 32 rows to every peer
+        auto send = [&](const uint32_t (&pk)[64], uint32_t dst, uint32_t fbar) {
 #pragma unroll
-                for (int i = 0; i < C::NQ / 32; ++i) {
-                    const int qa = qb + 32 * i + lane;
-                    vreg[i] = qa < L ? (s_role ? src[lbase + qa] * kLog2e : src[lbase + qa]) : (s_role ? INFINITY : 0.f);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    st_shared_v4(dst + hh * kSub + sw128_offset(trow, ch * 8), pk[hh * 32 + ch * 4], pk[hh * 32 + ch * 4 + 1],
+                                 pk[hh * 32 + ch * 4 + 2], pk[hh * 32 + ch * 4 + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                const uint32_t row0 = (uint32_t)(share * C::NQ + (quad & 1) * 32) * 128;  // the warp's 32 rows
+                for (uint32_t peer = 0; peer < (uint32_t)C::NC; ++peer) {
+                    if (peer == rank) continue;
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t rows = dst + hh * kSub + row0;
+                        bulk_copy_to_peer(mapa_shared(rows, peer), rows, 4096, mapa_shared(fbar, peer));
+                    }
                 }
             }
-            // role result of this step -> registers, then hand its columns back to the MMA
-            const int b = t % C::RB;
-            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&r_full[b]), (t / C::RB) & 1, abort_flag, a.status, 0x2a));
-            uint32_t rr[C::NQ];
+            mbar_arrive(fbar);
+        };
+
+        // Per pair-step: read the role result and hand it back (the next pair-step's product may
+        // start), send P (both steps) or dS of the first step, put out dQ of the previous step,
+        // send dS of the second step (its buffer is free once the first step's dK / dQ have read
+        // it, and that dQ needs the previous step's dQ out of tensor memory), put out dQ of the
+        // first step.
+        for (int T = 0; T < np; ++T) {
+            const int t = 2 * T + half;   // this thread's step
+            const bool real = t < n;      // false only for the absent second step of the last pair
+            const int q0 = real ? qtile_of(t) : 0;
+            const int qa = q0 + trow;     // this thread's query
+            float v = 0.f;                // lse in log2 units (+inf past the end: P = 0), or Delta
+            if (real) {
+                const int h = head_of(t);
+                const size_t li = (a.cu_seqlens ? (size_t)h * a.T + seq_start : ((size_t)seq * a.Hq + h) * a.S) + qa;
+                v = qa < L ? (s_role ? a.lse[li] * kLog2e : a.delta[li]) : (s_role ? INFINITY : 0.f);
+            }
+            ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(r_full), T & 1, abort_flag, a.status, 0x2a));
+            uint32_t pk[64];  // this row of P or dS over the 128 keys, bf16 pairs
             if (ok) {
                 tc_fence_after();
+                if (s_role) {
+                    // P(query qa, key k0 + c) = exp2(S * scale * log2 e - lse2); on edge tiles only the
+                    // keys c_lo .. c_hi are allowed
+                    // (c_hi < c_lo when no key of the tile is allowed: every key is masked)
+                    const int c_hi = min(kB - 1, min(qa, L - 1) - k0);
+                    const int c_lo = a.window > 0 ? max(0, qa - a.window + 1 - k0) : 0;
+                    const bool edge = c_lo > 0 || c_hi < kB - 1;
 #pragma unroll
-                for (int c = 0; c < C::NQ / 32; ++c) {
-                    uint32_t tmp[32];
-                    tmem_ld32(tR + b * C::NQ + c * 32 + lane_base, tmp);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) rr[c * 32 + e] = tmp[e];
-                }
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(smem_u32(&r_free[b]));
-            }
-            uint32_t pk[C::NQ / 2];
-            if (s_role) {
-                // P^T(key j, query qb + c) = exp2(S^T * scale * log2 e - lse2)
-                const bool edge = !(k0 + kB - 1 <= q0 && (a.window <= 0 || q0 + kB - 1 - k0 < a.window) &&
-                                    q0 + kB <= L && k0 + kB <= L);
-                // on edge tiles key j sees the queries qa with 0 <= qa - kabs < span
-                int qhi = key_ok ? L : kabs;
-                if (a.window > 0) qhi = min(qhi, kabs + a.window);
-                const unsigned span = qhi > kabs ? (unsigned)(qhi - kabs) : 0u;
-                auto p_row = [&](auto masked) {
-#pragma unroll
-                    for (int c = 0; c < C::NQ; c += 2) {
-                        float p[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const float lv = __shfl_sync(0xffffffffu, vreg[(c + u) >> 5], (c + u) & 31);
-                            p[u] = fast_exp2(fmaf(__uint_as_float(rr[c + u]), a.scale_log2, -lv));
-                            if (decltype(masked)::value && (unsigned)(qb + c + u - kabs) >= span) p[u] = 0.f;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t rr[64];
+                        tmem_ld32(tR + hh * 64 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
+                        tmem_ld32(tR + hh * 64 + 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
+                        tmem_ld_wait();
+                        if (hh == 1) {
+                            tc_fence_before();
+                            mbar_arrive(smem_u32(r_free));
                         }
-                        pk[c / 2] = pack_bf16x2(p[0], p[1]);
-                    }
-                };
-                if (edge) p_row(std::true_type{});
-                else p_row(std::false_type{});
-                // buffer t % PBUF was last read at step t - PBUF
-                if (t >= C::PBUF) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_free[t % C::PBUF]), ((t / C::PBUF) - 1) & 1, abort_flag, a.status, 0x2b));
-            } else {
-                // dS^T = P^T (dP^T - Delta), P^T from the S-role partner
-                ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[t % C::PBUF]), (t / C::PBUF) & 1, abort_flag, a.status, 0x2c));
-                if (ok) {
+                        auto p_half = [&](auto masked) {
 #pragma unroll
-                    for (int st = 0; st < C::NQ / 64; ++st) {
-                        const uint32_t tile = sP + (t % C::PBUF) * 2 * kSub + (share * (C::NQ / 64) + st) * kSub;
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            uint32_t x0, x1, x2, x3;
-                            ld_shared_v4(tile + sw128_offset(j, ch * 8), x0, x1, x2, x3);
-                            const uint32_t pw[4] = {x0, x1, x2, x3};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int c = st * 64 + ch * 8 + 2 * e;
-                                const float p0 = __uint_as_float(pw[e] << 16), p1 = __uint_as_float(pw[e] & 0xffff0000u);
-                                const float d0 = __shfl_sync(0xffffffffu, vreg[c >> 5], c & 31);
-                                const float d1 = __shfl_sync(0xffffffffu, vreg[(c + 1) >> 5], (c + 1) & 31);
-                                pk[c / 2] = pack_bf16x2(p0 * (__uint_as_float(rr[c]) - d0),
-                                                        p1 * (__uint_as_float(rr[c + 1]) - d1));
+                            for (int c = 0; c < 64; c += 2) {
+                                float p0 = fast_exp2(fmaf(__uint_as_float(rr[c]), a.scale_log2, -v));
+                                float p1 = fast_exp2(fmaf(__uint_as_float(rr[c + 1]), a.scale_log2, -v));
+                                if (decltype(masked)::value) {
+                                    if (hh * 64 + c < c_lo || hh * 64 + c > c_hi) p0 = 0.f;
+                                    if (hh * 64 + c + 1 < c_lo || hh * 64 + c + 1 > c_hi) p1 = 0.f;
+                                }
+                                pk[hh * 32 + c / 2] = pack_bf16x2(p0, p1);
                             }
-                        }
+                        };
+                        if (edge) p_half(std::true_type{});
+                        else p_half(std::false_type{});
+                    }
+                    // buffer t & 1 was last read at step t - 2
+                    if (real && t >= 2)
+                        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_free[half]), ((t >> 1) - 1) & 1, abort_flag, a.status, 0x2b));
+                    if (real && ok) send(pk, sP + half * 2 * kSub, smem_u32(&p_full[half]));
+                } else {
+                    // dS = P (dP - Delta), P from the S-role partner's rows. The role result is read
+                    // out and handed back first, so the next pair-step's products need not wait for P.
+                    uint32_t rr[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tmem_ld32(tR + c * 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(r_free));
+                    if (real) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_full[half]), (t >> 1) & 1, abort_flag, a.status, 0x2c));
+                    if (real && ok) {
+                        const uint32_t ptile = sP + half * 2 * kSub;
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                            for (int ch = 0; ch < 8; ++ch) {
+                                uint32_t pw[4];
+                                ld_shared_v4(ptile + hh * kSub + sw128_offset(trow, ch * 8), pw[0], pw[1], pw[2], pw[3]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int c = hh * 64 + ch * 8 + 2 * e;
+                                    pk[c / 2] = pack_bf16x2(__uint_as_float(pw[e] << 16) * (__uint_as_float(rr[c]) - v),
+                                                            __uint_as_float(pw[e] & 0xffff0000u) * (__uint_as_float(rr[c + 1]) - v));
+                                }
+                            }
+                    }
+                    // the first step's dS: its buffer was last read at step 2T - 1
+                    if (half == 0 && real) {
+                        if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
+                        if (ok) send(pk, sDS, smem_u32(ds_full));
                     }
                 }
-                if (t > 0) ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
             }
-            // write this thread's row of the share, then copy the warp's 32 rows to every peer
-            const uint32_t dst = s_role ? sP + (t % C::PBUF) * 2 * kSub : sDS;
-            const uint32_t fbar = smem_u32(s_role ? &p_full[t % C::PBUF] : ds_full);
-            if (ok) {
-#pragma unroll
-                for (int st = 0; st < C::NQ / 64; ++st) {
-                    const uint32_t tile = dst + (share * (C::NQ / 64) + st) * kSub;
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_v4(tile + sw128_offset(j, ch * 8), pk[st * 32 + ch * 4], pk[st * 32 + ch * 4 + 1],
-                                     pk[st * 32 + ch * 4 + 2], pk[st * 32 + ch * 4 + 3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    for (uint32_t peer = 0; peer < (uint32_t)C::NC; ++peer) {
-                        if (peer == rank) continue;
-#pragma unroll
-                        for (int st = 0; st < C::NQ / 64; ++st) {
-                            const uint32_t rows = dst + (share * (C::NQ / 64) + st) * kSub + quad * 4096;
-                            bulk_copy_to_peer(mapa_shared(rows, peer), rows, 4096, mapa_shared(fbar, peer));
-                        }
-                    }
-                }
-                mbar_arrive(fbar);
+            if (T > 0) ok = drain_dq(2 * T - 1) && ok;
+            if (!s_role && half == 1 && real) {  // the second step's dS, once dK / dQ of the first have read the buffer
+                ok = ok && __all_sync(0xffffffffu, mbar_wait(smem_u32(ds_free), (t - 1) & 1, abort_flag, a.status, 0x2f));
+                if (ok) send(pk, sDS, smem_u32(ds_full));
             }
-            if (t > 0) ok = drain_dq(t - 1) && ok;
+            ok = drain_dq(2 * T) && ok;
             ok = named_bar_and(3, 128, ok);
             if (!ok) break;
         }
-        if (ok) ok = drain_dq(n - 1);
+        if (ok && (n & 1) == 0) ok = drain_dq(n - 1);
         if (tid == 64) bulk_wait_group0();  // every reduce issued by this CTA has landed
         // every arrival owed to this CTA's exchange barriers has landed before it exits
         if (ok) {
             if (s_role) {
-                for (int t = max(0, n - C::PBUF); t < n; ++t)
-                    mbar_drain(smem_u32(&p_free[t % C::PBUF]), (t / C::PBUF) & 1, a.status, 0x30);
+                for (int t = max(0, n - 2); t < n; ++t)
+                    mbar_drain(smem_u32(&p_free[t & 1]), (t >> 1) & 1, a.status, 0x30);
             }
             else mbar_drain(smem_u32(ds_free), (n - 1) & 1, a.status, 0x31);
         }
@@ -546,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {  // warp-uniform: the TMEM loads below are warp collectives
+            const bool key_ok = kabs < L;
             const size_t row = (size_t)(a.cu_seqlens ? seq_start + kabs : seq * a.S + kabs) * a.Hkv + g;
             uint16_t* dv_row = a.dV + row * D + c0;
             uint16_t* dk_row = a.dK + row * D + c0;
