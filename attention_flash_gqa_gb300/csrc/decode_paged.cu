@@ -141,11 +141,13 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
-    // Launched with programmatic stream serialisation: wait for the previous kernel on the stream
-    // to finish (and its writes to be visible) before touching anything, so the call keeps plain
-    // stream order while its CTAs become resident and start early. Then let the merge kernel that
-    // follows be scheduled: it waits for this grid's completion before it reads its outputs.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Launched with programmatic stream serialisation, so the grid may start while the kernel
+    // before it on the stream still runs when that kernel allows it (the merge kernel of a previous
+    // decode call does; a kernel launched without the attribute finishes first). The prologue
+    // and the first page copies read only seq_lens, block_table and the caches; the consumer
+    // warps wait (griddepcontrol.wait) for the predecessor's completion before they read q or
+    // write the partials, so the call keeps plain stream order for everything else. The merge
+    // kernel that follows may be scheduled at once: it waits for this grid before it reads.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
@@ -306,6 +308,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     }
 
     // ---------------------------------- consumers ----------------------------------------
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Every consumer warp serves one KV head for all G query heads of its group (one K/V
     // row read feeds all of them) with its own running softmax state; when two warps share
     // a head (token halves), they are merged like split partials at the end.

@@ -181,9 +181,16 @@ ATTN_API int attn_bwd(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v
  *   256-byte aligned; it holds the split partials of the requests that several CTAs share and
  *   each request's offset into them. Contents on entry do not matter. Calls that share a
  *   workspace must not overlap on the GPU.
- *   Enqueues two kernels on `stream`: the split decode and the merge of its partials. The merge
- *   is launched with programmatic stream serialisation (it may become resident while the decode
- *   grid runs and waits on the device for that grid's completion).
+ *   Enqueues two kernels on `stream`: the split decode and the merge of its partials, both
+ *   launched with programmatic stream serialisation. The merge may become resident while the
+ *   decode grid runs and waits on the device for that grid's completion. The decode grid may
+ *   start while the kernel enqueued just before it still runs, if that kernel allows dependents
+ *   to launch early (the merge of a previous decode call does; a kernel launched without that
+ *   attribute, the default, always finishes first): it then reads seq_lens, block_table and the
+ *   caches before that kernel has finished, and waits for it only before reading q or writing
+ *   the workspace. So a kernel that allows early launch must not write those three inputs of
+ *   the decode call that follows it. In particular the o / lse of one decode call may be the q
+ *   of the next, but not its caches, block_table or seq_lens.
  */
 ATTN_API int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16* v_cache,
                       const int32_t* block_table, const int32_t* seq_lens, attn_bf16* o, float* lse, int B, int Hq,
