@@ -46,7 +46,7 @@ constexpr int kSoftmaxThreads = 256;
 constexpr uint32_t kSubBytes = 16384;  // 128 rows x 64 bf16
 constexpr float kRescaleLog2 = 8.0f;
 
-template <int DQK>
+template <int DQK, bool PAIR = false>
 struct FwdCfg {
     static constexpr int kDV = DQK < 256 ? DQK : 256;      // O columns per CTA
     // score buffers in tensor memory: three when O takes at most 128 of the 512 columns, so the
@@ -55,8 +55,10 @@ struct FwdCfg {
     static constexpr int kSubs = DQK >= 128 ? 2 : 1;        // 64-column sub-tiles per slot
     static constexpr int kSlotCols = 64 * kSubs;
     static constexpr uint32_t kSlotBytes = kSubs * kSubBytes;
-    static constexpr int kQChunks = DQK / kSlotCols;        // slots per K tile
-    static constexpr int kVChunks = kDV / kSlotCols;        // slots per V tile (this CTA's columns)
+    // A CTA of a pair holds half of each key tile: its 64 keys x 256 columns per slot (four
+    // 8 KB sub-tiles of 64 rows), and half of the V columns of the O block: one slot.
+    static constexpr int kQChunks = PAIR ? DQK / 256 : DQK / kSlotCols;  // slots per K tile
+    static constexpr int kVChunks = PAIR ? 1 : kDV / kSlotCols;          // slots per V tile (this CTA's columns)
     // ring depth: what shared memory leaves next to the resident Q tile
     static constexpr int kStages = DQK == 512 ? 3 : DQK == 256 ? 5 : DQK == 128 ? 6 : 12;
     static constexpr uint32_t kQBytes = DQK * 256;  // 128 rows x DQK bf16
@@ -67,6 +69,7 @@ struct FwdCfg {
     // paged slots: the slot's sub-tiles interleaved per 8-row group
     static constexpr uint32_t kPagedGroupStride = 1024 * kSubs;
     static_assert(kSmem <= 232448, "shared memory");
+    static_assert(!PAIR || DQK >= 256, "the CTA pair serves head_dim 256 and 512");
 };
 
 struct FwdArgs {
@@ -92,11 +95,19 @@ struct FwdArgs {
 // (keys 8G .. 8G+7) at byte G*2048 + c*1024, each a 1 KB 128-byte-swizzle atom. The MMA
 // descriptors differ only in their strides (kPagedGroupStride); one box moves 256 bytes per
 // row, which the TMA engine streams about 1.5x faster than sixteen 16-row boxes of 64 columns.
-template <int DQK, bool PAGED>
+// PAIR: a cluster of two CTAs (a CTA pair) computes one query tile for two query heads of the
+// same GQA group, so both need the same keys and values. The even CTA issues every MMA for
+// both as an M = 256 product (tcgen05 cta_group::2): for S = Q K^T each CTA supplies its own Q
+// rows and half of the key tile (64 keys), for P V its own P (tensor memory) and half of the
+// O block's V columns. Each CTA therefore streams half of K and half of V per key step. Both
+// CTAs' copies complete on the even CTA's barriers; the MMA commits are multicast to both; the
+// odd CTA's softmax warps report P ready on the even CTA's barrier.
+template <int DQK, bool PAGED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, FwdArgs a) {
-    using C = FwdCfg<DQK>;
+    using C = FwdCfg<DQK, PAIR>;
+    static_assert(!(PAGED && PAIR), "the CTA pair serves the dense and varlen forward");
     // ---- which tile ------------------------------------------------------------------
     const int h = blockIdx.x;
     const int seq = blockIdx.y / a.nsplit, split = blockIdx.y % a.nsplit;
@@ -163,7 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(smem_u32(q_full), 1);
         for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&s_full[b]), 1);
-        for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&p_full[b]), kSoftmaxThreads);
+        // P ready: every softmax thread, or (pair) one arrival per softmax warp of both CTAs, counted
+        // on the even CTA's barrier
+        for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&p_full[b]), PAIR ? 2 * kSoftmaxThreads / 32 : kSoftmaxThreads);
         for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&pv_done[b]), 1);
         mbar_init(smem_u32(mma_idle), 1);
         mbar_init(smem_u32(vfix), 1);
@@ -171,13 +184,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), 512);  // the same columns in both CTAs of the pair
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), 512);
+            tmem_relinquish();
+        }
     }
     __syncthreads();
+    if (PAIR) {  // the peer's barriers are initialised before anything signals them
+        tc_fence_before();
+        cluster_sync_all();
+    }
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     const uint32_t tO = tbase, tS0 = tbase + 512 - C::kSBuf * 128;
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0;  // 0: the CTA that issues the pair's MMAs
+    // the even CTA's barriers, in the cluster window (pair: both CTAs' copies complete on them)
+    auto lead_bar = [&](const uint64_t* bar) -> uint32_t { return PAIR ? mapa_shared(smem_u32(bar), 0) : smem_u32(bar); };
 
     // keys past the end in the last tile (paged: their cache rows may hold any bits)
     const bool tail_fix = PAGED && (t_end * kBKV > L);
@@ -294,29 +319,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
             const int row_q = seq_start + q0;
-            mbar_expect_tx(smem_u32(q_full), C::kQBytes);
-            for (int c = 0; c < DQK / 64; ++c)
-                tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, row_q, bcoord);
+            // pair: the even CTA expects both CTAs' bytes on its barriers, and the copies of both
+            // complete there
+            if (crank == 0) mbar_expect_tx(smem_u32(q_full), (PAIR ? 2 : 1) * C::kQBytes);
+            for (int c = 0; c < DQK / 64; ++c) {
+                if (PAIR) tma_load_4d_pair(sQ + c * kSubBytes, &tq, lead_bar(q_full), c * 64, h, row_q, bcoord);
+                else tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, row_q, bcoord);
+            }
             int slot = 0, round = 0;
             bool ok = true;
-            auto load_chunk = [&](const CUtensorMap* map, int col0, int row0) -> bool {
+            // one slot: kSubs sub-tiles of 128 rows x 64 columns (col0 + 64 sub, rows row0 ..); pair
+            // K slots: four sub-tiles of 64 rows (this CTA's keys) x 64 columns
+            auto load_chunk = [&](const CUtensorMap* map, int col0, int row0, bool k_half) -> bool {
                 if (round > 0 && !mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag, a.status, 0x11)) return false;
-                const uint32_t fb = smem_u32(&full[slot]);
-                mbar_expect_tx(fb, C::kSlotBytes);
+                if (crank == 0) mbar_expect_tx(smem_u32(&full[slot]), (PAIR ? 2 : 1) * C::kSlotBytes);
                 const uint32_t dst = sSlots + slot * C::kSlotBytes;
-                for (int sub = 0; sub < C::kSubs; ++sub)
-                    tma_load_4d(dst + sub * kSubBytes, map, fb, col0 + sub * 64, g, row0, bcoord);
+                if (PAIR) {
+                    const uint32_t fb = lead_bar(&full[slot]);
+                    if (k_half) {
+                        for (int sub = 0; sub < 4; ++sub)
+                            tma_load_4d_pair(dst + sub * (kSubBytes / 2), map, fb, col0 + sub * 64, g, row0 + 64 * (int)crank, bcoord);
+                    } else {
+                        for (int sub = 0; sub < C::kSubs; ++sub)
+                            tma_load_4d_pair(dst + sub * kSubBytes, map, fb, col0 + 128 * (int)crank + sub * 64, g, row0, bcoord);
+                    }
+                } else {
+                    const uint32_t fb = smem_u32(&full[slot]);
+                    for (int sub = 0; sub < C::kSubs; ++sub)
+                        tma_load_4d(dst + sub * kSubBytes, map, fb, col0 + sub * 64, g, row0, bcoord);
+                }
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
             auto load_k = [&](int t) -> bool {
                 for (int c = 0; c < C::kQChunks; ++c)
-                    if (!load_chunk(&tk, c * C::kSlotCols, seq_start + (t_begin + t) * kBKV)) return false;
+                    if (!load_chunk(&tk, c * (PAIR ? 256 : C::kSlotCols), seq_start + (t_begin + t) * kBKV, true)) return false;
                 return true;
             };
             auto load_v = [&](int t) -> bool {
                 for (int c = 0; c < C::kVChunks; ++c)
-                    if (!load_chunk(&tv, dv0 + c * C::kSlotCols, seq_start + (t_begin + t) * kBKV)) return false;
+                    if (!load_chunk(&tv, dv0 + c * C::kSlotCols, seq_start + (t_begin + t) * kBKV, false)) return false;
                 return true;
             };
             // the issuer's order: K(0) .. K(kSBuf - 1), then V(j), K(j + kSBuf) for every step j
@@ -325,19 +367,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = load_v(j);
                 if (ok && j + C::kSBuf < n) ok = load_k(j + C::kSBuf);
             }
-            // Drain: wait (bounded) for the last copy issued into every slot.
-            const int issued = round * C::kStages + slot;
-            for (int s = 0; s < C::kStages && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
-                mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x18);
+            // Drain: wait (bounded) for the last copy issued into every slot. Pair: the even CTA's
+            // barriers count both CTAs' copies, and the odd CTA stays until then (the cluster
+            // barrier at the end).
+            if (crank == 0) {
+                const int issued = round * C::kStages + slot;
+                for (int s = 0; s < C::kStages && s < issued; ++s) {
+                    const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+                    mbar_drain(smem_u32(&full[s]), (last / C::kStages) & 1, a.status, 0x18);
+                }
+                mbar_drain(smem_u32(q_full), 0, a.status, 0x19);
             }
-            mbar_drain(smem_u32(q_full), 0, a.status, 0x19);
         }
     } else if (warp == 1) {
         // ------------------------------- UMMA issuer -----------------------------------
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // Q K^T: both K-major
-            constexpr uint32_t idO = idesc_bf16_f32(128, C::kSlotCols, false, true);  // P (TMEM) V: V is N-major
+        // (pair: the even CTA issues for both; the odd CTA's warp 1 only allocates tensor memory)
+        if (lane == 0 && crank == 0) {
+            // Q K^T: both K-major (pair: M = 256 over both CTAs' query rows, N = 128 keys split 64 / 64)
+            constexpr uint32_t idS = idesc_bf16_f32(PAIR ? 256 : 128, 128, false, false);
+            // P (TMEM) V: V is N-major (pair: N = the 256-column O block, 128 columns in each CTA)
+            constexpr uint32_t idO = idesc_bf16_f32(PAIR ? 256 : 128, PAIR ? 256 : C::kSlotCols, false, true);
+            // a commit reaches this CTA's barrier, or (pair) the barrier at that offset in both CTAs
+            auto commit = [&](uint64_t* bar) {
+                if (PAIR) umma_commit_pair(smem_u32(bar), (uint16_t)3);
+                else umma_commit(smem_u32(bar));
+            };
             int slot = 0, round = 0;
             bool ok = mbar_wait(smem_u32(q_full), 0, abort_flag, a.status, 0x12);
             tc_fence_after();
@@ -347,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto release_slot = [&]() {
-                umma_commit(smem_u32(&empty[slot]));
+                commit(&empty[slot]);
                 if (++slot == C::kStages) slot = 0, ++round;
             };
             auto issue_s = [&](int buf) -> bool {
@@ -355,18 +409,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kQChunks; ++c) {
                     if (!next_slot()) return false;
                     const uint32_t kslot = sSlots + slot * C::kSlotBytes;
-                    for (int sub = 0; sub < C::kSubs; ++sub)
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad =
-                                sdesc_sw128(sQ + (C::kSubs * c + sub) * kSubBytes + kk * 32, 16, 1024);
-                            const uint64_t bd =
-                                PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, C::kPagedGroupStride)
-                                      : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
-                            umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
-                        }
+                    if (PAIR) {  // four sub-tiles of this CTA's 64 keys x 64 columns (8 KB each)
+                        for (int sub = 0; sub < 4; ++sub)
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_pair_ss(dst, sdesc_sw128(sQ + (4 * c + sub) * kSubBytes + kk * 32, 16, 1024),
+                                             sdesc_sw128(kslot + sub * (kSubBytes / 2) + kk * 32, 16, 1024), idS,
+                                             (c | sub | kk) ? 1u : 0u);
+                    } else {
+                        for (int sub = 0; sub < C::kSubs; ++sub)
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad =
+                                    sdesc_sw128(sQ + (C::kSubs * c + sub) * kSubBytes + kk * 32, 16, 1024);
+                                const uint64_t bd =
+                                    PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, C::kPagedGroupStride)
+                                          : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
+                                umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
+                            }
+                    }
                     release_slot();
                 }
-                umma_commit(smem_u32(&s_full[buf]));
+                commit(&s_full[buf]);
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
@@ -383,12 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd =
                             PAGED ? sdesc_sw128(vslot + kk * 2 * C::kPagedGroupStride, 1024, C::kPagedGroupStride)
                                   : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
-                        umma_bf16_ts(tO + c * C::kSlotCols, tP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
+                        if (PAIR)
+                            umma_pair_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                        else
+                            umma_bf16_ts(tO + c * C::kSlotCols, tP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     release_slot();
                 }
-                umma_commit(smem_u32(&pv_done[j % C::kSBuf]));
+                commit(&pv_done[j % C::kSBuf]);
                 return true;
             };
             for (int b = 0; ok && b < C::kSBuf && b < n; ++b) ok = issue_s(b);
@@ -402,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok && j + C::kSBuf < n) ok = issue_s(j % C::kSBuf);
             }
             // every issued UMMA has finished before TMEM may be released
-            umma_commit(smem_u32(mma_idle));
+            if (PAIR) umma_commit_pair(smem_u32(mma_idle), (uint16_t)1);
+            else umma_commit(smem_u32(mma_idle));
             mbar_drain(smem_u32(mma_idle), 0, a.status, 0x1a);
         }
     } else {
@@ -513,7 +579,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tS0 + buf * 128 + 64 * hf + lane_base, pk);
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(smem_u32(&p_full[buf]));
+            if (PAIR) {  // one arrival per warp, on the even CTA's barrier (it issues P V for both)
+                __syncwarp();
+                if (lane == 0) {
+                    if (crank == 0) mbar_arrive(smem_u32(&p_full[buf]));
+                    else mbar_arrive_cluster(lead_bar(&p_full[buf]));
+                }
+            } else {
+                mbar_arrive(smem_u32(&p_full[buf]));
+            }
         }
         // ---- epilogue: O / l -> bf16, lse -------------------------------------------------
         // the last P V, and so every earlier one; its barrier has no older phase pending
@@ -557,15 +631,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
     }
     __syncthreads();
+    if (PAIR) {  // the even CTA has drained every copy and product of the pair
+        tc_fence_before();
+        cluster_sync_all();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, 512);
+        if (PAIR) tmem_dealloc_pair(tbase, 512);
+        else tmem_dealloc(tbase, 512);
     }
+    if (PAIR) cluster_sync_all();  // neither CTA leaves while the other may still address it
 }
 
-template <int DQK, bool PAGED>
+template <int DQK, bool PAGED, bool PAIR>
 cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
-    using C = FwdCfg<DQK>;
+    using C = FwdCfg<DQK, PAIR>;
     FwdArgs a;
     a.o = L.o, a.lse = L.lse, a.cu_seqlens = L.cu_seqlens, a.status = L.status;
     a.block_table = L.block_table, a.seq_lens = L.seq_lens, a.cu_q = L.cu_q;
@@ -576,14 +656,33 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
     a.T = L.total_rows;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<DQK, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(fwd_kernel<DQK, PAGED, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid(L.Hq, L.nseq * a.nsplit, a.n_qtiles);
     static const char* const kNames[2][4] = {{"fwd_d64", "fwd_d128", "fwd_d256", "fwd_d512"},
                                              {"fwd_paged_d64", "fwd_paged_d128", "fwd_paged_d256", "fwd_paged_d512"}};
     const char* name = kNames[PAGED ? 1 : 0][DQK == 64 ? 0 : DQK == 128 ? 1 : DQK == 256 ? 2 : 3];
     const ProfMark m = prof_begin(stream, name);
-    fwd_kernel<DQK, PAGED><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
+    if (PAIR) {
+        // CTA pairs along the head dimension: query heads 2i, 2i + 1 (one GQA group) share the keys
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fwd_kernel<DQK, PAGED, PAIR>, L.tq, L.tk_half, L.tv, a);
+        prof_end(stream, m);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    fwd_kernel<DQK, PAGED, PAIR><<<grid, kThreads, C::kSmem, stream>>>(L.tq, L.tk, L.tv, a);
     prof_end(stream, m);
     return cudaGetLastError();
 }
@@ -593,10 +692,16 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     if (L.nseq == 0 || L.S == 0) return cudaSuccess;
     const bool paged = L.block_table != nullptr;
-    if (L.D == 64) return paged ? launch_fwd_t<64, true>(L, stream) : launch_fwd_t<64, false>(L, stream);
-    if (L.D == 128) return paged ? launch_fwd_t<128, true>(L, stream) : launch_fwd_t<128, false>(L, stream);
-    if (L.D == 256) return paged ? launch_fwd_t<256, true>(L, stream) : launch_fwd_t<256, false>(L, stream);
-    if (L.D == 512) return paged ? launch_fwd_t<512, true>(L, stream) : launch_fwd_t<512, false>(L, stream);
+    // CTA pairs when two consecutive query heads always share a KV head (an even GQA group)
+    const bool pair = !paged && L.pair_ok && (L.Hq / L.Hkv) % 2 == 0;
+    if (L.D == 64) return paged ? launch_fwd_t<64, true, false>(L, stream) : launch_fwd_t<64, false, false>(L, stream);
+    if (L.D == 128) return paged ? launch_fwd_t<128, true, false>(L, stream) : launch_fwd_t<128, false, false>(L, stream);
+    if (L.D == 256)
+        return paged ? launch_fwd_t<256, true, false>(L, stream)
+                     : pair ? launch_fwd_t<256, false, true>(L, stream) : launch_fwd_t<256, false, false>(L, stream);
+    if (L.D == 512)
+        return paged ? launch_fwd_t<512, true, false>(L, stream)
+                     : pair ? launch_fwd_t<512, false, true>(L, stream) : launch_fwd_t<512, false, false>(L, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -44,6 +44,8 @@ cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream);
 // box (16 rows x 128 dims of one head of one page).
 struct FwdLaunch {
     CUtensorMap tq, tk, tv;
+    CUtensorMap tk_half;        // k with a 64 x 1 x 64 x 1 box (CTA-pair forward: half a key tile per CTA)
+    bool pair_ok = false;       // tk_half is valid: the CTA-pair forward may be used
     uint16_t* o;
     float* lse;
     const int32_t* cu_seqlens;  // null: dense (or paged)
