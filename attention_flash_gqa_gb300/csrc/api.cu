@@ -188,7 +188,7 @@ int fwd_common(const attn_bf16* q, const attn_bf16* k, const attn_bf16* v, attn_
     if (!make_map(&L.tq, q, D, Hq, map_rows, batch_dim) || !make_map(&L.tk, k, D, Hkv, map_rows, batch_dim) ||
         !make_map(&L.tv, v, D, Hkv, map_rows, batch_dim))
         return ATTN_ERR_LAUNCH;
-    if (D >= 256 && (Hq / Hkv) % 2 == 0) {
+    if (D == 512 && (Hq / Hkv) % 2 == 0) {
         if (!make_map(&L.tk_half, k, D, Hkv, map_rows, batch_dim, 64)) return ATTN_ERR_LAUNCH;
         L.pair_ok = true;
     }

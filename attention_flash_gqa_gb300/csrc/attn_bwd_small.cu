@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);  // X_u x Y_u^T: both K-major
             constexpr uint32_t idG = idesc_bf16_f32(128, 64, false, true);    // P^T / dS^T x 64 slice columns
-            constexpr uint32_t idQ = idesc_bf16_f32(128, 64, true, true);     // dS (MN-major) x 64 columns of K
+            constexpr uint32_t idG128 = idesc_bf16_f32(128, 128, false, true);  // dS^T x the slice, both halves
+            constexpr uint32_t idQ128 = idesc_bf16_f32(128, 128, true, true);   // dS x the slice of K, both halves
             int slot = 0, round = 0;
             auto acquire = [&](int& s) -> bool {
                 if (!mbar_wait(smem_u32(&full[slot]), round & 1, abort_flag, a.status, 0x42)) return false;
@@ -319,24 +320,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x45);
                 if (!ok) break;
                 tc_fence_after();
-                // dQ_c = dS K_c first (its readout starts while dK runs), into R1; K_c is resident
+                // dQ_c = dS K_c first (its readout starts while dK runs), into R1; K_c is resident,
+                // its two 64-column sub-tiles adjacent: one N = 128 product per K step
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sDS + kk * 2048, kSub, 1024);
-                    umma_bf16_ss(tDQ, ad, sdesc_sw128(sK + us0 * kSub + kk * 2048, kSub, 1024), idQ, kk > 0 ? 1u : 0u);
-                    umma_bf16_ss(tDQ + 64, ad, sdesc_sw128(sK + (us0 + 1) * kSub + kk * 2048, kSub, 1024), idQ,
-                                 kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024),
+                                 sdesc_sw128(sK + us0 * kSub + kk * 2048, kSub, 1024), idQ128, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 // dK_c += dS^T Q_c: B = the slice's two Q sub-tiles
                 ok = acquire(b0) && acquire(b1);
                 if (!ok) break;
+                if (b1 == b0 + 1) {  // adjacent ring slots (the ring did not wrap between them): N = 128
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad = sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
-                    const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
-                    umma_bf16_ss(tDK, ad, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
-                    umma_bf16_ss(tDK + 64, ad, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                    for (int kk = 0; kk < 8; ++kk)
+                        umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
+                                     sdesc_sw128(ring(b0) + kk * 2048, C::kSlot, 1024), idG128, (t > 0 || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                        const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
+                        umma_bf16_ss(tDK, ad, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
+                        umma_bf16_ss(tDK + 64, ad, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                    }
                 }
                 umma_commit(smem_u32(&empty[b0]));
                 umma_commit(smem_u32(&empty[b1]));

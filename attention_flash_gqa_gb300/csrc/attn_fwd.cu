@@ -692,8 +692,12 @@ cudaError_t launch_fwd_t(const FwdLaunch& L, cudaStream_t stream) {
 cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     if (L.nseq == 0 || L.S == 0) return cudaSuccess;
     const bool paged = L.block_table != nullptr;
-    // CTA pairs when two consecutive query heads always share a KV head (an even GQA group)
-    const bool pair = !paged && L.pair_ok && (L.Hq / L.Hkv) % 2 == 0;
+    // CTA pairs when two consecutive query heads always share a KV head (an even GQA group), at
+    // head_dim 512: there each CTA streams 192 KB of keys and values per key step alone, against
+    // 96 KB in a pair. At head_dim 256 the sliding-window workload (about nine key steps per
+    // CTA) measured slower in pairs (0.713 against 0.665 ms), the pair's fixed cost outweighing
+    // the halved stream, so 256 keeps single CTAs.
+    const bool pair = !paged && L.pair_ok && (L.Hq / L.Hkv) % 2 == 0 && L.D == 512;
     if (L.D == 64) return paged ? launch_fwd_t<64, true, false>(L, stream) : launch_fwd_t<64, false, false>(L, stream);
     if (L.D == 128) return paged ? launch_fwd_t<128, true, false>(L, stream) : launch_fwd_t<128, false, false>(L, stream);
     if (L.D == 256)
