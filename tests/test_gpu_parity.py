@@ -86,6 +86,14 @@ def test_wide_gqa_group(orc, D):
     compare_dense(orc, synth.dense(1, 16, 1, 200, D, 0, seed=16 + D))
 
 
+@pytest.mark.parametrize("Hq,Hkv,window", [(2, 2, 0), (3, 1, 0), (6, 3, 130), (4, 2, 0), (8, 2, 300)])
+def test_d512_forward_paths(orc, Hq, Hkv, window):
+    """Head_dim 512: even GQA groups run the forward in CTA pairs (two query heads of a group on
+    two SMs sharing one MMA), odd groups (1, 3) in single CTAs; both against the oracle, with a
+    ragged last tile and, for some, a window."""
+    compare_dense(orc, synth.dense(1, Hq, Hkv, 333, 512, window, seed=Hq * 7 + Hkv + window))
+
+
 def test_forward_is_deterministic():
     p = synth.dense(1, 4, 2, 300, 512, 0, seed=4, with_do=False)
     q, k, v = to_dev(p.q), to_dev(p.k), to_dev(p.v)
