@@ -264,17 +264,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++slot == C::kStages) slot = 0, ++round;
                 return true;
             };
-            auto ring = [&](int s) { return sRing + (uint32_t)s * C::kSlot; };
             const int us0 = c0 / 64;  // the slice's first sub-tile
+            // descriptor bases, stepped with sdesc_at in the loops (K-major views: LBO unused;
+            // N-major: LBO = the 64-column sub-tile stride)
+            const uint64_t dKk = sdesc_sw128(sK, 16, 1024), dKn = sdesc_sw128(sK, kSub, 1024);
+            const uint64_t dRk = sdesc_sw128(sRing, 16, 1024), dRn = sdesc_sw128(sRing, kSub, 1024);
+            const uint64_t dRn2 = sdesc_sw128(sRing, C::kSlot, 1024);
+            const uint64_t dSk = sdesc_sw128(sDS, 16, 1024), dSn = sdesc_sw128(sDS, kSub, 1024);
+            auto slot_desc = [&](uint64_t base, int s) { return sdesc_at(base, (uint32_t)s * C::kSlot); };
             // S^T = sum_u K_u (resident) Q_u^T, each Q_u released once read
             auto issue_s = [&]() -> bool {
                 for (int u = 0; u < C::NSUB; ++u) {
                     int ys;
                     if (!acquire(ys)) return false;
+                    const uint64_t da = sdesc_at(dKk, u * kSub), db = slot_desc(dRk, ys);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(tR0, sdesc_sw128(sK + u * kSub + kk * 32, 16, 1024),
-                                     sdesc_sw128(ring(ys) + kk * 32, 16, 1024), idS, (u | kk) ? 1u : 0u);
+                        umma_bf16_ss(tR0, sdesc_at(da, kk * 32), sdesc_at(db, kk * 32), idS, (u | kk) ? 1u : 0u);
                     umma_commit(smem_u32(&empty[ys]));
                 }
                 umma_commit(smem_u32(s_full));
@@ -287,10 +293,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < C::NSUB; ++i) {
                     int xs, ys;
                     if (!acquire(xs) || !acquire(ys)) return false;
+                    const uint64_t da = slot_desc(dRk, xs), db = slot_desc(dRk, ys);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(tR1, sdesc_sw128(ring(xs) + kk * 32, 16, 1024),
-                                     sdesc_sw128(ring(ys) + kk * 32, 16, 1024), idS, (i | kk) ? 1u : 0u);
+                        umma_bf16_ss(tR1, sdesc_at(da, kk * 32), sdesc_at(db, kk * 32), idS, (i | kk) ? 1u : 0u);
                     umma_commit(smem_u32(&empty[xs]));
                     if (i >= C::NSUB - DS / 64) doc[i - (C::NSUB - DS / 64)] = ys;
                     else umma_commit(smem_u32(&empty[ys]));
@@ -308,12 +314,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 int b0 = doc[0], b1 = doc[1];
+                {
+                    const uint64_t db0 = slot_desc(dRn, b0), db1 = slot_desc(dRn, b1);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t at = tR0 + (kk >> 2) * 64 + (kk & 3) * 8;
-                    const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
-                    umma_bf16_ts(tDV, at, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
-                    umma_bf16_ts(tDV + 64, at, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t at = tR0 + (kk >> 2) * 64 + (kk & 3) * 8;
+                        const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
+                        umma_bf16_ts(tDV, at, sdesc_at(db0, kk * 2048), idG, accf);
+                        umma_bf16_ts(tDV + 64, at, sdesc_at(db1, kk * 2048), idG, accf);
+                    }
                 }
                 umma_commit(smem_u32(&empty[b0]));
                 umma_commit(smem_u32(&empty[b1]));
@@ -324,24 +333,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // its two 64-column sub-tiles adjacent: one N = 128 product per K step
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024),
-                                 sdesc_sw128(sK + us0 * kSub + kk * 2048, kSub, 1024), idQ128, kk > 0 ? 1u : 0u);
+                    umma_bf16_ss(tDQ, sdesc_at(dSn, kk * 2048), sdesc_at(dKn, us0 * kSub + kk * 2048), idQ128,
+                                 kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 // dK_c += dS^T Q_c: B = the slice's two Q sub-tiles
                 ok = acquire(b0) && acquire(b1);
                 if (!ok) break;
                 if (b1 == b0 + 1) {  // adjacent ring slots (the ring did not wrap between them): N = 128
+                    const uint64_t db = slot_desc(dRn2, b0);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
-                                     sdesc_sw128(ring(b0) + kk * 2048, C::kSlot, 1024), idG128, (t > 0 || kk > 0) ? 1u : 0u);
+                        umma_bf16_ss(tDK, sdesc_at(dSk, (kk >> 2) * kSub + (kk & 3) * 32), sdesc_at(db, kk * 2048),
+                                     idG128, (t > 0 || kk > 0) ? 1u : 0u);
                 } else {
+                    const uint64_t db0 = slot_desc(dRn, b0), db1 = slot_desc(dRn, b1);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024);
+                        const uint64_t ad = sdesc_at(dSk, (kk >> 2) * kSub + (kk & 3) * 32);
                         const uint32_t accf = (t > 0 || kk > 0) ? 1u : 0u;
-                        umma_bf16_ss(tDK, ad, sdesc_sw128(ring(b0) + kk * 2048, kSub, 1024), idG, accf);
-                        umma_bf16_ss(tDK + 64, ad, sdesc_sw128(ring(b1) + kk * 2048, kSub, 1024), idG, accf);
+                        umma_bf16_ss(tDK, ad, sdesc_at(db0, kk * 2048), idG, accf);
+                        umma_bf16_ss(tDK + 64, ad, sdesc_at(db1, kk * 2048), idG, accf);
                     }
                 }
                 umma_commit(smem_u32(&empty[b0]));
@@ -379,13 +390,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             // acc(128 x 128) = X (resident [keys x D], K-major) x Y^T (ring tile [queries x D], K-major)
+            // descriptor bases, stepped with sdesc_at in the loops
+            const uint64_t dRk = sdesc_sw128(sRing, 16, 1024), dRn = sdesc_sw128(sRing, kSub, 1024);
+            const uint64_t dSk = sdesc_sw128(sDS, 16, 1024), dSn = sdesc_sw128(sDS, kSub, 1024);
+            const uint64_t dKn = sdesc_sw128(sK, kSub, 1024);
             auto rows_x_tile = [&](uint32_t dacc, uint32_t x, int ys) {
-                const uint32_t y = sRing + ys * C::kSlot;
+                const uint64_t dx = sdesc_sw128(x, 16, 1024), dy = sdesc_at(dRk, (uint32_t)ys * C::kSlot);
+#pragma unroll
                 for (int u = 0; u < C::NSUB; ++u)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16_ss(dacc, sdesc_sw128(x + u * kSub + kk * 32, 16, 1024),
-                                     sdesc_sw128(y + u * kSub + kk * 32, 16, 1024), idS, (u | kk) ? 1u : 0u);
+                        umma_bf16_ss(dacc, sdesc_at(dx, u * kSub + kk * 32), sdesc_at(dy, u * kSub + kk * 32), idS,
+                                     (u | kk) ? 1u : 0u);
             };
             bool ok = mbar_wait(smem_u32(kv_full), 0, abort_flag, a.status, 0x43);
             tc_fence_after();
@@ -405,11 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(smem_u32(p_full), t & 1, abort_flag, a.status, 0x44);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t dob = sRing + ds * C::kSlot;
+                const uint64_t dob = sdesc_at(dRn, (uint32_t)ds * C::kSlot);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)  // queries 64h .. 64h+63 of P^T sit at R0 columns 64h .. 64h+31
-                    umma_bf16_ts(tDV, tR0 + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(dob + kk * 2048, kSub, 1024),
-                                 idG, (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ts(tDV, tR0 + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(dob, kk * 2048), idG,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(smem_u32(&empty[ds]));
                 const int qs_t = qs;
                 // S^T(t+1) over R0: issued after the P V read of R0 (the MMA pipe runs in order)
@@ -431,15 +447,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_ss(tDQ, sdesc_sw128(sDS + kk * 2048, kSub, 1024), sdesc_sw128(sK + kk * 2048, kSub, 1024),
-                                 idQ, kk > 0 ? 1u : 0u);
+                    umma_bf16_ss(tDQ, sdesc_at(dSn, kk * 2048), sdesc_at(dKn, kk * 2048), idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 // dK += dS^T Q: A = dS^T (K-major, shared memory), B = Q (N-major)
-                const uint32_t qb = sRing + qs_t * C::kSlot;
+                const uint64_t qb = sdesc_at(dRn, (uint32_t)qs_t * C::kSlot);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    umma_bf16_ss(tDK, sdesc_sw128(sDS + (kk >> 2) * kSub + (kk & 3) * 32, 16, 1024),
-                                 sdesc_sw128(qb + kk * 2048, kSub, 1024), idG, (t > 0 || kk > 0) ? 1u : 0u);
+                    umma_bf16_ss(tDK, sdesc_at(dSk, (kk >> 2) * kSub + (kk & 3) * 32), sdesc_at(qb, kk * 2048), idG,
+                                 (t > 0 || kk > 0) ? 1u : 0u);
                 umma_commit(smem_u32(&empty[qs_t]));
                 umma_commit(smem_u32(ds_free));
                 // dP^T(t+1) over R1 (at D = 128 once dQ(t) has left it)

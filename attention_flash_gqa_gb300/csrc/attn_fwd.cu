@@ -404,25 +404,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 commit(&empty[slot]);
                 if (++slot == C::kStages) slot = 0, ++round;
             };
+            // descriptor bases, stepped with sdesc_at in the loops
+            const uint64_t dQk = sdesc_sw128(sQ, 16, 1024);
             auto issue_s = [&](int buf) -> bool {
                 const uint32_t dst = tS0 + buf * 128;
                 for (int c = 0; c < C::kQChunks; ++c) {
                     if (!next_slot()) return false;
                     const uint32_t kslot = sSlots + slot * C::kSlotBytes;
                     if (PAIR) {  // four sub-tiles of this CTA's 64 keys x 64 columns (8 KB each)
+                        const uint64_t dq = sdesc_at(dQk, 4 * c * kSubBytes), dk = sdesc_sw128(kslot, 16, 1024);
+#pragma unroll
                         for (int sub = 0; sub < 4; ++sub)
+#pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                umma_pair_ss(dst, sdesc_sw128(sQ + (4 * c + sub) * kSubBytes + kk * 32, 16, 1024),
-                                             sdesc_sw128(kslot + sub * (kSubBytes / 2) + kk * 32, 16, 1024), idS,
-                                             (c | sub | kk) ? 1u : 0u);
+                                umma_pair_ss(dst, sdesc_at(dq, sub * kSubBytes + kk * 32),
+                                             sdesc_at(dk, sub * (kSubBytes / 2) + kk * 32), idS, (c | sub | kk) ? 1u : 0u);
                     } else {
+                        const uint64_t dq = sdesc_at(dQk, C::kSubs * c * kSubBytes);
+                        const uint64_t dk = PAGED ? sdesc_sw128(kslot, 16, C::kPagedGroupStride) : sdesc_sw128(kslot, 16, 1024);
+#pragma unroll
                         for (int sub = 0; sub < C::kSubs; ++sub)
+#pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t ad =
-                                    sdesc_sw128(sQ + (C::kSubs * c + sub) * kSubBytes + kk * 32, 16, 1024);
-                                const uint64_t bd =
-                                    PAGED ? sdesc_sw128(kslot + sub * 1024 + kk * 32, 16, C::kPagedGroupStride)
-                                          : sdesc_sw128(kslot + sub * kSubBytes + kk * 32, 16, 1024);
+                                const uint64_t ad = sdesc_at(dq, sub * kSubBytes + kk * 32);
+                                const uint64_t bd = sdesc_at(dk, (PAGED ? sub * 1024 : sub * kSubBytes) + kk * 32);
                                 umma_bf16_ss(dst, ad, bd, idS, (c | sub | kk) ? 1u : 0u);
                             }
                     }
@@ -441,10 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vslot = sSlots + slot * C::kSlotBytes;
                     // P of step j, packed bf16 pairs: keys 64 hf .. 64 hf + 63 at columns 64 hf .. 64 hf + 31
                     const uint32_t tP = tS0 + (j % C::kSBuf) * 128;
+                    const uint64_t dv = PAGED ? sdesc_sw128(vslot, 1024, C::kPagedGroupStride) : sdesc_sw128(vslot, kSubBytes, 1024);
+#pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {  // 16 keys per step
-                        const uint64_t bd =
-                            PAGED ? sdesc_sw128(vslot + kk * 2 * C::kPagedGroupStride, 1024, C::kPagedGroupStride)
-                                  : sdesc_sw128(vslot + kk * 2048, kSubBytes, 1024);
+                        const uint64_t bd = sdesc_at(dv, PAGED ? kk * 2 * C::kPagedGroupStride : kk * 2048);
                         if (PAIR)
                             umma_pair_ts(tO, tP + (kk >> 2) * 64 + (kk & 3) * 8, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
                         else

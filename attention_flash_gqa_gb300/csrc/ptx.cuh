@@ -435,6 +435,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     d |= (uint64_t)2 << 61;
     return d;
 }
+// The descriptor of the same view `bytes` further on: sdesc_sw128(a + bytes, ...) ==
+// sdesc_sw128(a, ...) + bytes / 16 whenever a + bytes stays below 256 KB (every shared-memory
+// address here does), since the start-address field then takes no carry. One add instead of
+// rebuilding the descriptor, in the MMA issuers' inner loops.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base_desc, uint32_t bytes) { return base_desc + (bytes >> 4); }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator:
 // D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12) = 1,
