@@ -153,3 +153,30 @@ def test_decode_window_head_blocks_group8(orc, window):
     """A GQA group of 8 at head_dim 128 (KV heads in blocks of 4) with a sliding window."""
     pp = synth.paged_from_lengths(LENS, 64, 8, 128, page_size=16, num_pages=512, seed=window, max_pages=160)
     compare(orc, pp, window)
+
+
+def test_decode_back_to_back_with_q_rewritten_between(orc):
+    """Three decode calls on one stream sharing one workspace, with an ordinary kernel (a torch
+    copy) rewriting q before each call. Each decode grid may launch while the previous call's
+    merge still runs, so it must wait for that merge before it reads q or writes the partials the
+    merge still reads. Every output matches the oracle for the q it was given."""
+    pps = [synth.paged_from_lengths([900, 1, 0, 513, 40, 2048, 77, 16], 32, 8, 128, num_pages=640, seed=s,
+                                    max_pages=130) for s in (11, 12, 13)]
+    base = pps[0]
+    kc, vc = to_dev(base.k_cache), to_dev(base.v_cache)
+    bt, sl = torch.from_numpy(base.block_table).cuda(), torch.from_numpy(base.seq_lens).cuda()
+    qs = [to_dev(p.q) for p in pps]
+    q = torch.empty_like(qs[0])
+    ws = torch.empty(attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, base.B, base.Hq, base.Hkv, 0, base.D),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for i in range(3):
+        q.copy_(qs[i])  # an ordinary kernel on the same stream, just before the call
+        o, lse = attn.attn_decode_paged(q, kc, vc, bt, sl, scale=base.scale, workspace=ws)
+        outs.append((o, lse))
+    torch.cuda.synchronize()
+    assert attn.attn_get_device_status() == 0
+    for p, (o, lse) in zip(pps, outs):
+        ro, rl = orc.decode_paged(p.q, base.k_cache, base.v_cache, base.block_table, base.seq_lens, base.scale)
+        check("o", to_np(o), ro)
+        check_lse("lse", to_np(lse), rl)
