@@ -62,10 +62,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // sub-tiles in place (they are the newest slots, so holding them cannot block the strictly
 // ordered ring); the slice's Q sub-tiles, needed only after the elementwise step, are streamed
 // a second time for dK (held from the S^T stream they would block the ring when it wraps).
-// Sliced, the readout adds each dQ row straight from registers into the fp32 accumulator with
-// vector reductions (red.global.add.v4.f32) instead of staging it for TMA reduce-adds: the 16 KB
-// staging buffer becomes an eighth ring slot, and the ring's capacity is what bounds this mode
-// (measured: 3.29 against 3.35 ms for the window workload's backward).
+// Sliced, one 16 KB dQ staging buffer sits beside a 7-slot ring. (Adding each dQ row straight from
+// registers with vector reductions, red.global.add.v4.f32, and giving the buffer to the ring as an
+// eighth slot measured 2.77 against 2.68 ms for the window workload's backward; two staging
+// buffers and six slots, 2.69 ms.)
 template <int D, int DS>
 struct SmallCfg {
     static constexpr bool SLICED = DS < D;
@@ -73,13 +73,13 @@ struct SmallCfg {
     static constexpr int NSL = D / DS;                    // CTAs per key tile
     static constexpr uint32_t kTile = NSUB * kSub;        // a whole [128 x D] tile
     static constexpr uint32_t kSlot = SLICED ? kSub : kTile;  // ring slot: a sub-tile (sliced) or a tile
-    static constexpr int kStages = SLICED ? 8 : D == 128 ? 3 : 8;
-    static constexpr int NSTAGE = SLICED ? 0 : 2;         // dQ staging buffers
+    static constexpr int kStages = SLICED ? 7 : D == 128 ? 3 : 8;
+    static constexpr int NSTAGE = SLICED ? 1 : 2;         // dQ staging buffers
     static constexpr bool ALIAS = DS == 128;              // dQ reuses R1
     static constexpr uint32_t kOffK = 0;                  // K tile, resident
     static constexpr uint32_t kOffV = kOffK + kTile;      // V tile, resident (not sliced)
     static constexpr uint32_t kOffDS = kOffV + (SLICED ? 0 : kTile);  // dS^T [128 keys x 128 queries] bf16
-    static constexpr uint32_t kOffStage = kOffDS + 2 * kSub;  // dQ staging, 2 x (128 rows x 32 fp32)
+    static constexpr uint32_t kOffStage = kOffDS + 2 * kSub;  // dQ staging, NSTAGE x (128 rows x 32 fp32)
     static constexpr uint32_t kOffRing = kOffStage + NSTAGE * kSub;
     static constexpr uint32_t kOffVec = kOffRing + kStages * kSlot;  // step's lse2[128], Delta[128]
     static constexpr uint32_t kOffBar = kOffVec + 1024;
@@ -88,7 +88,6 @@ struct SmallCfg {
 };
 
 struct SmallArgs {
-    float* dq_acc;
     const float* lse;
     const float* delta;
     uint16_t *dK, *dV;
@@ -476,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp >= kDrainWarp0) {
         // ------------------------------ dQ readout warps -----------------------------------
-        // dQ(t) rows (queries on lanes): scale and add into the fp32 accumulator, straight from
-        // registers (sliced) or staged 32 columns at a time in shared memory for TMA bulk reduce-adds
+        // dQ(t) rows (queries on lanes): scale, stage 32 columns at a time in shared memory and add
+        // into the fp32 accumulator with TMA bulk reduce-adds
         const bool leader = warp == kDrainWarp0 && lane == 0;
         bool ok = true;
         for (int t = 0; t < n; ++t) {
@@ -501,19 +500,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(smem_u32(dq_free));
-            if constexpr (C::SLICED) {
-                // the row straight into the fp32 accumulator: vector reductions at L2
-                if (ok && q0 + j < L) {
-                    float* dst = a.dq_acc +
-                                 ((size_t)(a.cu_seqlens ? seq_start + q0 + j : (size_t)seq * a.S + q0 + j) * a.Hq + h) * D + c0;
-#pragma unroll
-                    for (int c = 0; c < DS; c += 4)
-                        asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c),
-                                     "f"(__uint_as_float(rq[c]) * f), "f"(__uint_as_float(rq[c + 1]) * f),
-                                     "f"(__uint_as_float(rq[c + 2]) * f), "f"(__uint_as_float(rq[c + 3]) * f)
-                                     : "memory");
-                }
-            } else {
 #pragma unroll
             for (int c4 = 0; c4 < DS / 32; ++c4) {
                 const uint32_t buf = sStage + (c4 % C::NSTAGE) * kSub;
@@ -537,7 +523,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_reduce_add_4d(&tdq, buf, c0 + 32 * c4, h, seq_start + q0, bcoord);
                     bulk_commit_group();
                 }
-            }
             }
             if (!ok) break;
         }
@@ -698,7 +683,7 @@ template <int D>
 cudaError_t launch_bwd_small_main(const BwdLaunch& L, cudaStream_t stream) {
     constexpr int DS = D < 128 ? D : 128;
     SmallArgs a;
-    a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV, a.dq_acc = L.dq_acc;
+    a.lse = L.lse, a.delta = L.delta, a.dK = L.dK, a.dV = L.dV;
     a.cu_seqlens = L.cu_seqlens, a.status = L.status;
     a.Hq = L.Hq, a.Hkv = L.Hkv, a.S = L.S, a.window = L.window, a.T = L.total_rows;
     a.scale = L.scale, a.scale_log2 = L.scale * kLog2e;
