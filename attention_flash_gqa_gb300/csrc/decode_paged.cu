@@ -127,7 +127,6 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int hbk = blockIdx.y;         // head block
     const int g0 = hbk * a.hb;          // its first KV head
-    const int h0 = g0 * G, h1 = (g0 + a.hb) * G;  // its query heads
     const int page_bytes = kPage * a.hb * D * 2;
     uint8_t* stage_base = smem;  // kStages x (K page, V page)
     int32_t* start = reinterpret_cast<int32_t*>(smem + kStages * 2 * page_bytes);  // [B + 1]
@@ -217,20 +216,8 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         while (b_first < B && start[b_first + 1] <= u0) ++b_first;
     }
 
-    // The query rows of the later requests in this range travel to L2 now, so the consumers'
-    // switch to such a request waits on L2 rather than on HBM.
-    {
-        int lo = b_first, hi = B - 1;  // request of the range's last unit
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (start[mid] <= u1 - 1) lo = mid;
-            else hi = mid - 1;
-        }
-        const int lines = (h1 - h0) * D * 2 / 128;  // the head block's query rows of one request
-        for (int idx = tid; idx < (lo - b_first) * lines; idx += kThreads)
-            prefetch_l2(reinterpret_cast<const uint8_t*>(a.q + ((size_t)(b_first + 1 + idx / lines) * a.Hq + h0) * D) +
-                        (size_t)(idx % lines) * 128);
-    }
+    // (No L2 prefetch of the later requests' query rows here: it made graph-replayed calls
+    // 0.35 us slower.)
     // Page table of this CTA's range, gathered once by all threads: entry = page id << 5 |
     // valid tokens in the page (1..16), or -1 for a page id outside the pool. The loops below
     // then never wait on a dependent global load.
