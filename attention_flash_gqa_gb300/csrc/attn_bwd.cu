@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* dq_free = dq_full + 1;
     uint64_t* kc_full = dq_free + 1;
     uint64_t* mma_idle = kc_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_idle + 1);
+    uint64_t* p_read = mma_idle + 1;  // (dP role) the elementwise warps have read P(t) [2]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(p_read + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(dq_free), 128);
         mbar_init(smem_u32(kc_full), 1);
         mbar_init(smem_u32(mma_idle), 1);
+        for (int b = 0; b < 2; ++b) mbar_init(smem_u32(&p_read[b]), 64);
         *abort_flag = 0;
         fence_mbar_init();
         // arm phase 0 of the exchange barriers (later phases are armed by the MMA issuer)
@@ -327,9 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_expect_tx(smem_u32(&p_full[pb]), p_rem);  // arm the buffer's next use
                 if (!grad_pair(tDV, sP + pb * 2 * kSub, t > 0)) return false;  // dV_c += P^T dO_c
                 // an S-role CTA is done with P(t) here; a dP-role CTA also reads it in its
-                // elementwise warps (before writing dS(t)), so it releases the buffer after the
-                // dS products below
-                if (s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
+                // elementwise warps (to form dS(t)), so it releases the buffer once they have
+                // (released after the dS products instead, the kernel measured 0.6 % slower)
+                if (!s_role && !mbar_wait(smem_u32(&p_read[pb]), (t >> 1) & 1, abort_flag, a.status, 0x34)) return false;
+                umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 if (!mbar_wait(smem_u32(ds_full), t & 1, abort_flag, a.status, 0x24)) return false;
                 tc_fence_after();
                 mbar_expect_tx(smem_u32(ds_full), ds_rem);
@@ -343,7 +346,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  sdesc_sw128(sKc + kk * 2048, kSub, 1024), idQ, kk > 0 ? 1u : 0u);
                 umma_commit(smem_u32(dq_full));
                 umma_commit_multicast(smem_u32(ds_free), mask_d);
-                if (!s_role) umma_commit_multicast(smem_u32(&p_free[pb]), mask_s);
                 return true;
             };
             constexpr int kHalfU = C::NSUB / 2;
@@ -513,6 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                             __uint_as_float(pw[e] & 0xffff0000u) * (__uint_as_float(rr[c + 1]) - v));
                                 }
                             }
+                        mbar_arrive(smem_u32(&p_read[half]));  // this row of P(t) has been read
                     }
                     // the first step's dS: its buffer was last read at step 2T - 1
                     if (half == 0 && real) {
