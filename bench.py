@@ -51,7 +51,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # bwd_main_d512: captured at B=1 (half the workload, same per-cluster work) and doubled.
 KERNEL_SOURCES = {"bwd_main_d512": ["attn_bwd.cu", "ptx.cuh", "attn_internal.h"],
                   "fwd_d512": ["attn_fwd.cu", "ptx.cuh", "attn_internal.h"]}
-TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (2.553221e9 + 1.430890e9), "src": "77d3ce5bfa9f0909"}}
+TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (3.062595e9 + 1.750719e9), "src": "6d153befeb82325a"}}
 
 
 def pairs_causal(S: int, W: int = 0) -> int:
