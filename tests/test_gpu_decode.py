@@ -180,3 +180,25 @@ def test_decode_back_to_back_with_q_rewritten_between(orc):
         ro, rl = orc.decode_paged(p.q, base.k_cache, base.v_cache, base.block_table, base.seq_lens, base.scale)
         check("o", to_np(o), ro)
         check_lse("lse", to_np(lse), rl)
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF])
+def test_decode_long_contexts_over_repeated_calls(orc, fill):
+    """Sixteen requests with long and ragged contexts (several pages per CTA), three calls in a row
+    on one workspace that starts as zeros or as 0xFF bytes: every call writes all of the partials
+    it reads, so whatever the workspace held before does not matter. Every call matches the
+    oracle."""
+    lens = [3000, 17, 2500, 1, 0, 4100, 800, 1601, 2048, 333, 3999, 64, 1200, 16, 2777, 900]
+    pp = synth.paged_from_lengths(lens, 32, 8, 128, num_pages=1600, seed=21, max_pages=260)
+    assert sum((L + 15) // 16 for L in lens) >= 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    q, kc, vc = to_dev(pp.q), to_dev(pp.k_cache), to_dev(pp.v_cache)
+    bt, sl = torch.from_numpy(pp.block_table).cuda(), torch.from_numpy(pp.seq_lens).cuda()
+    ws = torch.full((attn.attn_workspace_size(attn.ATTN_OP_DECODE_PAGED, pp.B, pp.Hq, pp.Hkv, 0, pp.D),), fill,
+                    dtype=torch.uint8, device="cuda")
+    ro, rl = orc.decode_paged(pp.q, pp.k_cache, pp.v_cache, pp.block_table, pp.seq_lens, pp.scale, 0)
+    for _ in range(3):
+        o, lse = attn.attn_decode_paged(q, kc, vc, bt, sl, scale=pp.scale, workspace=ws)
+        torch.cuda.synchronize()
+        assert attn.attn_get_device_status() == 0
+        check("o", to_np(o), ro)
+        check_lse("lse", to_np(lse), rl)
