@@ -62,7 +62,9 @@ struct DecCfg {
     static constexpr int HB = (D == 128 && G == 8) ? 4 : kUnitBytes / (kPage * D * 2);
     static constexpr int CW = WPH * HB;                    // consumer warps
     static constexpr int TPW = 16 / WPH;                   // page tokens per warp
-    static constexpr int kThreads = (CW + 1) * 32;         // + one producer warp
+    // A producer warp of its own, or (packed) none: see the kernel
+    static constexpr bool OWN_PRODUCER = !PACKED;
+    static constexpr int kThreads = (CW + (OWN_PRODUCER ? 1 : 0)) * 32;
     static constexpr int kRowF = D + 4;  // partial row: o[D], m, l, 2 pad floats (float4 alignment)
     static_assert(QD * NL == D, "lanes x dims per lane must cover the head");
     static_assert(CW <= kMaxConsumerWarps, "consumer warps");
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     uint64_t* empty = bars + kStages;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
     int* warp_sums = const_cast<int*>(abort_flag) + 2;  // [8]
+    int* released = warp_sums + 8;                       // [kStages] consumer warps done with a stage
     int32_t* unit_tab = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [kMaxUnits]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             mbar_init(smem_u32(&empty[s]), kConsumerWarps);
         }
         *abort_flag = 0;
+        for (int s = 0; s < kStages; ++s) released[s] = 0;
         fence_mbar_init();
     }
 
@@ -240,8 +244,8 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         const int nt = min(kPage, L - p * kPage);
         return (page << 5) | nt;
     };
-    // The producer warp stages the first units itself and issues their pages at once, so
-    // the copies are in flight while the rest of the table is staged.
+    // Warp 0 stages the first units itself and issues their pages at once, so the copies are in
+    // flight while the rest of the table is staged.
     const int n_pre = min(n_units, kStages);
     // every cached byte is read once per step: evict-first keeps the stream from displacing
     // (or forcing the write-back of) other lines in L2
@@ -264,9 +268,12 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             mbar_arrive(fb);
         }
     };
-    const int rot = (tid + kThreads - kConsumerWarps * 32) % kThreads;  // producer warp stages units 0..31
+    // The warp that issues the first pages (the producer warp, or consumer warp 0 without one)
+    // stages units 0..31 itself
+    constexpr int kFirstWarp = DC::OWN_PRODUCER ? kConsumerWarps : 0;
+    const int rot = (tid + kThreads - kFirstWarp * 32) % kThreads;
     for (int kk = rot; kk < n_units && kk < kMaxUnits; kk += kThreads) unit_tab[kk] = make_entry(kk);
-    if (warp == kConsumerWarps) {
+    if (warp == kFirstWarp) {
         __syncwarp();
         if (lane == 0)
             for (int i = 0; i < n_pre; ++i) issue(i, unit_tab[i]);
@@ -274,25 +281,47 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     __syncthreads();
     auto unit_entry = [&](int kk) -> int32_t { return kk < kMaxUnits ? unit_tab[kk] : make_entry(kk); };
 
-    if (warp == kConsumerWarps) {
-        // ---------------------------- producer ------------------------------------------
-        if (lane == 0) {
-            int i = 0;
-            for (long long u = u0; u < u1; ++u, ++i) {
-                if (i < n_pre) continue;  // issued before the table was staged
-                const int s = i % kStages, r = i / kStages;
-                if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1, abort_flag, a.status, 0x31)) break;
-                issue(i, unit_entry(i));
+    if constexpr (DC::OWN_PRODUCER) {
+        if (warp == kConsumerWarps) {
+            // -------------------------- producer ----------------------------------------
+            if (lane == 0) {
+                int i = 0;
+                for (long long u = u0; u < u1; ++u, ++i) {
+                    if (i < n_pre) continue;  // issued before the table was staged
+                    const int s = i % kStages, r = i / kStages;
+                    if (r > 0 && !mbar_wait(smem_u32(&empty[s]), (r - 1) & 1, abort_flag, a.status, 0x31)) break;
+                    issue(i, unit_entry(i));
+                }
+                // Drain: every issued copy completes before this CTA may exit.
+                const int issued = i;
+                for (int s = 0; s < kStages && s < issued; ++s) {
+                    const int last = s + ((issued - 1 - s) / kStages) * kStages;
+                    mbar_drain(smem_u32(&full[s]), (last / kStages) & 1, a.status, 0x33);
+                }
             }
-            // Drain: every issued copy completes before this CTA may exit.
-            const int issued = i;
-            for (int s = 0; s < kStages && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / kStages) * kStages;
-                mbar_drain(smem_u32(&full[s]), (last / kStages) & 1, a.status, 0x33);
-            }
+            return;
         }
-        return;
     }
+    // Without a producer warp (the packed layout), the consumer warp that releases a stage last
+    // refills it with the unit kStages further on; its wait on the stage's empty barrier, which
+    // every consumer warp arrives on after its reads, orders those reads before the copy. Eight
+    // warps alone put two on each SM scheduler, so a warp may use up to 255 registers; a ninth
+    // warp puts three on one scheduler and caps every warp at 168, where the packed consumer
+    // spills. Measured at the head_dim 128 decode workload: 35.7 against 36.4 us per call. The
+    // other layouts keep their producer warp: the window workload at head_dim 256 took 163.2
+    // against 158.4 us without it.
+    auto release = [&](int i) -> bool {  // consumer warp done with unit i's stage (lane 0)
+        const int s = i % kStages;
+        mbar_arrive(smem_u32(&empty[s]));
+        if constexpr (DC::OWN_PRODUCER) return true;
+        if (atomicAdd(&released[s], 1) != kConsumerWarps - 1) return true;
+        released[s] = 0;
+        const int inext = i + kStages;
+        if (inext >= n_units) return true;
+        if (!mbar_wait(smem_u32(&empty[s]), (i / kStages) & 1, abort_flag, a.status, 0x31)) return false;
+        issue(inext, unit_entry(inext));
+        return true;
+    };
 
     // ---------------------------------- consumers ----------------------------------------
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -522,7 +551,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        bool rel_ok = true;
+        if (lane == 0) rel_ok = release(i);
+        ok = __shfl_sync(0xffffffffu, rel_ok, 0) && ok;
 
         // ---- end of this request inside this CTA: write its partials (o, m, l) -----------
         // The merge kernel that follows this grid combines each request's slots.
@@ -562,6 +593,12 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < QD; ++e) acc_o[hh][e] = 0.f;
         }
+    }
+    // After a give-up, copies issued into the ring may still be landing: let them finish before
+    // the CTA's shared memory is released. (On the normal path every issued copy was waited on.)
+    if (!ok) {
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000ull) __nanosleep(1000);
     }
 }
 
