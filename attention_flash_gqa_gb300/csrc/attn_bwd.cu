@@ -460,31 +460,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c_hi = min(kB - 1, min(qa, L - 1) - k0);
                     const int c_lo = a.window > 0 ? max(0, qa - a.window + 1 - k0) : 0;
                     const bool edge = c_lo > 0 || c_hi < kB - 1;
+                    uint32_t rr[128];
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        uint32_t rr[64];
-                        tmem_ld32(tR + hh * 64 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-                        tmem_ld32(tR + hh * 64 + 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-                        tmem_ld_wait();
-                        if (hh == 1) {
-                            tc_fence_before();
-                            mbar_arrive(smem_u32(r_free));
-                        }
-                        auto p_half = [&](auto masked) {
+                    for (int c = 0; c < 4; ++c)
+                        tmem_ld32(tR + c * 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(&rr[c * 32]));
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    mbar_arrive(smem_u32(r_free));
+                    auto p_row = [&](auto masked) {
 #pragma unroll
-                            for (int c = 0; c < 64; c += 2) {
-                                float p0 = fast_exp2(fmaf(__uint_as_float(rr[c]), a.scale_log2, -v));
-                                float p1 = fast_exp2(fmaf(__uint_as_float(rr[c + 1]), a.scale_log2, -v));
-                                if (decltype(masked)::value) {
-                                    if (hh * 64 + c < c_lo || hh * 64 + c > c_hi) p0 = 0.f;
-                                    if (hh * 64 + c + 1 < c_lo || hh * 64 + c + 1 > c_hi) p1 = 0.f;
-                                }
-                                pk[hh * 32 + c / 2] = pack_bf16x2(p0, p1);
+                        for (int c = 0; c < 128; c += 2) {
+                            float p0 = fast_exp2(fmaf(__uint_as_float(rr[c]), a.scale_log2, -v));
+                            float p1 = fast_exp2(fmaf(__uint_as_float(rr[c + 1]), a.scale_log2, -v));
+                            if (decltype(masked)::value) {
+                                if (c < c_lo || c > c_hi) p0 = 0.f;
+                                if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
                             }
-                        };
-                        if (edge) p_half(std::true_type{});
-                        else p_half(std::false_type{});
-                    }
+                            pk[c / 2] = pack_bf16x2(p0, p1);
+                        }
+                    };
+                    if (edge) p_row(std::true_type{});
+                    else p_row(std::false_type{});
                     // buffer t & 1 was last read at step t - 2
                     if (real && t >= 2)
                         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&p_free[half]), ((t >> 1) - 1) & 1, abort_flag, a.status, 0x2b));
