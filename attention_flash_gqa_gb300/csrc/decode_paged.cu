@@ -91,6 +91,17 @@ struct DecodeArgs {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// d += a b on one warp: a 16 x 16 (row-major), b 16 x 8 (column-major), bf16 in, fp32 out.
+// Fragments: g = lane / 4, c = lane % 4; a = {(g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..), (g+8, 2c+8..)},
+// b = {(2c..2c+1, g), (2c+8.., g)}, d = {(g, 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)}.
+__device__ __forceinline__ void mma_16x8x16_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Clamped length of request b (records a bounds fault for lengths beyond the table).
 __device__ __forceinline__ int req_len(const DecodeArgs& a, int b) {
     int L = a.seq_lens[b];
@@ -355,6 +366,16 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     const int tok0 = TPW * half + NT * sub;     // first page token of this lane's tokens
 
     float qv[G][QD];  // this lane's query dims, loaded when the request changes
+    // packed layout: the scores of a page are one 16 x 8 x 128 product on the tensor cores,
+    // S^T = K_page Q^T (rows: the page's 16 tokens; columns: the group's heads, zero past G).
+    // Its reduction index k runs over the dims in an order of our choosing, the same for both
+    // operands: lane (g, c) of k-step s holds dims 32 (s / 2) + 8 c + 4 (s % 2) + {0, 1} as
+    // k = 2c, 2c+1 and + {2, 3} as k = 2c+8, 2c+9. So a lane's dims for one token are the four
+    // 16-byte chunks 32 j + 8 c .. +7 (j = 0..3) of its row, read as they are stored.
+    const int mg = lane >> 2, mc = lane & 3;  // fragment row group and column pair
+    uint32_t qb[16];                          // query head mg (zero past G), chunk j at [4 j .. 4 j + 3]
+#pragma unroll
+    for (int e = 0; e < 16; ++e) qb[e] = 0u;
     float acc_o[G][QD];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh)
@@ -372,7 +393,15 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         if (b != cur_b) {
             cur_b = b;
             lo_tok = first_token(a, req_len(a, b)) % kPage;
-            if (active) {
+            if (PACKED && active && mg < G) {
+                const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + mg) * D + 8 * mc;
+#pragma unroll
+                for (int jc = 0; jc < 4; ++jc) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * jc);
+                    qb[4 * jc] = w.x, qb[4 * jc + 1] = w.y, qb[4 * jc + 2] = w.z, qb[4 * jc + 3] = w.w;
+                }
+            }
+            if (!PACKED && active) {
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + hh) * D + dim0;
@@ -397,61 +426,102 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         if (active && nt > 0 && tlo < TPW) {
             const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes;
             const uint8_t* vp = kp + page_bytes;
-            // partial scores over this lane's dims: v[t * G + hh] for its NT tokens
-            float v[NVL];
+            if constexpr (PACKED) {
+                // Rows mg and mg + 8 of K: chunk j of a row at byte 64 j + 16 mc. The 8 lanes of a
+                // shared-memory phase hold two rows, whose addresses agree modulo 128 bytes; so
+                // odd rows read the chunks in the order 1, 0, 3, 2 (the phase then covers all
+                // 32 banks once) and are put back in place after the loads.
+                const bool odd = mg & 1;
+                uint32_t ka[2][16];
 #pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2;
-                if constexpr (QD == 8) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(krow);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                    float2 k2[4];
+                for (int rr = 0; rr < 2; ++rr) {
+                    const uint8_t* krow = kp + ((size_t)((mg + 8 * rr) * a.hb + gl) * D) * 2 + 16 * mc;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
-#pragma unroll
-                        for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
-                        v[t * G + hh] = acc.x + acc.y;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(krow + 64 * (q ^ (odd ? 1 : 0)));
+                        ka[rr][4 * q] = w.x, ka[rr][4 * q + 1] = w.y, ka[rr][4 * q + 2] = w.z, ka[rr][4 * q + 3] = w.w;
                     }
-                } else {
-                    const uint2 w = *reinterpret_cast<const uint2*>(krow);
-                    const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
 #pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-                        v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
-                }
-            }
-            // butterfly reduce-scatter over the NL lanes of a token group (offsets NL/2 .. 1):
-            // after KH halvings a lane holds NF values, index (ln >> (log2 NL - KH)) * NF + j;
-            // remaining offsets all-reduce.
-            int count = NVL;
+                    for (int q = 0; q < 4; q += 2)
 #pragma unroll
-            for (int off = NL / 2; off >= 1; off >>= 1) {
-                if (count > 1) {
-                    const int hf = count >> 1;
-                    const bool upper = (lane & off) != 0;
-#pragma unroll
-                    for (int j = 0; j < NVL / 2; ++j) {
-                        if (j < hf) {
-                            const float send = upper ? v[j] : v[hf + j];
-                            const float keep = upper ? v[hf + j] : v[j];
-                            v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t x = ka[rr][4 * q + e], y = ka[rr][4 * q + 4 + e];
+                            ka[rr][4 * q + e] = odd ? y : x;
+                            ka[rr][4 * q + 4 + e] = odd ? x : y;
                         }
-                    }
-                    count = hf;
-                } else {
-                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
                 }
-            }
-            constexpr int LOGNL = PACKED ? 4 : 5;
-            if ((ln & ((1 << (LOGNL - KH)) - 1)) == 0) {
+                float sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int j = 0; j < NF; ++j) {
-                    const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
-                    const int tw = NT * sub + idx / G;               // token within the warp's 8
-                    sc[tw * G + idx % G] = tw < nt && tw >= tlo ? v[j] * a.scale_log2 : -INFINITY;
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int r0 = 4 * (ks >> 1) + 2 * (ks & 1);
+                    mma_16x8x16_bf16(sd, ka[0][r0], ka[1][r0], ka[0][r0 + 1], ka[1][r0 + 1], qb[r0], qb[r0 + 1]);
+                }
+                // sd = S(token mg, heads 2 mc, 2 mc + 1), S(token mg + 8, same heads)
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int tw = mg + 8 * rr;
+                    const bool vis = tw < nt && tw >= tlo;
+#pragma unroll
+                    for (int dh = 0; dh < 2; ++dh)
+                        if (2 * mc + dh < G) sc[tw * G + 2 * mc + dh] = vis ? sd[2 * rr + dh] * a.scale_log2 : -INFINITY;
+                }
+            } else {
+                // partial scores over this lane's dims: v[t * G + hh] for its NT tokens
+                float v[NVL];
+    #pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2;
+                    if constexpr (QD == 8) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(krow);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        float2 k2[4];
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
+    #pragma unroll
+                        for (int hh = 0; hh < G; ++hh) {
+                            float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
+    #pragma unroll
+                            for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
+                            v[t * G + hh] = acc.x + acc.y;
+                        }
+                    } else {
+                        const uint2 w = *reinterpret_cast<const uint2*>(krow);
+                        const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
+    #pragma unroll
+                        for (int hh = 0; hh < G; ++hh)
+                            v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
+                    }
+                }
+                // butterfly reduce-scatter over the NL lanes of a token group (offsets NL/2 .. 1):
+                // after KH halvings a lane holds NF values, index (ln >> (log2 NL - KH)) * NF + j;
+                // remaining offsets all-reduce.
+                int count = NVL;
+    #pragma unroll
+                for (int off = NL / 2; off >= 1; off >>= 1) {
+                    if (count > 1) {
+                        const int hf = count >> 1;
+                        const bool upper = (lane & off) != 0;
+    #pragma unroll
+                        for (int j = 0; j < NVL / 2; ++j) {
+                            if (j < hf) {
+                                const float send = upper ? v[j] : v[hf + j];
+                                const float keep = upper ? v[hf + j] : v[j];
+                                v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                            }
+                        }
+                        count = hf;
+                    } else {
+                        v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+                    }
+                }
+                constexpr int LOGNL = PACKED ? 4 : 5;
+                if ((ln & ((1 << (LOGNL - KH)) - 1)) == 0) {
+    #pragma unroll
+                    for (int j = 0; j < NF; ++j) {
+                        const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
+                        const int tw = NT * sub + idx / G;               // token within the warp's 8
+                        sc[tw * G + idx % G] = tw < nt && tw >= tlo ? v[j] * a.scale_log2 : -INFINITY;
+                    }
                 }
             }
             __syncwarp();
