@@ -22,8 +22,10 @@
 //  * Consumer warps serve one KV head each (two per head on the two halves of the page's
 //    tokens when a warp's registers cannot hold the whole head): each serves all query heads
 //    of the head's GQA group (one K/V row read feeds all of them) with its own running
-//    softmax state. D = 128 with GQA groups up to 4: one warp per head, each half-warp takes
-//    8 of the page's tokens with 8 dims per lane and paired fp32 FMAs. D = 128 with a group
+//    softmax state. D = 128 with GQA groups up to 4: one warp per head; the page's scores
+//    for the whole group are one 16 x 8 x 128 warp-level MMA (bf16 in, fp32 out), and for
+//    P V each half-warp takes 8 of the page's tokens with 8 dims per lane and paired fp32
+//    FMAs. D = 128 with a group
 //    of 8: two warps per head, lane l owns dims 4l..4l+3 of the warp's 8 tokens. D = 256:
 //    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
 //    a butterfly reduce-scatter across the lanes that split a token.
@@ -339,10 +341,10 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     // Every consumer warp serves one KV head for all G query heads of its group (one K/V
     // row read feeds all of them) with its own running softmax state; when two warps share
     // a head (token halves), they are merged like split partials at the end.
-    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): half-warp s
-    //    takes tokens 8s .. 8s+7; lane l owns dims 8 (l % 16) .. +7, so a 16-lane butterfly
-    //    finishes the dot products, and the products use paired fp32 FMAs. The half-warps'
-    //    o accumulators are summed once per request.
+    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): the scores
+    //    are a warp MMA (below). For P V half-warp s takes tokens 8s .. 8s+7, lane l owns
+    //    dims 8 (l % 16) .. +7, and the products use paired fp32 FMAs. The half-warps' o
+    //    accumulators are summed once per request.
     //  * G = 8 (two warps per KV head, 8 tokens each): lane l owns dims 4l .. 4l+3 of the
     //    warp's 8 tokens (32-lane butterfly).
     constexpr bool PACKED = DC::PACKED;
