@@ -55,7 +55,7 @@ constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tok
 // consumer warps.
 template <int G, int D>
 struct DecCfg {
-    static constexpr bool PACKED = D == 128 && G <= 4;
+    static constexpr bool PACKED = D == 128 && G <= 4;  // decode_packed_layout(G, D)
     static constexpr int QD = D == 128 && !PACKED ? 4 : 8;  // dims per lane
     static constexpr int NL = PACKED ? 16 : 32;            // lanes that split one token's dims
     static constexpr int WPH = PACKED ? 1 : 2;             // consumer warps per KV head
@@ -102,6 +102,14 @@ __device__ __forceinline__ void mma_16x8x16_bf16(float (&d)[4], uint32_t a0, uin
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i+7 give the row addresses
+// of matrix i; lane (g, c) receives rows 2c, 2c+1 of column g of each.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
 
 // Clamped length of request b (records a bounds fault for lengths beyond the table).
@@ -272,11 +280,15 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             if (a.nhb == 1) {  // every head: the page is contiguous
                 const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * D;
                 bulk_load_hint(dk, a.kc + off, page_bytes, fb, policy);
-                bulk_load_hint(dv, a.vc + off, page_bytes, fb, policy);
+                if constexpr (!DC::PACKED) bulk_load_hint(dv, a.vc + off, page_bytes, fb, policy);
             } else {  // 16 tokens x hb heads x D of the page
                 tma_load_3d_hint(dk, &tk, fb, 0, g0, (entry >> 5) * kPage, policy);
-                tma_load_3d_hint(dv, &tv, fb, 0, g0, (entry >> 5) * kPage, policy);
+                if constexpr (!DC::PACKED) tma_load_3d_hint(dv, &tv, fb, 0, g0, (entry >> 5) * kPage, policy);
             }
+            // packed layout: V as [64-dim half][head][token][64 dims], 128-byte swizzled (the
+            // 16-byte chunk c of token t's row at chunk c ^ (t % 8)), for the transposed
+            // fragment loads of P V
+            if constexpr (DC::PACKED) tma_load_5d_hint(dv, &tv, fb, 0, 0, g0, 0, entry >> 5, policy);
         } else {
             mbar_arrive(fb);
         }
@@ -383,6 +395,13 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     for (int hh = 0; hh < G; ++hh)
 #pragma unroll
         for (int e = 0; e < QD; ++e) qv[hh][e] = 0.f, acc_o[hh][e] = 0.f;
+    // packed layout: O^T (128 dims x 8 columns) as 8 MMA tiles of 16 dims; lane (mg, mc) holds
+    // dims 16 t + mg (+ 8) of heads 2 mc, 2 mc + 1
+    float acc_t[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc_t[t][e] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G)
 
     int b = b_first;
@@ -550,11 +569,19 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                 // o and l are zero while m_run is -inf
                 const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
                 l_run *= alpha;
+                if constexpr (PACKED) {
+                    // head h's factor sits in lane h (lanes hold head lane % G); columns past G are zero
+                    const float al0 = __shfl_sync(0xffffffffu, alpha, 2 * mc);
+                    const float al1 = __shfl_sync(0xffffffffu, alpha, 2 * mc + 1);
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float al = __shfl_sync(0xffffffffu, alpha, hh);
+                    for (int t = 0; t < 8; ++t) acc_t[t][0] *= al0, acc_t[t][1] *= al1, acc_t[t][2] *= al0, acc_t[t][3] *= al1;
+                } else {
 #pragma unroll
-                    for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
+                    for (int hh = 0; hh < G; ++hh) {
+                        const float al = __shfl_sync(0xffffffffu, alpha, hh);
+#pragma unroll
+                        for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
+                    }
                 }
                 m_run = m_new;
             }
@@ -569,35 +596,34 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             __syncwarp();
             // o update: add this lane's tokens
             if constexpr (PACKED) {
-                // every token of the page visible (the common case): no per-token masking
-                const bool all_valid = nt >= TPW && tlo <= 0;
+                // O^T += V^T P^T: 8 MMAs of 16 dims x 8 columns x the page's 16 tokens. B = P^T
+                // (tokens 2 mc, 2 mc + 1 and + 8, + 9 of head mg; zero past G) in bf16, as the
+                // prefill's P V takes P.
+                uint32_t pb0 = 0u, pb1 = 0u;
+                if (mg < G) {
+                    pb0 = pack_bf16x2(sp[(2 * mc) * G + mg], sp[(2 * mc + 1) * G + mg]);
+                    pb1 = pack_bf16x2(sp[(2 * mc + 8) * G + mg], sp[(2 * mc + 9) * G + mg]);
+                }
+                // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
+                uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+                if (!(nt >= TPW && tlo <= 0)) {
+                    const int t0 = 2 * mc;
+                    vm0 = (t0 < nt && t0 >= tlo ? 0x0000ffffu : 0u) | (t0 + 1 < nt && t0 + 1 >= tlo ? 0xffff0000u : 0u);
+                    vm1 = (t0 + 8 < nt && t0 + 8 >= tlo ? 0x0000ffffu : 0u) | (t0 + 9 < nt && t0 + 9 >= tlo ? 0xffff0000u : 0u);
+                }
+                // A = V^T by transposed loads: lanes 0-7 / 8-15 / 16-23 / 24-31 address tokens 0-7,
+                // 0-7, 8-15, 8-15 at the tile's lower / upper / lower / upper 8 dims. The swizzle puts
+                // the 8 rows of each matrix in 8 different bank groups.
+                const int lt = (lane & 7) + ((lane >> 4) << 3);
+                const int lhi = (lane >> 3) & 1;
+                const uint32_t vrow = smem_u32(vp) + (uint32_t)(gl * kPage + lt) * 128u;
+                const uint32_t vhalf = (uint32_t)a.hb * kPage * 128u;  // the upper 64 dims of every head
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const int tw = NT * sub + t;
-                    const uint4 w = *reinterpret_cast<const uint4*>(vp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2);
-                    // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
-                    const bool valid = all_valid || (tw < nt && tw >= tlo);
-                    const uint32_t ws[4] = {valid ? w.x : 0u, valid ? w.y : 0u, valid ? w.z : 0u, valid ? w.w : 0u};
-                    float2 v2[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) v2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
-                    float pt[G];
-                    if constexpr (G == 4) {
-                        const float4 p4 = *reinterpret_cast<const float4*>(sp + tw * 4);
-                        pt[0] = p4.x, pt[1] = p4.y, pt[2] = p4.z, pt[3] = p4.w;
-                    } else {
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh) pt[hh] = sp[tw * G + hh];
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float2 pp = make_float2(pt[hh], pt[hh]);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float2 o2 = __ffma2_rn(pp, v2[e], make_float2(acc_o[hh][2 * e], acc_o[hh][2 * e + 1]));
-                            acc_o[hh][2 * e] = o2.x, acc_o[hh][2 * e + 1] = o2.y;
-                        }
-                    }
+                for (int t = 0; t < 8; ++t) {
+                    const int ch = 2 * (t & 3) + lhi;  // 16-byte chunk of the tile's 8 dims within their half
+                    uint32_t v0, v1, v2, v3;
+                    ldsm_x4_trans(vrow + (t >> 2) * vhalf + (uint32_t)((ch ^ (lt & 7)) << 4), v0, v1, v2, v3);
+                    mma_16x8x16_bf16(acc_t[t], v0 & vm0, v1 & vm0, v2 & vm1, v3 & vm1, pb0, pb1);
                 }
             } else {
                 const int tmax = nt < 8 ? nt : 8;
@@ -633,20 +659,23 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             // slot of (request b, CTA k, token half): (b + k) * 2 + half
             float* slot = a.part + ((size_t)(b + k) * 2 + half) * a.Hq * kRowF;
             if (active) {
-                if constexpr (PACKED) {
-                    // the two half-warps hold the same dims for different tokens: sum them
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-                        for (int e = 0; e < QD; ++e) acc_o[hh][e] += __shfl_xor_sync(0xffffffffu, acc_o[hh][e], 16);
-                }
                 // the head's sum: its lanes (lane % G) each hold a share
 #pragma unroll
                 for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
+                if constexpr (PACKED) {
+#pragma unroll
+                    for (int dh = 0; dh < 2; ++dh) {
+                        if (2 * mc + dh < G) {
+                            float* row = slot + (size_t)(g * G + 2 * mc + dh) * kRowF;
+#pragma unroll
+                            for (int t = 0; t < 8; ++t) row[16 * t + mg] = acc_t[t][dh], row[16 * t + 8 + mg] = acc_t[t][2 + dh];
+                        }
+                    }
+                }
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float* row = slot + (size_t)(g * G + hh) * kRowF;
-                    if (sub == 0) {
+                    if (!PACKED && sub == 0) {
 #pragma unroll
                         for (int e = 0; e < QD; e += 4)
                             *reinterpret_cast<float4*>(row + dim0 + e) =
@@ -664,6 +693,10 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             for (int hh = 0; hh < G; ++hh)
 #pragma unroll
                 for (int e = 0; e < QD; ++e) acc_o[hh][e] = 0.f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc_t[t][e] = 0.f;
         }
     }
     // After a give-up, copies issued into the ring may still be landing: let them finish before
@@ -801,6 +834,8 @@ size_t decode_smem_bytes(int hb, int D) {
 
 int decode_max_grid() { return 256; }
 int decode_row_floats(int D) { return D + 4; }
+
+bool decode_packed_layout(int G, int D) { return D == 128 && G <= 4; }
 
 int decode_heads_per_unit(int Hkv, int D, int G) {
     int cap = (D == 128 && G == 8) ? 4 : D > 0 ? (int)(kUnitBytes / (kPage * D * 2)) : 1;
