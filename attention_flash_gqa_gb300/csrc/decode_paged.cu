@@ -12,7 +12,8 @@
 //  * A unit is one page (16 tokens) of a block of hb KV heads, 32 KB of K and 32 KB of V
 //    at most (hb = 8 heads at D = 128, 4 at D = 256). When the block is every head the
 //    page is contiguous and K and V are fetched with two untiled TMA bulk copies; otherwise
-//    with two 3-D tensor copies (16 tokens x hb heads x D) into a 3-stage ring. KV-head
+//    with two 3-D tensor copies (16 tokens x hb heads x D) into a 3-stage ring. In the packed
+//    layout below V is always one 5-D tensor copy with the 128-byte swizzle. KV-head
 //    blocks are the grid's y dimension; each block runs the scheme below on its heads.
 //  * With a window only the pages that hold keys of the window are units; tokens of the
 //    window's first page below L-W are masked like the slots past L in the last page.
@@ -23,9 +24,8 @@
 //    tokens when a warp's registers cannot hold the whole head): each serves all query heads
 //    of the head's GQA group (one K/V row read feeds all of them) with its own running
 //    softmax state. D = 128 with GQA groups up to 4: one warp per head; the page's scores
-//    for the whole group are one 16 x 8 x 128 warp-level MMA (bf16 in, fp32 out), and for
-//    P V each half-warp takes 8 of the page's tokens with 8 dims per lane and paired fp32
-//    FMAs. D = 128 with a group
+//    for the whole group are one 16 x 8 x 128 warp-level MMA (bf16 in, fp32 out), and P V
+//    eight 16 x 8 x 16 ones over V copied swizzled (see the consumer). D = 128 with a group
 //    of 8: two warps per head, lane l owns dims 4l..4l+3 of the warp's 8 tokens. D = 256:
 //    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
 //    a butterfly reduce-scatter across the lanes that split a token.
@@ -49,10 +49,9 @@ constexpr int kPage = 16;
 constexpr int kStages = 3;
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tokens x hb heads x D
-// D = 128 with GQA groups up to 4 uses one consumer warp per KV head (8 warps: fewer warps per
-// scheduler, so each thread can hold its 8 query dims and 8 output dims per head in
-// registers); a group of 8, and D = 256, use two warps per head. Every configuration runs 8
-// consumer warps.
+// D = 128 with GQA groups up to 4 uses one consumer warp per KV head, whose products are warp
+// MMAs over the whole page; a group of 8, and D = 256, use two warps per head (fp32 FMAs, the
+// query and output dims of every head in registers). Every configuration runs 8 consumer warps.
 template <int G, int D>
 struct DecCfg {
     static constexpr bool PACKED = D == 128 && G <= 4;  // decode_packed_layout(G, D)
@@ -353,10 +352,8 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     // Every consumer warp serves one KV head for all G query heads of its group (one K/V
     // row read feeds all of them) with its own running softmax state; when two warps share
     // a head (token halves), they are merged like split partials at the end.
-    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): the scores
-    //    are a warp MMA (below). For P V half-warp s takes tokens 8s .. 8s+7, lane l owns
-    //    dims 8 (l % 16) .. +7, and the products use paired fp32 FMAs. The half-warps' o
-    //    accumulators are summed once per request.
+    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): Q K^T and
+    //    P V are warp MMAs (below); the o accumulator is O^T in MMA fragments.
     //  * G = 8 (two warps per KV head, 8 tokens each): lane l owns dims 4l .. 4l+3 of the
     //    warp's 8 tokens (32-lane butterfly).
     constexpr bool PACKED = DC::PACKED;
@@ -367,14 +364,14 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     float* sc = scratch + warp * 2 * TPW * G;  // [TPW * G] scores (log2 domain), index token * G + head
     float* sp = sc + TPW * G;                  // [TPW * G] probabilities
     constexpr int QD = DC::QD;            // dims per lane
-    constexpr int NT = 8;                 // tokens per lane group (half-warp when packed)
+    constexpr int NT = 8;                 // tokens per lane group
     constexpr int NL = DC::NL;            // lanes that split one token's dims
     constexpr int NV = TPW * G;           // (token, head) values of the warp's tokens
     constexpr int NVL = NT * G;           // partial values per lane
     constexpr int NF = NVL >= NL ? NVL / NL : 1;  // finished values per lane after the butterfly
     constexpr int KH = NVL >= NL ? (PACKED ? 4 : 5) : (NVL == 16 ? 4 : (NVL == 8 ? 3 : (NVL == 4 ? 2 : 1)));
     constexpr int NH = NV >= 32 ? NV / 32 : 1;  // values per lane in the softmax layout
-    const int sub = PACKED ? (lane >> 4) : 0;   // half-warp (packed layout)
+    const int sub = PACKED ? (lane >> 4) : 0;   // half-warp (packed layout; unused by its MMAs)
     const int ln = PACKED ? (lane & 15) : lane; // lane within the group that splits a token
     const int dim0 = QD * ln;
     const int tok0 = TPW * half + NT * sub;     // first page token of this lane's tokens
