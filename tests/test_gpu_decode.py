@@ -64,13 +64,18 @@ def test_decode_d128_head_blocks(orc, Hq, Hkv):
     compare(orc, pp, 300)
 
 
-def test_decode_window_unused_tokens_are_never_read(orc):
-    """Tokens before the window and slots past the end hold NaN: neither reaches the result."""
-    pp = synth.paged_from_lengths([40, 100, 17], 8, 4, 256, page_size=16, num_pages=16, seed=5, max_pages=7)
-    W = 37
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 4, 256), (32, 8, 128), (8, 4, 128), (4, 4, 128), (16, 2, 128)])
+@pytest.mark.parametrize("W", [37, 0])
+def test_decode_window_unused_tokens_are_never_read(orc, Hq, Hkv, D, W):
+    """Tokens before the window and slots past the end hold NaN: neither reaches the result. At
+    head_dim 128 with groups up to 4 the page's products are matrix instructions over whole
+    pages, so the NaN rows sit inside the operands and must be masked, not skipped."""
+    pp = synth.paged_from_lengths([40, 100, 17, 16, 1], Hq, Hkv, D, page_size=16, num_pages=24, seed=5 + D + Hq,
+                                  max_pages=7)
     kc, vc = pp.k_cache.copy(), pp.v_cache.copy()
     for b, L in enumerate(pp.seq_lens):
-        for t in list(range(0, max(0, L - W))) + list(range(L, ((L + 15) // 16) * 16)):
+        before = list(range(0, max(0, L - W))) if W > 0 else []
+        for t in before + list(range(L, ((L + 15) // 16) * 16)):
             page = pp.block_table[b, t // 16]
             kc[page, t % 16] = 0x7FC0
             vc[page, t % 16] = 0x7FC0
