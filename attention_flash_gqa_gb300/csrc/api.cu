@@ -177,10 +177,10 @@ bool make_decode_map(CUtensorMap* m, const void* base, int D, int H, int num_pag
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 5-D map over a paged V cache [num_pages, 16, heads, D = 128] viewed as (64 dims, 16 tokens, heads,
-// 2 halves of D, pages); box = 64 x 16 x hb x 2 x 1, the whole page of hb heads. Shared memory gets
-// [half][head][token][64 dims], each token's 128-byte row swizzled by token % 8.
-bool make_decode_v_map(CUtensorMap* m, const void* base, int D, int H, int num_pages, int hb) {
+// 5-D map over a paged K or V cache [num_pages, 16, heads, D = 128] viewed as (64 dims, 16 tokens,
+// heads, 2 halves of D, pages); box = 64 x 16 x hb x 2 x 1, the whole page of hb heads. Shared memory
+// gets [half][head][token][64 dims], each token's 128-byte row swizzled by token % 8.
+bool make_decode_swz_map(CUtensorMap* m, const void* base, int D, int H, int num_pages, int hb) {
     const cuuint64_t row = (cuuint64_t)H * D * 2;
     cuuint64_t dims[5] = {64, 16, (cuuint64_t)H, (cuuint64_t)D / 64, (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {row, (cuuint64_t)D * 2, 128, 16 * row};
@@ -465,11 +465,14 @@ int attn_decode_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_b
     attn::DecodeLaunch L;
     std::memset(&L, 0, sizeof(L));
     const int hb = attn::decode_heads_per_unit(Hkv, D, G), nhb = Hkv / hb;
-    const bool packed = attn::decode_packed_layout(G, D);
-    if (nhb > 1 && !make_decode_map(&L.tk, k_cache, D, Hkv, num_pages, hb)) return ATTN_ERR_LAUNCH;
-    if (packed ? !make_decode_v_map(&L.tv, v_cache, D, Hkv, num_pages, hb)
-               : nhb > 1 && !make_decode_map(&L.tv, v_cache, D, Hkv, num_pages, hb))
+    if (attn::decode_packed_layout(G, D)) {
+        if (!make_decode_swz_map(&L.tk, k_cache, D, Hkv, num_pages, hb) ||
+            !make_decode_swz_map(&L.tv, v_cache, D, Hkv, num_pages, hb))
+            return ATTN_ERR_LAUNCH;
+    } else if (nhb > 1 && (!make_decode_map(&L.tk, k_cache, D, Hkv, num_pages, hb) ||
+                           !make_decode_map(&L.tv, v_cache, D, Hkv, num_pages, hb))) {
         return ATTN_ERR_LAUNCH;
+    }
     L.q = q, L.k_cache = k_cache, L.v_cache = v_cache, L.block_table = block_table, L.seq_lens = seq_lens;
     L.o = o, L.lse = lse, L.status = dev->status;
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -35,7 +35,7 @@ size_t decode_smem_bytes(int hb, int D);
 int decode_max_grid();
 int decode_row_floats(int D);              // floats per (slot, head) partial row
 int decode_heads_per_unit(int Hkv, int D, int G);  // hb: KV heads per unit (divides Hkv)
-bool decode_packed_layout(int G, int D);  // V is copied as [64-dim half][head][token][64], 128-byte swizzled
+bool decode_packed_layout(int G, int D);  // K, V copied as [64-dim half][head][token][64], 128-byte swizzled
 cudaError_t launch_decode_paged(const DecodeLaunch& L, cudaStream_t stream);
 
 // ---- prefill forward ---------------------------------------------------------------------

@@ -23,9 +23,9 @@
 //  * Consumer warps serve one KV head each (two per head on the two halves of the page's
 //    tokens when a warp's registers cannot hold the whole head): each serves all query heads
 //    of the head's GQA group (one K/V row read feeds all of them) with its own running
-//    softmax state. D = 128 with GQA groups up to 4: one warp per head; the page's scores
-//    for the whole group are one 16 x 8 x 128 warp-level MMA (bf16 in, fp32 out), and P V
-//    eight 16 x 8 x 16 ones over V copied swizzled (see the consumer). D = 128 with a group
+//    softmax state. D = 128 with GQA groups up to 4: one warp per head; S = Q K^T and
+//    O += P V over the page are warp-level MMAs with the group's heads as rows, over K and V
+//    copied swizzled, and the softmax stays in registers (see the consumer). D = 128 with a group
 //    of 8: two warps per head, lane l owns dims 4l..4l+3 of the warp's 8 tokens. D = 256:
 //    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
 //    a butterfly reduce-scatter across the lanes that split a token.
@@ -103,8 +103,14 @@ __device__ __forceinline__ void mma_16x8x16_bf16(float (&d)[4], uint32_t a0, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Four 8 x 8 b16 matrices from shared memory, transposed: lanes 8i .. 8i+7 give the row addresses
-// of matrix i; lane (g, c) receives rows 2c, 2c+1 of column g of each.
+// Four 8 x 8 b16 matrices from shared memory: lanes 8i .. 8i+7 give the row addresses of matrix i;
+// lane (g, c) receives columns 2c, 2c+1 of row g of each.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// The same, transposed: lane (g, c) receives rows 2c, 2c+1 of column g of each.
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -276,18 +282,19 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         if (entry >= 0) {
             mbar_expect_tx(fb, 2u * page_bytes);
             const uint32_t dk = smem_u32(stage_base + (size_t)s * 2 * page_bytes), dv = dk + page_bytes;
-            if (a.nhb == 1) {  // every head: the page is contiguous
+            if constexpr (DC::PACKED) {
+                // K and V as [64-dim half][head][token][64 dims], 128-byte swizzled (the 16-byte
+                // chunk c of token t's row at chunk c ^ (t % 8)), for the consumers' matrix loads
+                tma_load_5d_hint(dk, &tk, fb, 0, 0, g0, 0, entry >> 5, policy);
+                tma_load_5d_hint(dv, &tv, fb, 0, 0, g0, 0, entry >> 5, policy);
+            } else if (a.nhb == 1) {  // every head: the page is contiguous
                 const size_t off = (size_t)(entry >> 5) * kPage * a.Hkv * D;
                 bulk_load_hint(dk, a.kc + off, page_bytes, fb, policy);
-                if constexpr (!DC::PACKED) bulk_load_hint(dv, a.vc + off, page_bytes, fb, policy);
+                bulk_load_hint(dv, a.vc + off, page_bytes, fb, policy);
             } else {  // 16 tokens x hb heads x D of the page
                 tma_load_3d_hint(dk, &tk, fb, 0, g0, (entry >> 5) * kPage, policy);
-                if constexpr (!DC::PACKED) tma_load_3d_hint(dv, &tv, fb, 0, g0, (entry >> 5) * kPage, policy);
+                tma_load_3d_hint(dv, &tv, fb, 0, g0, (entry >> 5) * kPage, policy);
             }
-            // packed layout: V as [64-dim half][head][token][64 dims], 128-byte swizzled (the
-            // 16-byte chunk c of token t's row at chunk c ^ (t % 8)), for the transposed
-            // fragment loads of P V
-            if constexpr (DC::PACKED) tma_load_5d_hint(dv, &tv, fb, 0, 0, g0, 0, entry >> 5, policy);
         } else {
             mbar_arrive(fb);
         }
@@ -377,28 +384,27 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     const int tok0 = TPW * half + NT * sub;     // first page token of this lane's tokens
 
     float qv[G][QD];  // this lane's query dims, loaded when the request changes
-    // packed layout: the scores of a page are one 16 x 8 x 128 product on the tensor cores,
-    // S^T = K_page Q^T (rows: the page's 16 tokens; columns: the group's heads, zero past G).
-    // Its reduction index k runs over the dims in an order of our choosing, the same for both
-    // operands: lane (g, c) of k-step s holds dims 32 (s / 2) + 8 c + 4 (s % 2) + {0, 1} as
-    // k = 2c, 2c+1 and + {2, 3} as k = 2c+8, 2c+9. So a lane's dims for one token are the four
-    // 16-byte chunks 32 j + 8 c .. +7 (j = 0..3) of its row, read as they are stored.
-    const int mg = lane >> 2, mc = lane & 3;  // fragment row group and column pair
-    uint32_t qb[16];                          // query head mg (zero past G), chunk j at [4 j .. 4 j + 3]
-#pragma unroll
-    for (int e = 0; e < 16; ++e) qb[e] = 0u;
     float acc_o[G][QD];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh)
 #pragma unroll
         for (int e = 0; e < QD; ++e) qv[hh][e] = 0.f, acc_o[hh][e] = 0.f;
-    // packed layout: O^T (128 dims x 8 columns) as 8 MMA tiles of 16 dims; lane (mg, mc) holds
-    // dims 16 t + mg (+ 8) of heads 2 mc, 2 mc + 1
-    float acc_t[8][4];
+    // Packed layout: per page S = Q K^T and O += P V are warp MMAs (m16n8k16, bf16 in, fp32 out)
+    // with the group's heads as the 16 rows (rows past G are zero). Lane (mg, mc) holds:
+    //  * qa: head mg's query as A fragments, dims 16 s + 2 mc, +1 and 16 s + 8 + 2 mc, +1 of k-step s;
+    //  * the scores of head mg for tokens 2 mc, 2 mc + 1, 8 + 2 mc, 9 + 2 mc, which are exactly the
+    //    A fragment of P for P V, so the softmax runs in registers;
+    //  * oa[n]: head mg's output dims 8 n + 2 mc, +1 (n = 0..15).
+    // m_run and l_run then belong to head mg (l_run: this lane's share of its 16 tokens).
+    const int mg = lane >> 2, mc = lane & 3;
+    uint32_t qa[16];
+    float oa[16][4];
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
+    for (int e = 0; e < 16; ++e) qa[e] = 0u;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc_t[t][e] = 0.f;
+    for (int n8 = 0; n8 < 16; ++n8)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oa[n8][e] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G)
 
     int b = b_first;
@@ -412,11 +418,11 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             cur_b = b;
             lo_tok = first_token(a, req_len(a, b)) % kPage;
             if (PACKED && active && mg < G) {
-                const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + mg) * D + 8 * mc;
+                const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + mg) * D + 2 * mc;
 #pragma unroll
-                for (int jc = 0; jc < 4; ++jc) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(qrow + 32 * jc);
-                    qb[4 * jc] = w.x, qb[4 * jc + 1] = w.y, qb[4 * jc + 2] = w.z, qb[4 * jc + 3] = w.w;
+                for (int ks = 0; ks < 8; ++ks) {
+                    qa[2 * ks] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks);
+                    qa[2 * ks + 1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8);
                 }
             }
             if (!PACKED && active) {
@@ -445,67 +451,101 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
             const uint8_t* kp = stage_base + (size_t)s * 2 * page_bytes;
             const uint8_t* vp = kp + page_bytes;
             if constexpr (PACKED) {
-                // Rows mg and mg + 8 of K: chunk j of a row at byte 64 j + 16 mc. The 8 lanes of a
-                // shared-memory phase hold two rows, whose addresses agree modulo 128 bytes; so
-                // odd rows read the chunks in the order 1, 0, 3, 2 (the phase then covers all
-                // 32 banks once) and are put back in place after the loads.
-                const bool odd = mg & 1;
-                uint32_t ka[2][16];
+                const uint32_t kb = smem_u32(kp), vb = smem_u32(vp);
+                const uint32_t hbytes = (uint32_t)a.hb * kPage * 128u;  // one 64-dim half of every head
+                auto vis = [&](int t) { return t < nt && t >= tlo; };
+                // S = Q K^T: tiles of tokens 0-7 and 8-15. Per k-step one matrix load gives both
+                // tiles' B fragments: lanes 0-7 / 8-15 / 16-23 / 24-31 address tokens 0-7, 0-7,
+                // 8-15, 8-15 at the step's lower / upper / lower / upper 8 dims; the swizzle puts
+                // the 8 rows of each matrix in 8 different bank groups.
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                {
+                    const int lt = (lane & 7) + ((lane >> 4) << 3), lhi = (lane >> 3) & 1;
+                    const uint32_t krow = kb + (uint32_t)(gl * kPage + lt) * 128u;
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const uint8_t* krow = kp + ((size_t)((mg + 8 * rr) * a.hb + gl) * D) * 2 + 16 * mc;
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(krow + 64 * (q ^ (odd ? 1 : 0)));
-                        ka[rr][4 * q] = w.x, ka[rr][4 * q + 1] = w.y, ka[rr][4 * q + 2] = w.z, ka[rr][4 * q + 3] = w.w;
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const int ch = 2 * (ks & 3) + lhi;
+                        uint32_t k0, k1, k2, k3;
+                        ldsm_x4(krow + (ks >> 2) * hbytes + (uint32_t)((ch ^ (lt & 7)) << 4), k0, k1, k2, k3);
+                        mma_16x8x16_bf16(sa, qa[2 * ks], 0u, qa[2 * ks + 1], 0u, k0, k1);
+                        mma_16x8x16_bf16(sb, qa[2 * ks], 0u, qa[2 * ks + 1], 0u, k2, k3);
                     }
-#pragma unroll
-                    for (int q = 0; q < 4; q += 2)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const uint32_t x = ka[rr][4 * q + e], y = ka[rr][4 * q + 4 + e];
-                            ka[rr][4 * q + e] = odd ? y : x;
-                            ka[rr][4 * q + 4 + e] = odd ? x : y;
-                        }
                 }
-                float sd[4] = {0.f, 0.f, 0.f, 0.f};
+                // head mg, tokens 2 mc, 2 mc + 1, 8 + 2 mc, 9 + 2 mc (log2 units; -inf if not visible)
+                const int t0 = 2 * mc;
+                float sv[4] = {sa[0], sa[1], sb[0], sb[1]};
+                bool over = false;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const int r0 = 4 * (ks >> 1) + 2 * (ks & 1);
-                    mma_16x8x16_bf16(sd, ka[0][r0], ka[1][r0], ka[0][r0 + 1], ka[1][r0 + 1], qb[r0], qb[r0 + 1]);
+                for (int e = 0; e < 4; ++e) {
+                    const int tt = t0 + (e & 1) + 8 * (e >> 1);
+                    sv[e] = mg < G && vis(tt) ? sv[e] * a.scale_log2 : -INFINITY;
+                    over |= sv[e] > m_run + 8.f;
                 }
-                // sd = S(token mg, heads 2 mc, 2 mc + 1), S(token mg + 8, same heads)
+                // lazy running max, as in the other layouts: it moves only when a score exceeds
+                // it by more than 8, so p <= 2^8 and most pages need no rescale
+                if (__any_sync(0xffffffffu, over)) {
+                    float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));  // over head mg's 16 tokens
+                    const float m_new = mx > m_run + 8.f ? mx : m_run;
+                    const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
+                    l_run *= alpha;
 #pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int tw = mg + 8 * rr;
-                    const bool vis = tw < nt && tw >= tlo;
+                    for (int n8 = 0; n8 < 16; ++n8) oa[n8][0] *= alpha, oa[n8][1] *= alpha;
+                    m_run = m_new;
+                }
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                float pv[4];
 #pragma unroll
-                    for (int dh = 0; dh < 2; ++dh)
-                        if (2 * mc + dh < G) sc[tw * G + 2 * mc + dh] = vis ? sd[2 * rr + dh] * a.scale_log2 : -INFINITY;
+                for (int e = 0; e < 4; ++e) {
+                    pv[e] = sv[e] == -INFINITY ? 0.f : fast_exp2(sv[e] - m_use);
+                    l_run += pv[e];
+                }
+                // O += P V: A = P (bf16, as the prefill's P V takes it), B = V by transposed matrix
+                // loads, two 8-dim tiles per load: lanes 0-7 / 8-15 / 16-23 / 24-31 address tokens
+                // 0-7, 8-15, 0-7, 8-15 at the lower / lower / upper / upper 8 dims
+                const uint32_t pa0 = pack_bf16x2(pv[0], pv[1]), pa1 = pack_bf16x2(pv[2], pv[3]);
+                // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
+                uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+                if (!(nt >= TPW && tlo <= 0)) {
+                    vm0 = (vis(t0) ? 0x0000ffffu : 0u) | (vis(t0 + 1) ? 0xffff0000u : 0u);
+                    vm1 = (vis(t0 + 8) ? 0x0000ffffu : 0u) | (vis(t0 + 9) ? 0xffff0000u : 0u);
+                }
+                {
+                    const int lt = (lane & 7) + (((lane >> 3) & 1) << 3), lhi = lane >> 4;
+                    const uint32_t vrow = vb + (uint32_t)(gl * kPage + lt) * 128u;
+#pragma unroll
+                    for (int i8 = 0; i8 < 8; ++i8) {
+                        const int ch = 2 * (i8 & 3) + lhi;
+                        uint32_t v0, v1, v2, v3;
+                        ldsm_x4_trans(vrow + (i8 >> 2) * hbytes + (uint32_t)((ch ^ (lt & 7)) << 4), v0, v1, v2, v3);
+                        mma_16x8x16_bf16(oa[2 * i8], pa0, 0u, pa1, 0u, v0 & vm0, v1 & vm1);
+                        mma_16x8x16_bf16(oa[2 * i8 + 1], pa0, 0u, pa1, 0u, v2 & vm0, v3 & vm1);
+                    }
                 }
             } else {
                 // partial scores over this lane's dims: v[t * G + hh] for its NT tokens
                 float v[NVL];
-    #pragma unroll
+#pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2;
                     if constexpr (QD == 8) {
                         const uint4 w = *reinterpret_cast<const uint4*>(krow);
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                         float2 k2[4];
-    #pragma unroll
+#pragma unroll
                         for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
-    #pragma unroll
+#pragma unroll
                         for (int hh = 0; hh < G; ++hh) {
                             float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
-    #pragma unroll
+#pragma unroll
                             for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
                             v[t * G + hh] = acc.x + acc.y;
                         }
                     } else {
                         const uint2 w = *reinterpret_cast<const uint2*>(krow);
                         const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
-    #pragma unroll
+#pragma unroll
                         for (int hh = 0; hh < G; ++hh)
                             v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
                     }
@@ -514,12 +554,12 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                 // after KH halvings a lane holds NF values, index (ln >> (log2 NL - KH)) * NF + j;
                 // remaining offsets all-reduce.
                 int count = NVL;
-    #pragma unroll
+#pragma unroll
                 for (int off = NL / 2; off >= 1; off >>= 1) {
                     if (count > 1) {
                         const int hf = count >> 1;
                         const bool upper = (lane & off) != 0;
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < NVL / 2; ++j) {
                             if (j < hf) {
                                 const float send = upper ? v[j] : v[hf + j];
@@ -534,95 +574,55 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                 }
                 constexpr int LOGNL = PACKED ? 4 : 5;
                 if ((ln & ((1 << (LOGNL - KH)) - 1)) == 0) {
-    #pragma unroll
+#pragma unroll
                     for (int j = 0; j < NF; ++j) {
                         const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
                         const int tw = NT * sub + idx / G;               // token within the warp's 8
                         sc[tw * G + idx % G] = tw < nt && tw >= tlo ? v[j] * a.scale_log2 : -INFINITY;
                     }
                 }
-            }
-            __syncwarp();
-            // softmax layout: lane holds idx = lane + 32*j (head lane % G, token idx / G).
-            // Lazy running max (as in the prefill forward): m_run, shared by the lanes of a head,
-            // moves only when a page's score exceeds it by more than 8 (log2 units), so p <= 2^8
-            // and most pages need neither the max reduction nor a rescale of o and l. l_run is
-            // this lane's share of the head's sum, reduced across the head's lanes per piece.
-            float sv[NH];
-            bool over = false;
+                __syncwarp();
+                // softmax layout: lane holds idx = lane + 32*j (head lane % G, token idx / G).
+                // Lazy running max (as in the prefill forward): m_run, shared by the lanes of a head,
+                // moves only when a page's score exceeds it by more than 8 (log2 units), so p <= 2^8
+                // and most pages need neither the max reduction nor a rescale of o and l. l_run is
+                // this lane's share of the head's sum, reduced across the head's lanes per piece.
+                float sv[NH];
+                bool over = false;
 #pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                const int idx = lane + 32 * j;
-                sv[j] = idx < NV ? sc[idx] : -INFINITY;
-                over |= sv[j] > m_run + 8.f;
-            }
-            if (__any_sync(0xffffffffu, over)) {
-                float mx = -INFINITY;
+                for (int j = 0; j < NH; ++j) {
+                    const int idx = lane + 32 * j;
+                    sv[j] = idx < NV ? sc[idx] : -INFINITY;
+                    over |= sv[j] > m_run + 8.f;
+                }
+                if (__any_sync(0xffffffffu, over)) {
+                    float mx = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < NH; ++j) mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < NH; ++j) mx = fmaxf(mx, sv[j]);
 #pragma unroll
-                for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_new = mx > m_run + 8.f ? mx : m_run;
-                // o and l are zero while m_run is -inf
-                const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
-                l_run *= alpha;
-                if constexpr (PACKED) {
-                    // head h's factor sits in lane h (lanes hold head lane % G); columns past G are zero
-                    const float al0 = __shfl_sync(0xffffffffu, alpha, 2 * mc);
-                    const float al1 = __shfl_sync(0xffffffffu, alpha, 2 * mc + 1);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) acc_t[t][0] *= al0, acc_t[t][1] *= al1, acc_t[t][2] *= al0, acc_t[t][3] *= al1;
-                } else {
+                    for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    const float m_new = mx > m_run + 8.f ? mx : m_run;
+                    // o and l are zero while m_run is -inf
+                    const float alpha = m_run == -INFINITY ? 0.f : fast_exp2(m_run - m_new);
+                    l_run *= alpha;
 #pragma unroll
                     for (int hh = 0; hh < G; ++hh) {
                         const float al = __shfl_sync(0xffffffffu, alpha, hh);
 #pragma unroll
                         for (int e = 0; e < QD; ++e) acc_o[hh][e] *= al;
                     }
+                    m_run = m_new;
                 }
-                m_run = m_new;
-            }
-            const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
 #pragma unroll
-            for (int j = 0; j < NH; ++j) {
-                const int idx = lane + 32 * j;
-                const float pj = sv[j] == -INFINITY ? 0.f : fast_exp2(sv[j] - m_use);
-                if (idx < NV) sp[idx] = pj;
-                l_run += pj;
-            }
-            __syncwarp();
-            // o update: add this lane's tokens
-            if constexpr (PACKED) {
-                // O^T += V^T P^T: 8 MMAs of 16 dims x 8 columns x the page's 16 tokens. B = P^T
-                // (tokens 2 mc, 2 mc + 1 and + 8, + 9 of head mg; zero past G) in bf16, as the
-                // prefill's P V takes P.
-                uint32_t pb0 = 0u, pb1 = 0u;
-                if (mg < G) {
-                    pb0 = pack_bf16x2(sp[(2 * mc) * G + mg], sp[(2 * mc + 1) * G + mg]);
-                    pb1 = pack_bf16x2(sp[(2 * mc + 8) * G + mg], sp[(2 * mc + 9) * G + mg]);
+                for (int j = 0; j < NH; ++j) {
+                    const int idx = lane + 32 * j;
+                    const float pj = sv[j] == -INFINITY ? 0.f : fast_exp2(sv[j] - m_use);
+                    if (idx < NV) sp[idx] = pj;
+                    l_run += pj;
                 }
-                // tokens past the end hold arbitrary bytes: zero them (p is 0 there, but 0 * NaN is not)
-                uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-                if (!(nt >= TPW && tlo <= 0)) {
-                    const int t0 = 2 * mc;
-                    vm0 = (t0 < nt && t0 >= tlo ? 0x0000ffffu : 0u) | (t0 + 1 < nt && t0 + 1 >= tlo ? 0xffff0000u : 0u);
-                    vm1 = (t0 + 8 < nt && t0 + 8 >= tlo ? 0x0000ffffu : 0u) | (t0 + 9 < nt && t0 + 9 >= tlo ? 0xffff0000u : 0u);
-                }
-                // A = V^T by transposed loads: lanes 0-7 / 8-15 / 16-23 / 24-31 address tokens 0-7,
-                // 0-7, 8-15, 8-15 at the tile's lower / upper / lower / upper 8 dims. The swizzle puts
-                // the 8 rows of each matrix in 8 different bank groups.
-                const int lt = (lane & 7) + ((lane >> 4) << 3);
-                const int lhi = (lane >> 3) & 1;
-                const uint32_t vrow = smem_u32(vp) + (uint32_t)(gl * kPage + lt) * 128u;
-                const uint32_t vhalf = (uint32_t)a.hb * kPage * 128u;  // the upper 64 dims of every head
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int ch = 2 * (t & 3) + lhi;  // 16-byte chunk of the tile's 8 dims within their half
-                    uint32_t v0, v1, v2, v3;
-                    ldsm_x4_trans(vrow + (t >> 2) * vhalf + (uint32_t)((ch ^ (lt & 7)) << 4), v0, v1, v2, v3);
-                    mma_16x8x16_bf16(acc_t[t], v0 & vm0, v1 & vm0, v2 & vm1, v3 & vm1, pb0, pb1);
-                }
-            } else {
+                __syncwarp();
+                // o update: add this lane's tokens
                 const int tmax = nt < 8 ? nt : 8;
                 for (int t = tlo > 0 ? tlo : 0; t < tmax; ++t) {  // only the warp's visible tokens
                     const uint8_t* vrow = vp + ((size_t)((TPW * half + t) * a.hb + gl) * D + dim0) * 2;
@@ -655,24 +655,28 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
         if (u + 1 == start[b + 1] || u + 1 == u1) {
             // slot of (request b, CTA k, token half): (b + k) * 2 + half
             float* slot = a.part + ((size_t)(b + k) * 2 + half) * a.Hq * kRowF;
-            if (active) {
+            if (active && PACKED) {
+                // head mg's sum: its 4 lanes each hold a share
+                l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+                l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+                if (mg < G) {
+                    float* row = slot + (size_t)(g * G + mg) * kRowF;
+#pragma unroll
+                    for (int n8 = 0; n8 < 16; ++n8)
+                        *reinterpret_cast<float2*>(row + 8 * n8 + 2 * mc) = make_float2(oa[n8][0], oa[n8][1]);
+                    if (mc == 0) {
+                        row[D] = m_run;
+                        row[D + 1] = l_run;
+                    }
+                }
+            } else if (active) {
                 // the head's sum: its lanes (lane % G) each hold a share
 #pragma unroll
                 for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, off);
-                if constexpr (PACKED) {
-#pragma unroll
-                    for (int dh = 0; dh < 2; ++dh) {
-                        if (2 * mc + dh < G) {
-                            float* row = slot + (size_t)(g * G + 2 * mc + dh) * kRowF;
-#pragma unroll
-                            for (int t = 0; t < 8; ++t) row[16 * t + mg] = acc_t[t][dh], row[16 * t + 8 + mg] = acc_t[t][2 + dh];
-                        }
-                    }
-                }
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float* row = slot + (size_t)(g * G + hh) * kRowF;
-                    if (!PACKED && sub == 0) {
+                    if (sub == 0) {
 #pragma unroll
                         for (int e = 0; e < QD; e += 4)
                             *reinterpret_cast<float4*>(row + dim0 + e) =
@@ -691,9 +695,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                 for (int e = 0; e < QD; ++e) acc_o[hh][e] = 0.f;
 #pragma unroll
-            for (int t = 0; t < 8; ++t)
+            for (int n8 = 0; n8 < 16; ++n8)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc_t[t][e] = 0.f;
+                for (int e = 0; e < 4; ++e) oa[n8][e] = 0.f;
         }
     }
     // After a give-up, copies issued into the ring may still be landing: let them finish before
