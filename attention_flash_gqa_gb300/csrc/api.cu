@@ -111,11 +111,12 @@ bool make_map_f32(CUtensorMap* m, const void* base, int D, int H, int rows, int 
 // chunks of 64 dims, 2 groups of 8 rows, pages); box = 64 x 8 x 2 x 2 x 1: 16 rows x 128 dims of
 // one head of one page (4 KB), the two 64-dim chunks interleaved per 8-row group (D = 64: one
 // chunk, 2 KB).
-bool make_cache_map(CUtensorMap* m, const void* base, int D, int H, int num_pages) {
+bool make_cache_map(CUtensorMap* m, const void* base, int D, int H, int num_pages, int chunks = 0) {
     const cuuint64_t row = (cuuint64_t)H * D * 2;
     cuuint64_t dims[5] = {64, 8, (cuuint64_t)H * D / 64, 2, (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {row, 128, 8 * row, 16 * row};
-    cuuint32_t box[5] = {64, 8, D >= 128 ? 2u : 1u, 2, 1};  // the forward's slot width: 128 (or 64) dims
+    // the forward's slot width, 128 (or 64) dims; a CTA pair's K slot takes 256 (chunks = 4)
+    cuuint32_t box[5] = {64, 8, chunks > 0 ? (cuuint32_t)chunks : D >= 128 ? 2u : 1u, 2, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -392,6 +393,10 @@ int attn_fwd_paged(const attn_bf16* q, const attn_bf16* k_cache, const attn_bf16
     if (!make_map(&L.tq, q, D, Hq, total_q, 1) || !make_cache_map(&L.tk, k_cache, D, Hkv, num_pages) ||
         !make_cache_map(&L.tv, v_cache, D, Hkv, num_pages))
         return ATTN_ERR_LAUNCH;
+    if (D == 512) {  // CTA pairs: each CTA loads 4 pages x 256 columns of a key tile
+        if (!make_cache_map(&L.tk_half, k_cache, D, Hkv, num_pages, 4)) return ATTN_ERR_LAUNCH;
+        L.pair_ok = true;
+    }
     L.o = o, L.lse = lse, L.cu_seqlens = nullptr, L.status = dev->status;
     L.nseq = num_reqs, L.Hq = Hq, L.Hkv = Hkv, L.S = max_q_len, L.D = D, L.total_rows = total_q, L.window = window;
     L.scale = scale;

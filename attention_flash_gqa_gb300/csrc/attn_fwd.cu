@@ -68,6 +68,8 @@ struct FwdCfg {
     static constexpr uint32_t kSmem = kOffBar + 512 + 1024;  // barriers + alignment slack
     // paged slots: the slot's sub-tiles interleaved per 8-row group
     static constexpr uint32_t kPagedGroupStride = 1024 * kSubs;
+    // paged K slots of a pair: 64 keys x 256 columns, four 64-column sub-tiles per 8-row group
+    static constexpr uint32_t kPairPagedKGroupStride = 4096;
     static_assert(kSmem <= 232448, "shared memory");
     static_assert(!PAIR || DQK >= 256, "the CTA pair serves head_dim 256 and 512");
 };
@@ -101,13 +103,16 @@ struct FwdArgs {
 // rows and half of the key tile (64 keys), for P V its own P (tensor memory) and half of the
 // O block's V columns. Each CTA therefore streams half of K and half of V per key step. Both
 // CTAs' copies complete on the even CTA's barriers; the MMA commits are multicast to both; the
-// odd CTA's softmax warps report P ready on the even CTA's barrier.
+// odd CTA's softmax warps report P ready on the even CTA's barrier. Paged and paired, a CTA's
+// K slot is its four pages of the key tile, each one 8 KB box of 16 rows x 256 columns (8-row
+// groups of four 1 KB sub-tile atoms, 4 KB apart); its V slot is the paged V slot of its 128
+// columns. The last tile's V slot, when keys past the end must be zeroed, completes on a
+// barrier of its own CTA instead: each CTA zeroes its rows and reports on the even CTA's vfix.
 template <int DQK, bool PAGED, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                const __grid_constant__ CUtensorMap tv, FwdArgs a) {
     using C = FwdCfg<DQK, PAIR>;
-    static_assert(!(PAGED && PAIR), "the CTA pair serves the dense and varlen forward");
     // ---- which tile ------------------------------------------------------------------
     const int h = blockIdx.x;
     const int seq = blockIdx.y / a.nsplit, split = blockIdx.y % a.nsplit;
@@ -162,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* pv_done = p_full + 3;            // [3]: P V(j) complete
     uint64_t* mma_idle = pv_done + 3;          // 1
     uint64_t* vfix = mma_idle + 1;             // 1 (paged): the last tile's V rows past the end are zeroed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vfix + 1);
+    uint64_t* vtail = vfix + 1;                // 1 (paged pair): this CTA's copy of that V slot landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vtail + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -179,7 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&p_full[b]), PAIR ? 2 * kSoftmaxThreads / 32 : kSoftmaxThreads);
         for (int b = 0; b < 3; ++b) mbar_init(smem_u32(&pv_done[b]), 1);
         mbar_init(smem_u32(mma_idle), 1);
-        mbar_init(smem_u32(vfix), 1);
+        mbar_init(smem_u32(vfix), PAIR ? 2 : 1);
+        mbar_init(smem_u32(vtail), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -224,22 +231,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tq);
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            mbar_expect_tx(smem_u32(q_full), C::kQBytes);
-            for (int c = 0; c < DQK / 64; ++c)
-                tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, seq_start + q0, 0);
+            if (crank == 0) mbar_expect_tx(smem_u32(q_full), (PAIR ? 2 : 1) * C::kQBytes);
+            for (int c = 0; c < DQK / 64; ++c) {
+                if (PAIR) tma_load_4d_pair(sQ + c * kSubBytes, &tq, lead_bar(q_full), c * 64, h, seq_start + q0, 0);
+                else tma_load_4d(sQ + c * kSubBytes, &tq, smem_u32(q_full), c * 64, h, seq_start + q0, 0);
+            }
         }
         int slot = 0, round = 0;
         bool ok = true;
         // one slot = 128 keys x kSlotCols columns: lane i < 8 loads page i's box (16 rows x kSlotCols)
         const int chunk0 = g * (DQK / 64);  // first 64-column chunk of KV head g
-        auto load_slot = [&](const CUtensorMap* map, int col0, int ids, int& used_slot, int& used_round) -> bool {
+        // kind 0: a V slot (lane i < 8: page i, 16 rows x kSlotCols columns); 1: a pair's K slot
+        // (lane i < 4: page 4 crank + i, 16 rows x 256 columns); 2: the last V slot of a pair that
+        // zeroes keys past the end, completing on this CTA's vtail
+        bool vtail_armed = false;
+        auto load_slot = [&](const CUtensorMap* map, int col0, int ids, int kind, int& used_slot, int& used_round) -> bool {
             if (round > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[slot]), (round - 1) & 1, abort_flag,
                                                                  a.status, 0x11)))
                 return false;
-            const uint32_t fb = smem_u32(&full[slot]);
-            if (lane == 0) mbar_expect_tx(fb, C::kSlotBytes);
             const uint32_t dst = sSlots + slot * C::kSlotBytes;
-            if (lane < 8) tma_load_5d(dst + lane * 2 * C::kPagedGroupStride, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
+            if (!PAIR) {
+                const uint32_t fb = smem_u32(&full[slot]);
+                if (lane == 0) mbar_expect_tx(fb, C::kSlotBytes);
+                if (lane < 8) tma_load_5d(dst + lane * 2 * C::kPagedGroupStride, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
+            } else if (kind == 2) {
+                // the even CTA's barrier is armed without bytes: the issuer waits for vfix as well
+                if (lane == 0) {
+                    if (crank == 0) mbar_arrive(smem_u32(&full[slot]));
+                    mbar_expect_tx(smem_u32(vtail), C::kSlotBytes);
+                }
+                vtail_armed = true;
+                __syncwarp();
+                if (lane < 8)
+                    tma_load_5d(dst + lane * 2 * C::kPagedGroupStride, map, smem_u32(vtail), 0, 0, chunk0 + col0 / 64, 0, ids);
+            } else {
+                const uint32_t fb = lead_bar(&full[slot]);
+                if (lane == 0 && crank == 0) mbar_expect_tx(smem_u32(&full[slot]), 2 * C::kSlotBytes);
+                if (kind == 1) {
+                    const int id = __shfl_sync(0xffffffffu, ids, 4 * (int)crank + (lane & 3));
+                    if (lane < 4) tma_load_5d_pair(dst + lane * 2 * C::kPairPagedKGroupStride, map, fb, 0, 0, chunk0 + col0 / 64, 0, id);
+                } else if (lane < 8) {
+                    tma_load_5d_pair(dst + lane * 2 * C::kPagedGroupStride, map, fb, 0, 0, chunk0 + col0 / 64, 0, ids);
+                }
+            }
             used_slot = slot, used_round = round;
             if (++slot == C::kStages) slot = 0, ++round;
             return true;
@@ -248,18 +282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         int k_cur = page_id(t_begin), k_nxt = n > 1 ? page_id(t_begin + 1) : 0;
         int v_cur = k_cur, v_nxt = k_nxt;
         int vs[C::kVChunks], vr[C::kVChunks];
+        int kt = 0, vt = 0;  // next K / V tile to load
         auto load_k = [&]() -> bool {
             int us, ur;
             for (int c = 0; c < C::kQChunks; ++c)
-                if (!load_slot(&tk, c * C::kSlotCols, k_cur, us, ur)) return false;
+                if (!load_slot(&tk, c * (PAIR ? 256 : C::kSlotCols), k_cur, PAIR ? 1 : 0, us, ur)) return false;
             return true;
         };
         auto load_v = [&]() -> bool {
+            const int kind = PAIR && tail_fix && vt == n - 1 ? 2 : 0;
             for (int c = 0; c < C::kVChunks; ++c)
-                if (!load_slot(&tv, dv0 + c * C::kSlotCols, v_cur, vs[c], vr[c])) return false;
+                if (!load_slot(&tv, dv0 + (PAIR ? 128 * (int)crank : 0) + c * C::kSlotCols, v_cur, kind, vs[c], vr[c]))
+                    return false;
             return true;
         };
-        int kt = 0, vt = 0;  // next K / V tile to load
         auto next_k = [&]() {
             ++kt;
             k_cur = k_nxt;
@@ -287,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // zero the rows of keys >= L in the last tile's V slots before their P V (P is 0 there,
             // but 0 * NaN is not 0)
             const int r_valid = L - (t_end - 1) * kBKV;  // 1 .. 127
-            for (int c = 0; ok && c < C::kVChunks; ++c)
+            if (PAIR) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(vtail), 0, abort_flag, a.status, 0x1e));
+            for (int c = 0; !PAIR && ok && c < C::kVChunks; ++c)
                 ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&full[vs[c]]), vr[c] & 1, abort_flag, a.status, 0x1e));
             if (ok) {
                 const int units = (kBQ - r_valid) * 8 * C::kSubs;  // 16-byte pieces of the rows past the end
@@ -301,10 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(vfix));
+                if (lane == 0) {
+                    if (crank == 0) mbar_arrive(smem_u32(vfix));
+                    else mbar_arrive_cluster(lead_bar(vfix));
+                }
             }
         }
-        if (lane == 0) {
+        // pair: the even CTA's barriers count both CTAs' copies (the odd CTA stays until then: the
+        // cluster barrier at the end); a vtail copy was waited for above, or is drained here
+        if (lane == 0 && crank == 0) {
             const int issued = round * C::kStages + slot;
             for (int s = 0; s < C::kStages && s < issued; ++s) {
                 const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
@@ -312,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_drain(smem_u32(q_full), 0, a.status, 0x19);
         }
+        if (PAIR && lane == 0 && vtail_armed) mbar_drain(smem_u32(vtail), 0, a.status, 0x1d);
     } else if (warp == 0) {
         // ------------------------------- TMA producer ----------------------------------
         if (lane == 0) {
@@ -411,14 +454,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < C::kQChunks; ++c) {
                     if (!next_slot()) return false;
                     const uint32_t kslot = sSlots + slot * C::kSlotBytes;
-                    if (PAIR) {  // four sub-tiles of this CTA's 64 keys x 64 columns (8 KB each)
-                        const uint64_t dq = sdesc_at(dQk, 4 * c * kSubBytes), dk = sdesc_sw128(kslot, 16, 1024);
+                    if (PAIR) {  // four sub-tiles of this CTA's 64 keys x 64 columns (8 KB each; paged: interleaved)
+                        const uint64_t dq = sdesc_at(dQk, 4 * c * kSubBytes);
+                        const uint64_t dk = PAGED ? sdesc_sw128(kslot, 16, C::kPairPagedKGroupStride) : sdesc_sw128(kslot, 16, 1024);
 #pragma unroll
                         for (int sub = 0; sub < 4; ++sub)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 umma_pair_ss(dst, sdesc_at(dq, sub * kSubBytes + kk * 32),
-                                             sdesc_at(dk, sub * (kSubBytes / 2) + kk * 32), idS, (c | sub | kk) ? 1u : 0u);
+                                             sdesc_at(dk, (PAGED ? sub * 1024 : sub * (kSubBytes / 2)) + kk * 32), idS,
+                                             (c | sub | kk) ? 1u : 0u);
                     } else {
                         const uint64_t dq = sdesc_at(dQk, C::kSubs * c * kSubBytes);
                         const uint64_t dk = PAGED ? sdesc_sw128(kslot, 16, C::kPagedGroupStride) : sdesc_sw128(kslot, 16, 1024);
@@ -702,14 +747,14 @@ cudaError_t launch_fwd(const FwdLaunch& L, cudaStream_t stream) {
     // 96 KB in a pair. At head_dim 256 the sliding-window workload (about nine key steps per
     // CTA) measured slower in pairs (0.713 against 0.665 ms), the pair's fixed cost outweighing
     // the halved stream, so 256 keeps single CTAs.
-    const bool pair = !paged && L.pair_ok && (L.Hq / L.Hkv) % 2 == 0 && L.D == 512;
+    const bool pair = L.pair_ok && (L.Hq / L.Hkv) % 2 == 0 && L.D == 512;
     if (L.D == 64) return paged ? launch_fwd_t<64, true, false>(L, stream) : launch_fwd_t<64, false, false>(L, stream);
     if (L.D == 128) return paged ? launch_fwd_t<128, true, false>(L, stream) : launch_fwd_t<128, false, false>(L, stream);
     if (L.D == 256)
         return paged ? launch_fwd_t<256, true, false>(L, stream)
                      : pair ? launch_fwd_t<256, false, true>(L, stream) : launch_fwd_t<256, false, false>(L, stream);
     if (L.D == 512)
-        return paged ? launch_fwd_t<512, true, false>(L, stream)
+        return paged ? (pair ? launch_fwd_t<512, true, true>(L, stream) : launch_fwd_t<512, true, false>(L, stream))
                      : pair ? launch_fwd_t<512, false, true>(L, stream) : launch_fwd_t<512, false, false>(L, stream);
     return cudaErrorInvalidValue;
 }
