@@ -51,7 +51,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # bwd_main_d512: captured at B=1 (half the workload, same per-cluster work) and doubled.
 KERNEL_SOURCES = {"bwd_main_d512": ["attn_bwd.cu", "ptx.cuh", "attn_internal.h"],
                   "fwd_d512": ["attn_fwd.cu", "ptx.cuh", "attn_internal.h"]}
-TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (2.760725e9 + 1.602406e9), "src": "b1ef82cca1f88984"}}
+TRAFFIC = {"bwd_main_d512": {"bytes": 2 * (2.675791e9 + 1.553483e9), "src": "4aa4b8e941023f1f"}}
 
 
 def pairs_causal(S: int, W: int = 0) -> int:
