@@ -54,9 +54,10 @@ constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tok
 // query and output dims of every head in registers). Every configuration runs 8 consumer warps.
 template <int G, int D>
 struct DecCfg {
-    static constexpr bool PACKED = D == 128 && G <= 4;  // decode_packed_layout(G, D)
-    static constexpr int QD = D == 128 && !PACKED ? 4 : 8;  // dims per lane
-    static constexpr int NL = PACKED ? 16 : 32;            // lanes that split one token's dims
+    static constexpr bool PACKED = D == 128 && G <= 4;  // decode_packed_layout(G, D): warp MMAs
+    // the fp32-FMA layouts (not packed): dims per lane, and lanes that split one token's dims
+    static constexpr int QD = D == 128 ? 4 : 8;
+    static constexpr int NL = 32;
     static constexpr int WPH = PACKED ? 1 : 2;             // consumer warps per KV head
     // KV heads per unit at most: 32 KB of K per stage, and for a group of 8 at D = 128 half of
     // that, so 8 consumer warps (168 registers each) cover the unit without spilling
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     // row read feeds all of them) with its own running softmax state; when two warps share
     // a head (token halves), they are merged like split partials at the end.
     //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): Q K^T and
-    //    P V are warp MMAs (below); the o accumulator is O^T in MMA fragments.
+    //    P V are warp MMAs (below); the o accumulator is O in MMA fragments.
     //  * G = 8 (two warps per KV head, 8 tokens each): lane l owns dims 4l .. 4l+3 of the
     //    warp's 8 tokens (32-lane butterfly).
     constexpr bool PACKED = DC::PACKED;
@@ -376,12 +377,11 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     constexpr int NV = TPW * G;           // (token, head) values of the warp's tokens
     constexpr int NVL = NT * G;           // partial values per lane
     constexpr int NF = NVL >= NL ? NVL / NL : 1;  // finished values per lane after the butterfly
-    constexpr int KH = NVL >= NL ? (PACKED ? 4 : 5) : (NVL == 16 ? 4 : (NVL == 8 ? 3 : (NVL == 4 ? 2 : 1)));
+    constexpr int KH = NVL >= NL ? 5 : (NVL == 16 ? 4 : (NVL == 8 ? 3 : (NVL == 4 ? 2 : 1)));
     constexpr int NH = NV >= 32 ? NV / 32 : 1;  // values per lane in the softmax layout
-    const int sub = PACKED ? (lane >> 4) : 0;   // half-warp (packed layout; unused by its MMAs)
-    const int ln = PACKED ? (lane & 15) : lane; // lane within the group that splits a token
-    const int dim0 = QD * ln;
-    const int tok0 = TPW * half + NT * sub;     // first page token of this lane's tokens
+    // (the fp32-FMA layouts)
+    const int dim0 = QD * lane;
+    const int tok0 = TPW * half;  // first page token of this warp's tokens
 
     float qv[G][QD];  // this lane's query dims, loaded when the request changes
     float acc_o[G][QD];
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     for (int n8 = 0; n8 < 16; ++n8)
 #pragma unroll
         for (int e = 0; e < 4; ++e) oa[n8][e] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;  // for head (lane % G)
+    float m_run = -INFINITY, l_run = 0.f;  // for head lane % G (packed: head mg)
 
     int b = b_first;
     int i = 0;
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                     }
                 }
                 // butterfly reduce-scatter over the NL lanes of a token group (offsets NL/2 .. 1):
-                // after KH halvings a lane holds NF values, index (ln >> (log2 NL - KH)) * NF + j;
+                // after KH halvings a lane holds NF values, index (lane >> (5 - KH)) * NF + j;
                 // remaining offsets all-reduce.
                 int count = NVL;
 #pragma unroll
@@ -572,12 +572,11 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                         v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
                     }
                 }
-                constexpr int LOGNL = PACKED ? 4 : 5;
-                if ((ln & ((1 << (LOGNL - KH)) - 1)) == 0) {
+                if ((lane & ((1 << (5 - KH)) - 1)) == 0) {
 #pragma unroll
                     for (int j = 0; j < NF; ++j) {
-                        const int idx = (ln >> (LOGNL - KH)) * NF + j;  // t * G + hh within this lane's tokens
-                        const int tw = NT * sub + idx / G;               // token within the warp's 8
+                        const int idx = (lane >> (5 - KH)) * NF + j;  // t * G + hh within this lane's tokens
+                        const int tw = idx / G;                        // token within the warp's 8
                         sc[tw * G + idx % G] = tw < nt && tw >= tlo ? v[j] * a.scale_log2 : -INFINITY;
                     }
                 }
@@ -676,12 +675,10 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     float* row = slot + (size_t)(g * G + hh) * kRowF;
-                    if (sub == 0) {
 #pragma unroll
-                        for (int e = 0; e < QD; e += 4)
-                            *reinterpret_cast<float4*>(row + dim0 + e) =
-                                make_float4(acc_o[hh][e], acc_o[hh][e + 1], acc_o[hh][e + 2], acc_o[hh][e + 3]);
-                    }
+                    for (int e = 0; e < QD; e += 4)
+                        *reinterpret_cast<float4*>(row + dim0 + e) =
+                            make_float4(acc_o[hh][e], acc_o[hh][e + 1], acc_o[hh][e + 2], acc_o[hh][e + 3]);
                     if (lane == hh) {
                         row[D] = m_run;
                         row[D + 1] = l_run;
