@@ -23,12 +23,11 @@
 //  * Consumer warps serve one KV head each (two per head on the two halves of the page's
 //    tokens when a warp's registers cannot hold the whole head): each serves all query heads
 //    of the head's GQA group (one K/V row read feeds all of them) with its own running
-//    softmax state. D = 128 with GQA groups up to 4: one warp per head; S = Q K^T and
+//    softmax state. D = 128 (GQA groups up to 8): one warp per head; S = Q K^T and
 //    O += P V over the page are warp-level MMAs with the group's heads as rows, over K and V
-//    copied swizzled, and the softmax stays in registers (see the consumer). D = 128 with a group
-//    of 8: two warps per head, lane l owns dims 4l..4l+3 of the warp's 8 tokens. D = 256:
-//    two warps per head, lane l owns dims 8l..8l+7. Per-token dot products are finished by
-//    a butterfly reduce-scatter across the lanes that split a token.
+//    copied swizzled, and the softmax stays in registers (see the consumer). D = 256: two
+//    warps per head, lane l owns dims 8l..8l+7 with fp32 FMAs, and per-token dot products are
+//    finished by a butterfly reduce-scatter across the lanes that split a token.
 //  * fp32 online softmax in the log2 domain. Every (CTA, token half) touching a request
 //    leaves unnormalised partials (o, m, l) in the workspace, with no wait of any kind, and
 //    streams on. A second, small kernel merges each request's partials once the decode grid
@@ -49,19 +48,18 @@ constexpr int kPage = 16;
 constexpr int kStages = 3;
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tokens x hb heads x D
-// D = 128 with GQA groups up to 4 uses one consumer warp per KV head, whose products are warp
-// MMAs over the whole page; a group of 8, and D = 256, use two warps per head (fp32 FMAs, the
-// query and output dims of every head in registers). Every configuration runs 8 consumer warps.
+// D = 128 uses one consumer warp per KV head, whose products are warp MMAs over the whole page;
+// D = 256 uses two warps per head (fp32 FMAs, the query and output dims of every head in
+// registers). Every configuration runs 8 consumer warps.
 template <int G, int D>
 struct DecCfg {
-    static constexpr bool PACKED = D == 128 && G <= 4;  // decode_packed_layout(G, D): warp MMAs
+    static constexpr bool PACKED = D == 128 && G <= 8;  // decode_packed_layout(G, D): warp MMAs
     // the fp32-FMA layouts (not packed): dims per lane, and lanes that split one token's dims
     static constexpr int QD = D == 128 ? 4 : 8;
     static constexpr int NL = 32;
     static constexpr int WPH = PACKED ? 1 : 2;             // consumer warps per KV head
-    // KV heads per unit at most: 32 KB of K per stage, and for a group of 8 at D = 128 half of
-    // that, so 8 consumer warps (168 registers each) cover the unit without spilling
-    static constexpr int HB = (D == 128 && G == 8) ? 4 : kUnitBytes / (kPage * D * 2);
+    // KV heads per unit at most: 32 KB of K per stage
+    static constexpr int HB = kUnitBytes / (kPage * D * 2);
     static constexpr int CW = WPH * HB;                    // consumer warps
     static constexpr int TPW = 16 / WPH;                   // page tokens per warp
     // A producer warp of its own, or (packed) none: see the kernel
@@ -360,9 +358,9 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
     // Every consumer warp serves one KV head for all G query heads of its group (one K/V
     // row read feeds all of them) with its own running softmax state; when two warps share
     // a head (token halves), they are merged like split partials at the end.
-    //  * G <= 4 ("packed" layout, one warp per KV head, all 16 tokens of a page): Q K^T and
+    //  * D = 128 ("packed" layout, one warp per KV head, all 16 tokens of a page): Q K^T and
     //    P V are warp MMAs (below); the o accumulator is O in MMA fragments.
-    //  * G = 8 (two warps per KV head, 8 tokens each): lane l owns dims 4l .. 4l+3 of the
+    //  * D = 256 (two warps per KV head, 8 tokens each): lane l owns dims 8l .. 8l+7 of the
     //    warp's 8 tokens (32-lane butterfly).
     constexpr bool PACKED = DC::PACKED;
     constexpr int TPW = DC::TPW;
@@ -833,10 +831,11 @@ size_t decode_smem_bytes(int hb, int D) {
 int decode_max_grid() { return 256; }
 int decode_row_floats(int D) { return D + 4; }
 
-bool decode_packed_layout(int G, int D) { return D == 128 && G <= 4; }
+bool decode_packed_layout(int G, int D) { return D == 128 && G <= 8; }
 
 int decode_heads_per_unit(int Hkv, int D, int G) {
-    int cap = (D == 128 && G == 8) ? 4 : D > 0 ? (int)(kUnitBytes / (kPage * D * 2)) : 1;
+    int cap = D > 0 ? (int)(kUnitBytes / (kPage * D * 2)) : 1;
+    (void)G;
     if (cap < 1) cap = 1;  // head sizes no decode kernel takes: callers reject them, but never divide by 0
     int hb = Hkv < cap ? Hkv : cap;
     if (hb < 1) hb = 1;
