@@ -54,8 +54,8 @@ constexpr int kUnitBytes = 32768;  // K (or V) bytes of one unit at most: 16 tok
 template <int G, int D>
 struct DecCfg {
     static constexpr bool PACKED = D == 128 && G <= 8;  // decode_packed_layout(G, D): warp MMAs
-    // the fp32-FMA layouts (not packed): dims per lane, and lanes that split one token's dims
-    static constexpr int QD = D == 128 ? 4 : 8;
+    // the fp32-FMA layout (head_dim 256): dims per lane, and lanes that split one token's dims
+    static constexpr int QD = 8;
     static constexpr int NL = 32;
     static constexpr int WPH = PACKED ? 1 : 2;             // consumer warps per KV head
     // KV heads per unit at most: 32 KB of K per stage
@@ -66,7 +66,7 @@ struct DecCfg {
     static constexpr bool OWN_PRODUCER = !PACKED;
     static constexpr int kThreads = (CW + (OWN_PRODUCER ? 1 : 0)) * 32;
     static constexpr int kRowF = D + 4;  // partial row: o[D], m, l, 2 pad floats (float4 alignment)
-    static_assert(QD * NL == D, "lanes x dims per lane must cover the head");
+    static_assert(PACKED || QD * NL == D, "lanes x dims per lane must cover the head");
     static_assert(CW <= kMaxConsumerWarps, "consumer warps");
 };
 constexpr int kMaxB = 4096;
@@ -423,19 +423,14 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                     qa[2 * ks + 1] = *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8);
                 }
             }
-            if (!PACKED && active) {
+            if (!PACKED && active) {  // (the FMA layout)
 #pragma unroll
                 for (int hh = 0; hh < G; ++hh) {
                     const uint16_t* qrow = a.q + ((size_t)b * a.Hq + g * G + hh) * D + dim0;
-                    if constexpr (QD == 8) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(qrow);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    const uint4 w = *reinterpret_cast<const uint4*>(qrow);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) qv[hh][2 * e] = bf16_lo(ws[e]), qv[hh][2 * e + 1] = bf16_hi(ws[e]);
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(qrow);
-                        qv[hh][0] = bf16_lo(w.x), qv[hh][1] = bf16_hi(w.x), qv[hh][2] = bf16_lo(w.y), qv[hh][3] = bf16_hi(w.y);
-                    }
+                    for (int e = 0; e < 4; ++e) qv[hh][2 * e] = bf16_lo(ws[e]), qv[hh][2 * e + 1] = bf16_hi(ws[e]);
                 }
             }
         }
@@ -527,25 +522,17 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
                     const uint8_t* krow = kp + ((size_t)((tok0 + t) * a.hb + gl) * D + dim0) * 2;
-                    if constexpr (QD == 8) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(krow);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                        float2 k2[4];
+                    const uint4 w = *reinterpret_cast<const uint4*>(krow);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    float2 k2[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
+                    for (int e = 0; e < 4; ++e) k2[e] = make_float2(bf16_lo(ws[e]), bf16_hi(ws[e]));
 #pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
+                    for (int hh = 0; hh < G; ++hh) {
+                        float2 acc = __fmul2_rn(make_float2(qv[hh][0], qv[hh][1]), k2[0]);
 #pragma unroll
-                            for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
-                            v[t * G + hh] = acc.x + acc.y;
-                        }
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(krow);
-                        const float k0 = bf16_lo(w.x), k1 = bf16_hi(w.x), k2 = bf16_lo(w.y), k3 = bf16_hi(w.y);
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh)
-                            v[t * G + hh] = qv[hh][0] * k0 + qv[hh][1] * k1 + qv[hh][2] * k2 + qv[hh][3] * k3;
+                        for (int e = 1; e < 4; ++e) acc = __ffma2_rn(make_float2(qv[hh][2 * e], qv[hh][2 * e + 1]), k2[e], acc);
+                        v[t * G + hh] = acc.x + acc.y;
                     }
                 }
                 // butterfly reduce-scatter over the NL lanes of a token group (offsets NL/2 .. 1):
@@ -624,15 +611,10 @@ __global__ void __launch_bounds__(DecCfg<G, D>::kThreads, 1)
                 for (int t = tlo > 0 ? tlo : 0; t < tmax; ++t) {  // only the warp's visible tokens
                     const uint8_t* vrow = vp + ((size_t)((TPW * half + t) * a.hb + gl) * D + dim0) * 2;
                     float vv[QD];
-                    if constexpr (QD == 8) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(vrow);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    const uint4 w = *reinterpret_cast<const uint4*>(vrow);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) vv[2 * e] = bf16_lo(ws[e]), vv[2 * e + 1] = bf16_hi(ws[e]);
-                    } else {
-                        const uint2 w = *reinterpret_cast<const uint2*>(vrow);
-                        vv[0] = bf16_lo(w.x), vv[1] = bf16_hi(w.x), vv[2] = bf16_lo(w.y), vv[3] = bf16_hi(w.y);
-                    }
+                    for (int e = 0; e < 4; ++e) vv[2 * e] = bf16_lo(ws[e]), vv[2 * e + 1] = bf16_hi(ws[e]);
 #pragma unroll
                     for (int hh = 0; hh < G; ++hh) {
                         const float pt = sp[t * G + hh];
